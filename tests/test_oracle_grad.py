@@ -1,0 +1,92 @@
+"""Backward of the oracle pinned by central finite differences in fp64 and by torch autograd.
+
+L = sum(y * dy). Top-k selection and capacity ranks are piecewise constant, so the inputs
+are drawn until every token's top-(k+1) logits are separated by more than 1e-2; then a
+step of 1e-6 never changes the routing and the finite differences see only the smooth part.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+
+
+def _inputs(T, d, E, f, k, seed):
+    for s in range(seed, seed + 200):
+        rng = np.random.default_rng(s)
+        inp = dict(x=rng.standard_normal((T, d)), Wg=rng.standard_normal((E, d)) * 0.5,
+                   bg=rng.standard_normal(E) * 0.3,
+                   W1=rng.standard_normal((E, f, d)) * 0.4, b1=rng.standard_normal((E, f)) * 0.2,
+                   W2=rng.standard_normal((E, d, f)) * 0.4, b2=rng.standard_normal((E, d)) * 0.2)
+        if O.topk_gap(O.gate_logits(inp["x"], inp["Wg"], inp["bg"]), k).min() > 1e-2:
+            return inp, rng.standard_normal((T, d))
+    raise RuntimeError("no well-separated draw")
+
+
+def _loss(inp, dy, k, temp, C):
+    return float(np.sum(O.forward(inp, k, temp, C)["y"] * dy))
+
+
+CASES = [  # T, d, E, f, k, temperature, capacity
+    (7, 4, 5, 3, 2, 1.0, 2),
+    (6, 3, 6, 4, 3, 0.4, None),
+    (8, 3, 4, 2, 1, 1.0, 1),
+]
+
+
+@pytest.mark.parametrize("T,d,E,f,k,temp,C", CASES)
+def test_backward_matches_central_differences(T, d, E, f, k, temp, C):
+    inp, dy = _inputs(T, d, E, f, k, seed=T * 100 + k)
+    fwd = O.forward(inp, k, temp, C)
+    if C is not None:
+        assert fwd["n_dropped"] > 0  # the capacity path is exercised
+    g = O.backward(inp, fwd, dy)
+    h = 1e-6
+    names = {"x": "dx", "Wg": "dWg", "bg": "dbg", "W1": "dW1", "b1": "db1", "W2": "dW2", "b2": "db2"}
+    for p, gname in names.items():
+        base = inp[p]
+        fd = np.zeros_like(base)
+        for i in np.ndindex(base.shape):
+            orig = base[i]
+            base[i] = orig + h
+            lp = _loss(inp, dy, k, temp, C)
+            base[i] = orig - h
+            lm = _loss(inp, dy, k, temp, C)
+            base[i] = orig
+            fd[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g[gname], fd, atol=2e-7, rtol=1e-6, err_msg=gname)
+    # gradient w.r.t. the routing weights themselves: dL/dw[t,j] = <dy[t], Yp[row]>
+    w = fwd["w"]
+    for t in range(T):
+        for j in range(k):
+            r = fwd["slot_row"][t, j]
+            ref = 0.0 if r < 0 else float(dy[t] @ fwd["Yp"][r])
+            assert g["dw"][t, j] == pytest.approx(ref, abs=1e-12)
+    assert np.isfinite(w).all()
+
+
+def test_backward_matches_torch_autograd():
+    """Second opinion with a library routine: the same layer in torch fp64 with autograd,
+    top-k and capacity mask taken as given."""
+    T, d, E, f, k, temp, C = 40, 6, 8, 5, 2, 0.7, 8
+    inp, dy = _inputs(T, d, E, f, k, seed=900)
+    fwd = O.forward(inp, k, temp, C)
+    g = O.backward(inp, fwd, dy)
+    tt = {n: torch.tensor(v, requires_grad=True) for n, v in inp.items()}
+    z = tt["x"] @ tt["Wg"].T + tt["bg"]
+    idx = torch.from_numpy(fwd["idx"])
+    w = torch.softmax(torch.gather(z, 1, idx) / temp, dim=1)
+    keep = torch.from_numpy(fwd["slot_row"] >= 0)
+    y = torch.zeros(T, d, dtype=torch.float64)
+    for j in range(k):
+        W1 = tt["W1"][idx[:, j]]
+        b1 = tt["b1"][idx[:, j]]
+        W2 = tt["W2"][idx[:, j]]
+        b2 = tt["b2"][idx[:, j]]
+        h = torch.nn.functional.gelu(torch.einsum("tfd,td->tf", W1, tt["x"]) + b1)
+        ye = torch.einsum("tdf,tf->td", W2, h) + b2
+        y = y + torch.where(keep[:, j:j + 1], w[:, j:j + 1] * ye, torch.zeros_like(ye))
+    (y * torch.from_numpy(dy)).sum().backward()
+    np.testing.assert_allclose(fwd["y"], y.detach().numpy(), atol=1e-12)
+    for p, gname in {"x": "dx", "Wg": "dWg", "bg": "dbg", "W1": "dW1", "b1": "db1", "W2": "dW2", "b2": "db2"}.items():
+        np.testing.assert_allclose(g[gname], tt[p].grad.numpy(), atol=1e-11, err_msg=gname)
