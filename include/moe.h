@@ -1,0 +1,177 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) MoE layer library (libmoe.so): token routing and
+ * expert compute, forward and backward, on one GPU.
+ *
+ * The layer (pages cited by title and section):
+ *   z   = x Wg^T (+ bg)                                   gate linear
+ *   idx = top-k of z per token (ties -> lower expert id)  top-k selection
+ *   w   = softmax(z[idx] / temperature) over the k        routing weights
+ *     "Native MoE training system PithTrain", section 4.1 (PithTrainMoELayer.forward:
+ *     gate, torch.topk, softmax over the selected values); "Expert Parallelism: Scaling
+ *     Mixture-of-Experts Models", section 2.2 (softmax(gate(x)/temperature); hybrid top-8
+ *     pre-selection with soft weights over the 8), section 5.5 (route in FP32).
+ *   counts[e], balance_loss = mean_e (counts[e] - mean(counts))^2
+ *     "PyTorch distributed MoE training", section 3.3 (balance_loss).
+ *   capacity C = ceil(capacity_factor * T * k / E); assignment (t,j) -> e is kept iff
+ *   fewer than C earlier tokens picked e
+ *     PithTrain page, section 4.3 item 1 (capacity, overflow tokens dropped).
+ *   Xp = x rows permuted into expert buckets (token order inside a bucket)
+ *     Expert-Parallelism page, section 4.2 idea 2 (tokens written straight into
+ *     per-expert bucket offsets; one-device form of the sparse dispatch).
+ *   per expert e: A = Xp_e W1_e^T + b1_e, H = GELU(A) (erf form), Yp = H W2_e^T + b2_e
+ *     PyTorch-MoE page, section 3.2 (Expert); PithTrain page, section 4.1 (expert_pool).
+ *   y[t] = sum over kept slots j of w[t,j] Yp[row(t,j)]
+ *     PithTrain page, section 4.1 (output[mask] += expert_output * routing_weight).
+ *   backward of L = sum(y * dy) (+ aux_loss_weight * balance_loss, which has no gradient)
+ *     PithTrain page, section 4.2 (loss.backward()); PyTorch-MoE page, section 4.3
+ *     (aux_loss_weight = 0.01).
+ *
+ * Conventions (every entry point):
+ * - Pointers named as device pointers must point to device memory of the current device;
+ *   host pointers are only the moe_config_t. The caller owns every buffer; the library
+ *   allocates no device memory and keeps no per-call state. Outputs are overwritten.
+ * - All layouts are row-major, dense, following nn.Linear: x [T,d], Wg [E,d], bg [E] fp32,
+ *   W1 [E,d_ff,d], b1 [E,d_ff], W2 [E,d,d_ff], b2 [E,d]. "act" below means the element
+ *   type selected by cfg->dtype: fp32 (MOE_F32) or bf16 (MOE_BF16) for x, weights,
+ *   activations and their gradients. Routing weights, logits and bias gradients are fp32.
+ * - Permuted rows live in expert buckets: bucket e holds rows [offsets[e], offsets[e+1]),
+ *   offsets[e] is a multiple of MOE_ROW_ALIGN, the first kept[e] rows are expert e's tokens
+ *   in ascending token order and the rest of the bucket is padding (row_token = -1, zero
+ *   rows in Xp). Buffers of permuted rows have cfg->rows_capacity rows.
+ * - Calls are asynchronous on `stream` and never synchronise the host (except
+ *   moe_get_error). Nothing that depends on data (counts, offsets) is read back.
+ * - Host-side validation failures return MOE_ERR_INVALID_ARG (bad value, null pointer) or
+ *   MOE_ERR_UNSUPPORTED (valid but not implemented) and launch nothing. A failed launch
+ *   returns MOE_ERR_CUDA. Faults detected on the device (a bounded wait that ran out, an
+ *   index out of range) set a device error word that moe_get_error reports.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,
+    MOE_ERR_UNSUPPORTED = -2,
+    MOE_ERR_CUDA = -3,
+    MOE_ERR_DEVICE_TIMEOUT = -4,
+    MOE_ERR_DEVICE_BOUNDS = -5
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+#define MOE_ROW_ALIGN 128   /* rows per expert bucket are padded to a multiple of this */
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_K 8
+
+typedef struct {
+    /* set by the caller */
+    int32_t T;                 /* tokens, >= 0 */
+    int32_t d;                 /* model dim, >= 1 */
+    int32_t E;                 /* experts, 1..MOE_MAX_EXPERTS */
+    int32_t k;                 /* experts per token, 1..min(E, MOE_MAX_K) */
+    int32_t d_ff;              /* expert hidden dim, >= 1 */
+    float capacity_factor;     /* <= 0: no capacity limit */
+    float temperature;         /* > 0: softmax(z_sel / temperature) */
+    float aux_loss_weight;     /* weight of balance_loss in the reported loss (0.01 on the pages) */
+    int32_t has_gate_bias;     /* 0/1: bg is added to the logits */
+    int32_t dtype;             /* moe_dtype_t */
+    /* derived by moe_config_init */
+    int32_t capacity;          /* ceil(capacity_factor*T*k/E) in double, or INT32_MAX */
+    int32_t rows_capacity;     /* rows of every permuted buffer (Xp, A, H, Yp) */
+} moe_config_t;
+
+/* Validates the caller's fields and fills the derived ones. Must be called before any
+ * other entry point. Errors: MOE_ERR_INVALID_ARG (out-of-range field), MOE_ERR_UNSUPPORTED
+ * (T*k or rows_capacity*max(d,d_ff) beyond 2^31-1). */
+MOE_API moe_status_t moe_config_init(moe_config_t* cfg);
+
+/* Bytes of device scratch (`ws`) the entry points need for this configuration; one buffer
+ * of this size serves every call. Returns 0 for an invalid cfg. Aligned to 256 bytes. */
+MOE_API size_t moe_workspace_bytes(const moe_config_t* cfg);
+
+/* Gate linear + top-k + softmax over the k + expert counts + balance loss.
+ *   x [T,d] act, Wg [E,d] act, bg [E] fp32 (read iff cfg->has_gate_bias, else may be NULL)
+ *   -> idx [T,k] int32 (slot j = j-th largest logit), w [T,k] fp32 (rows sum to 1),
+ *      counts [E] int32 (pre-capacity choices, sum = T*k), balance_loss [1] fp32.
+ * Logits are accumulated in fp32. All pointers are device pointers. */
+MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
+                       int32_t* idx, float* w, int32_t* counts, float* balance_loss,
+                       void* ws, moe_stream_t stream);
+
+/* Capacity, stable counting sort into expert buckets and the gather of x.
+ *   idx [T,k] int32, x [T,d] act
+ *   -> kept [E] int32 (= min(counts, capacity)), offsets [E+1] int32 (bucket starts,
+ *      multiples of MOE_ROW_ALIGN, offsets[E] = rows in use), row_token [rows_capacity]
+ *      int32 (token of each row; -1 on padding; rows >= offsets[E] unspecified),
+ *      slot_row [T,k] int32 (row of assignment (t,j), -1 if dropped), n_dropped [1] int32,
+ *      Xp [rows_capacity, d] act (rows >= offsets[E] unspecified).
+ * Priority for capacity is token order. idx entries must lie in [0,E) and differ within a
+ * token; a violation sets MOE_ERR_DEVICE_BOUNDS on the device. */
+MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const void* x,
+                          int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                          int32_t* n_dropped, void* Xp, void* ws, moe_stream_t stream);
+
+/* Per-expert FFN over the buckets: A = Xp W1_e^T + b1_e, H = GELU(A), Yp = H W2_e^T + b2_e.
+ *   Xp [rows_capacity,d], offsets [E+1] (from moe_dispatch), W1 [E,d_ff,d], b1 [E,d_ff],
+ *   W2 [E,d,d_ff], b2 [E,d] -> A, H [rows_capacity,d_ff], Yp [rows_capacity,d] (all act;
+ *   rows >= offsets[E] untouched). A is kept for the backward. fp32 accumulation. */
+MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* Xp, const int32_t* offsets,
+                            const void* W1, const void* b1, const void* W2, const void* b2,
+                            void* A, void* H, void* Yp, void* ws, moe_stream_t stream);
+
+/* Weighted combine back to token order: y[t] = sum_{j: slot_row[t,j] >= 0} w[t,j] Yp[slot_row[t,j]],
+ * accumulated in fp32; a token whose slots were all dropped gets 0.  y [T,d] act. */
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const int32_t* slot_row,
+                         const float* w, void* y, moe_stream_t stream);
+
+/* Backward of the layer for the gradient seed dy [T,d] act, from the forward's saved tensors.
+ *   inputs : dy, x, Wg, idx, w, offsets, row_token, slot_row, Xp, A, H, Yp, W1, W2 (as above),
+ *            balance_loss [1] (nullable; enters the reported loss only)
+ *   outputs: dx [T,d] act, dWg [E,d] fp32, dW1 [E,d_ff,d] act, db1 [E,d_ff] fp32,
+ *            dW2 [E,d,d_ff] act, db2 [E,d] fp32, dbg [E] fp32 (nullable: gate-bias
+ *            gradient), dw [T,k] fp32 (nullable: gradient of the routing weights),
+ *            loss [1] fp32 (nullable: sum(y*dy) + aux_loss_weight*balance_loss).
+ * Dropped assignments give dw = 0 but still enter their token's softmax Jacobian. Experts
+ * with no kept rows get zero weight and bias gradients. Scratch comes from ws. */
+MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x, const void* Wg,
+                          const int32_t* idx, const float* w, const int32_t* offsets,
+                          const int32_t* row_token, const int32_t* slot_row, const void* Xp,
+                          const void* A, const void* H, const void* Yp, const void* W1,
+                          const void* W2, const float* balance_loss,
+                          void* dx, float* dWg, void* dW1, float* db1, void* dW2, float* db2,
+                          float* dbg, float* dw, float* loss, void* ws, moe_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the current
+ * device: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS; MOE_ERR_CUDA if the
+ * stream reports a CUDA error. */
+MOE_API moe_status_t moe_get_error(moe_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+MOE_API const char* moe_status_str(moe_status_t status);
+
+/* Number of kernels this library has launched in this process (all devices). */
+MOE_API uint64_t moe_kernel_launches(void);
+
+/* Library version string, e.g. "moe-gb300 0.1 sm_103a". */
+MOE_API const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

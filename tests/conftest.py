@@ -18,3 +18,21 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(scope="session")
+def moe_lib():
+    """The built libmoe.so (compiled in-tree if missing or older than its sources)."""
+    from token_routing_gb300 import build as _build
+    _build.build()
+    import token_routing_gb300 as moe
+    moe.load()
+    return moe
+
+
+@pytest.fixture(scope="session")
+def cuda_device(moe_lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    return torch.device("cuda:0")

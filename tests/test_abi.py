@@ -1,0 +1,128 @@
+"""The C ABI library on the host: it builds, loads, exports every symbol include/moe.h
+declares, and validates its arguments before touching a GPU (no compute calls here)."""
+import ctypes
+import math
+
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+
+
+def test_exports_every_declared_symbol(moe_lib):
+    lib = moe_lib.load()
+    names = moe_lib.header_symbols()
+    assert {"moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_backward",
+            "moe_config_init", "moe_workspace_bytes", "moe_get_error", "moe_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.moe_version().decode().startswith("moe-gb300")
+
+
+def test_status_strings(moe_lib):
+    lib = moe_lib.load()
+    for code in (0, -1, -2, -3, -4, -5):
+        s = lib.moe_status_str(code).decode()
+        assert s and s != "unknown status"
+    assert lib.moe_status_str(7).decode() == "unknown status"
+
+
+def _cfg(moe, **kw):
+    base = dict(T=1000, d=256, E=8, k=2, d_ff=512, capacity_factor=1.0, temperature=1.0,
+                aux_loss_weight=0.01, has_gate_bias=0, dtype=moe.MOE_BF16)
+    base.update(kw)
+    return moe.MoeConfig(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(T=-1), dict(d=0), dict(E=0), dict(E=257), dict(k=0),
+                                 dict(k=9, E=16), dict(k=5, E=4), dict(d_ff=0),
+                                 dict(temperature=0.0), dict(temperature=-1.0),
+                                 dict(temperature=float("inf")), dict(dtype=7),
+                                 dict(has_gate_bias=2), dict(capacity_factor=float("nan"))])
+def test_config_init_rejects(moe_lib, bad):
+    c = _cfg(moe_lib, **bad)
+    assert moe_lib.load().moe_config_init(ctypes.byref(c)) == moe_lib.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cf,T,k,E", [(1.0, 8192, 2, 16), (1.25, 16384, 2, 64), (1.0, 32768, 2, 256),
+                                      (1.0, 1001, 2, 8), (0.25, 600, 2, 8), (1.1, 1000, 2, 8),
+                                      (1.3, 777, 3, 7)])
+def test_capacity_matches_oracle(moe_lib, cf, T, k, E):
+    c = _cfg(moe_lib, T=T, k=k, E=E, capacity_factor=cf)
+    assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
+    assert c.capacity == O.capacity(cf, T, k, E)
+
+
+def test_rows_capacity_bounds_every_bucket_layout(moe_lib):
+    for T, k, E, cf in [(1000, 2, 8, 1.0), (1000, 2, 8, 0.0), (5, 1, 256, 0.0), (0, 2, 8, 1.0),
+                        (300, 8, 256, 0.0), (600, 2, 8, 0.25)]:
+        c = _cfg(moe_lib, T=T, k=k, E=E, capacity_factor=cf)
+        assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
+        C = c.capacity
+        n_max = min(T * k, E * C)
+        # worst case: every bucket wastes 127 rows of padding
+        worst = n_max + 127 * min(E, n_max)
+        assert c.rows_capacity >= worst and c.rows_capacity % 128 == 0
+        if cf <= 0:
+            assert C == 2 ** 31 - 1
+
+
+def test_unlimited_capacity_and_empty_batch(moe_lib):
+    c = _cfg(moe_lib, T=0, capacity_factor=0.0)
+    assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
+    assert c.rows_capacity == 0
+    assert moe_lib.load().moe_workspace_bytes(ctypes.byref(c)) > 0
+
+
+def test_workspace_grows_with_tokens(moe_lib):
+    lib = moe_lib.load()
+    sizes = []
+    for T in (100, 1000, 10000):
+        c = _cfg(moe_lib, T=T)
+        assert lib.moe_config_init(ctypes.byref(c)) == 0
+        sizes.append(lib.moe_workspace_bytes(ctypes.byref(c)))
+    assert sizes[0] < sizes[1] < sizes[2] and all(s % 256 == 0 for s in sizes)
+
+
+def test_entry_points_reject_uninitialised_config(moe_lib):
+    lib = moe_lib.load()
+    c = _cfg(moe_lib)  # moe_config_init not called: derived fields are 0
+    p = ctypes.c_void_p(1)
+    assert lib.moe_route(ctypes.byref(c), p, p, None, p, p, p, p, p, None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_bytes(ctypes.byref(c)) == 0
+
+
+def test_entry_points_reject_null_pointers(moe_lib):
+    lib = moe_lib.load()
+    c = _cfg(moe_lib)
+    assert lib.moe_config_init(ctypes.byref(c)) == 0
+    p = ctypes.c_void_p(16)
+    cfg = ctypes.byref(c)
+    inval = moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(cfg, None, p, None, p, p, p, p, p, None) == inval
+    assert lib.moe_dispatch(cfg, p, p, p, p, p, p, None, p, p, None) == inval
+    assert lib.moe_expert_ffn(cfg, p, p, p, p, None, p, p, p, p, p, None) == inval
+    assert lib.moe_combine(cfg, p, None, p, p, None) == inval
+    args = [p] * 26
+    args[19] = None  # dW2
+    assert lib.moe_backward(cfg, *args) == inval
+    c.has_gate_bias = 1
+    c2 = _cfg(moe_lib, has_gate_bias=1)
+    assert lib.moe_config_init(ctypes.byref(c2)) == 0
+    assert lib.moe_route(ctypes.byref(c2), p, p, None, p, p, p, p, p, None) == inval  # bg required
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_compute_call_without_gpu_reports_cuda_error(moe_lib):
+    lib = moe_lib.load()
+    c = _cfg(moe_lib, T=4, d=64, E=4, d_ff=64)
+    assert lib.moe_config_init(ctypes.byref(c)) == 0
+    p = ctypes.c_void_p(256)
+    assert lib.moe_combine(ctypes.byref(c), p, p, p, p, None) == moe_lib.MOE_ERR_CUDA
+
+
+def test_binding_make_config(moe_lib):
+    c = moe_lib.make_config(1000, 256, 8, 2, 512, capacity_factor=1.25, temperature=0.2)
+    assert c.capacity == math.ceil(1.25 * 1000 * 2 / 8)
+    with pytest.raises(moe_lib.MoeError):
+        moe_lib.make_config(10, 16, 4, 5, 16)

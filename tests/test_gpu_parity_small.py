@@ -1,0 +1,166 @@
+"""Stage-by-stage and end-to-end parity of the CUDA layer (through the C ABI) against the
+fp64 oracle, on scaled-down workloads that span several 128-row tiles with ragged tails.
+
+Each stage is fed the oracle's own upstream results (rounded to the storage dtype), so a
+stage is judged on its own arithmetic: dispatch gets the oracle's top-k indices, the FFN
+gets the oracle's permuted rows, the backward gets the oracle's saved forward tensors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+CASES = list(synth.SMALL_CASES) + ["tiny-fp32-fwd"]
+
+
+@pytest.fixture(scope="module")
+def cases():
+    return {}
+
+
+def _prepare(name, cases):
+    if name in cases:
+        return cases[name]
+    cfg = synth.get(name)
+    inp = synth.make_inputs(cfg)
+    npin = P.np_inputs(inp)
+    fwd, bwd = P.oracle_run(cfg, npin, npin["dy"] if cfg.backward else None)
+    cases[name] = (cfg, inp, npin, fwd, bwd)
+    return cases[name]
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_route(name, cases, moe_lib, cuda_device):
+    moe = moe_lib
+    cfg, inp, npin, fwd, _ = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=False)
+    moe.route(c, dev["x"], dev["Wg"], dev["bg"], b)
+    moe.get_error()
+    idx = b["idx"].cpu().numpy()
+    ok = P.nontie_tokens(fwd)
+    assert (idx[ok] == fwd["idx"][ok]).all(), f"{(idx[ok] != fwd['idx'][ok]).any(1).sum()} tokens differ"
+    w = b["w"].cpu().double().numpy()
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-5)
+    P.assert_close("w", w[ok], fwd["w"][ok], P.tol(cfg) if cfg.dtype == "f32" else 1e-4)
+    counts = b["counts"].cpu().numpy()
+    assert (counts == np.bincount(idx.reshape(-1), minlength=cfg.E)).all()
+    if ok.all():
+        assert (counts == fwd["counts"]).all()
+        assert b["balance_loss"].item() == pytest.approx(fwd["balance_loss"], rel=1e-6, abs=1e-6)
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_dispatch_bit_exact(name, cases, moe_lib, cuda_device):
+    moe = moe_lib
+    cfg, inp, npin, fwd, _ = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=False)
+    moe.dispatch(c, P.dev_i32(fwd["idx"]), dev["x"], b)
+    moe.get_error()
+    n = int(fwd["offsets"][-1])
+    assert b["kept"].cpu().tolist() == fwd["kept"].tolist()
+    assert b["offsets"].cpu().tolist() == fwd["offsets"].tolist()
+    assert b["n_dropped"].item() == fwd["n_dropped"]
+    assert (b["slot_row"].cpu().numpy() == fwd["slot_row"]).all()
+    assert (b["row_token"][:n].cpu().numpy() == fwd["row_token"]).all()
+    # the gather is a copy: bit-exact, zero padding rows
+    assert torch.equal(b["Xp"][:n].cpu(), torch.as_tensor(fwd["Xp"]).to(P.act_dtype(cfg)))
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_expert_ffn(name, cases, moe_lib, cuda_device):
+    moe = moe_lib
+    cfg, inp, npin, fwd, _ = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=False)
+    n = int(fwd["offsets"][-1])
+    b["Xp"][:n] = P.dev_act(cfg, fwd["Xp"])
+    offs = P.dev_i32(fwd["offsets"])
+    moe.expert_ffn(c, b["Xp"], offs, dev["W1"], dev["b1"], dev["W2"], dev["b2"], b)
+    moe.get_error()
+    kept_rows = fwd["row_token"] >= 0
+    for key in ("A", "H", "Yp"):
+        P.assert_close(key, P.f64(b[key][:n])[kept_rows], fwd[key][kept_rows], P.tol(cfg))
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_combine(name, cases, moe_lib, cuda_device):
+    moe = moe_lib
+    cfg, inp, npin, fwd, _ = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    b = moe.alloc_buffers(c, backward=False)
+    n = int(fwd["offsets"][-1])
+    b["Yp"][:n] = P.dev_act(cfg, fwd["Yp"])
+    moe.combine(c, b["Yp"], P.dev_i32(fwd["slot_row"]), P.dev_f32(fwd["w"]), b["y"])
+    moe.get_error()
+    P.assert_close("y", P.f64(b["y"]), fwd["y"], P.tol(cfg))
+    dropped_all = (fwd["slot_row"] < 0).all(axis=1)
+    assert (P.f64(b["y"])[dropped_all] == 0).all()
+
+
+@pytest.mark.parametrize("name", [n for n in CASES if synth.get(n).backward])
+def test_backward(name, cases, moe_lib, cuda_device):
+    moe = moe_lib
+    cfg, inp, npin, fwd, bwd = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=True)
+    n = int(fwd["offsets"][-1])
+    b["idx"].copy_(P.dev_i32(fwd["idx"]))
+    b["w"].copy_(P.dev_f32(fwd["w"]))
+    b["offsets"].copy_(P.dev_i32(fwd["offsets"]))
+    b["row_token"][:n] = P.dev_i32(fwd["row_token"])
+    b["slot_row"].copy_(P.dev_i32(fwd["slot_row"]))
+    for key in ("Xp", "A", "H", "Yp"):
+        b[key][:n] = P.dev_act(cfg, fwd[key])
+    b["balance_loss"].fill_(fwd["balance_loss"])
+    moe.backward(c, dev["dy"], dev["x"], dev["Wg"], dev["W1"], dev["W2"], b)
+    moe.get_error()
+    t = P.tol(cfg)
+    P.assert_close("dw", P.f64(b["dw"]), bwd["dw"], t)
+    for key in ("dx", "dWg", "dW1", "db1", "dW2", "db2"):
+        P.assert_close(key, P.f64(b[key]), bwd[key], t)
+    if cfg.gate_bias != "none":
+        P.assert_close("dbg", P.f64(b["dbg"]), bwd["dbg"], t)
+    loss_ref = P.O.layer_loss(fwd, npin["dy"])
+    assert abs(b["loss"].item() - loss_ref) <= t * max(1.0, abs(loss_ref))
+    # experts with no kept rows get exactly zero weight gradients
+    for e in np.nonzero(fwd["kept"] == 0)[0]:
+        assert (b["dW1"][e] == 0).all() and (b["dW2"][e] == 0).all()
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_end_to_end(name, cases, moe_lib, cuda_device):
+    """The whole path on the GPU (route -> dispatch -> FFN -> combine [-> backward])."""
+    moe = moe_lib
+    cfg, inp, npin, fwd, bwd = _prepare(name, cases)
+    c = moe.config_from(cfg)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=cfg.backward)
+    if cfg.backward:
+        moe.forward_backward(c, dev, dev["x"], dev["dy"], b)
+    else:
+        moe.forward(c, dev, dev["x"], b)
+    moe.get_error()
+    idx = b["idx"].cpu().numpy()
+    ok = P.nontie_tokens(fwd)
+    assert (idx[ok] == fwd["idx"][ok]).all()
+    if not (idx == fwd["idx"]).all():
+        pytest.skip(f"{(~ok).sum()} near-tie tokens routed differently; stage tests cover the values")
+    n = int(fwd["offsets"][-1])
+    assert b["offsets"].cpu().tolist() == fwd["offsets"].tolist()
+    assert (b["slot_row"].cpu().numpy() == fwd["slot_row"]).all()
+    assert (b["row_token"][:n].cpu().numpy() == fwd["row_token"]).all()
+    t = P.tol(cfg)
+    P.assert_close("y", P.f64(b["y"]), fwd["y"], t)
+    if cfg.backward:
+        for key in ("dx", "dWg", "dW1", "db1", "dW2", "db2", "dw"):
+            P.assert_close(key, P.f64(b[key]), bwd[key], t)

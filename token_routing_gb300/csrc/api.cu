@@ -1,0 +1,294 @@
+// C ABI of the MoE layer library: argument validation, workspace layout and the order of
+// kernel launches for each entry point. The arithmetic lives in router.cu, dispatch.cu,
+// gemm_tc.cu / gemm_simt.cu and combine.cu.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace moe {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+__device__ int g_err_word;  // one device error word per device (kErrNone / kErrTimeout / kErrBounds)
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    return dev;
+}
+
+int64_t derived_capacity(const moe_config_t& c) {
+    if (!(c.capacity_factor > 0.0f)) return INT32_MAX;
+    const double cap = std::ceil((double)c.capacity_factor * (double)c.T * (double)c.k / (double)c.E);
+    return cap > (double)INT32_MAX ? INT32_MAX : (int64_t)cap;
+}
+
+int64_t derived_rows(const moe_config_t& c, int64_t cap) {
+    const int64_t assignments = (int64_t)c.T * c.k;
+    const int64_t n_max = std::min(assignments, (int64_t)c.E * cap);
+    const int64_t buckets = std::min<int64_t>(c.E, n_max);
+    const int64_t rows = n_max + (int64_t)(MOE_ROW_ALIGN - 1) * buckets;
+    return (rows + MOE_ROW_ALIGN - 1) / MOE_ROW_ALIGN * MOE_ROW_ALIGN;
+}
+
+moe_status_t check_fields(const moe_config_t* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->d < 1 || c->E < 1 || c->E > MOE_MAX_EXPERTS || c->k < 1 ||
+        c->k > MOE_MAX_K || c->k > c->E || c->d_ff < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (!(c->temperature > 0.0f) || !std::isfinite(c->temperature)) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_loss_weight)) return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->has_gate_bias != 0 && c->has_gate_bias != 1) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c->T * c->k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    const int64_t rows = derived_rows(*c, derived_capacity(*c));
+    if (rows > INT32_MAX || rows * (int64_t)std::max(c->d, c->d_ff) > ((int64_t)1 << 40))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// The entry points accept only a config that moe_config_init has filled.
+moe_status_t check_config(const moe_config_t* c) {
+    moe_status_t st = check_fields(c);
+    if (st != MOE_OK) return st;
+    const int64_t cap = derived_capacity(*c);
+    if (c->capacity != cap || c->rows_capacity != derived_rows(*c, cap)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                   \
+    do {                                                \
+        cudaError_t _e = (expr);                        \
+        if (_e != cudaSuccess) return MOE_ERR_CUDA;     \
+    } while (0)
+
+struct BackwardScratch {
+    SortScratch sort;
+    void* dYp;
+    void* dA;
+    void* dXp;
+    float* dw;
+    float* dz;
+    float* lossrow;
+    float* dwg_part;
+};
+
+size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
+    Workspace ws{static_cast<char*>(base), 0};
+    const size_t es = c.dtype == MOE_BF16 ? 2 : 4;
+    const size_t R = (size_t)c.rows_capacity;
+    sort_scratch_take(ws, c, &b->sort);
+    b->dYp = ws.take<char>(R * c.d * es);
+    b->dA = ws.take<char>(R * c.d_ff * es);
+    b->dXp = ws.take<char>(R * c.d * es);
+    b->dw = ws.take<float>((size_t)c.T * c.k + 1);
+    b->dz = ws.take<float>((size_t)c.T * c.k + 1);
+    b->lossrow = ws.take<float>(R + 1);
+    b->dwg_part = ws.take<float>((size_t)c.E * dwg_chunks(c) * c.d);
+    return align_up(ws.used, 256);
+}
+
+bool use_tc(const moe_config_t& c) { return c.dtype == MOE_BF16 && tc_gemm_supported(c); }
+
+cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
+    return use_tc(c) ? launch_row_gemm_tc(c, a, s) : launch_row_gemm_simt(c, a, s);
+}
+cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
+    return use_tc(c) ? launch_wgrad_tc(c, a, s) : launch_wgrad_simt(c, a, s);
+}
+
+}  // namespace
+
+int* device_error_word() {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int num_sms() {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_num_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_num_sms[dev] = n;
+    }
+    return g_num_sms[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_config_init(moe_config_t* cfg) {
+    moe_status_t st = check_fields(cfg);
+    if (st != MOE_OK) return st;
+    const int64_t cap = derived_capacity(*cfg);
+    cfg->capacity = (int32_t)cap;
+    cfg->rows_capacity = (int32_t)derived_rows(*cfg, cap);
+    return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_config_t* cfg) {
+    if (check_config(cfg) != MOE_OK) return 0;
+    BackwardScratch b;
+    return carve_backward(*cfg, nullptr, &b);
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
+                       int32_t* idx, float* w, int32_t* counts, float* balance_loss, void* ws,
+                       moe_stream_t stream) {
+    (void)ws;
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!Wg || !counts || !balance_loss || (cfg->has_gate_bias && !bg)) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!x || !idx || !w)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route(*cfg, x, Wg, bg, idx, w, counts, balance_loss, (cudaStream_t)stream));
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const void* x, int32_t* kept,
+                          int32_t* offsets, int32_t* row_token, int32_t* slot_row, int32_t* n_dropped,
+                          void* Xp, void* ws, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!kept || !offsets || !n_dropped || !ws) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace w{static_cast<char*>(ws), 0};
+    SortScratch srt;
+    sort_scratch_take(w, *cfg, &srt);
+    MOE_TRY(launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s));
+    MOE_TRY(launch_gather(*cfg, x, offsets, row_token, Xp, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* Xp, const int32_t* offsets,
+                            const void* W1, const void* b1, const void* W2, const void* b2, void* A,
+                            void* H, void* Yp, void* ws, moe_stream_t stream) {
+    (void)ws;
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!offsets || !W1 || !b1 || !W2 || !b2) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!Xp || !A || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const moe_config_t& c = *cfg;
+    RowGemmArgs g1{};
+    g1.kind = kGemmFfn1; g1.A = Xp; g1.B = W1; g1.bias = b1; g1.out0 = A; g1.out1 = H;
+    g1.offsets = offsets; g1.E = c.E; g1.N = c.d_ff; g1.K = c.d; g1.rows_capacity = c.rows_capacity;
+    g1.sBe = (long long)c.d_ff * c.d; g1.sBn = c.d; g1.sBk = 1;
+    MOE_TRY(row_gemm(c, g1, s));
+    RowGemmArgs g2{};
+    g2.kind = kGemmFfn2; g2.A = H; g2.B = W2; g2.bias = b2; g2.out0 = Yp;
+    g2.offsets = offsets; g2.E = c.E; g2.N = c.d; g2.K = c.d_ff; g2.rows_capacity = c.rows_capacity;
+    g2.sBe = (long long)c.d * c.d_ff; g2.sBn = c.d_ff; g2.sBk = 1;
+    MOE_TRY(row_gemm(c, g2, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const int32_t* slot_row,
+                         const float* w, void* y, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T > 0 && (!Yp || !slot_row || !w || !y)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(*cfg, Yp, slot_row, w, y, (cudaStream_t)stream));
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x, const void* Wg,
+                          const int32_t* idx, const float* w, const int32_t* offsets,
+                          const int32_t* row_token, const int32_t* slot_row, const void* Xp,
+                          const void* A, const void* H, const void* Yp, const void* W1,
+                          const void* W2, const float* balance_loss, void* dx, float* dWg, void* dW1,
+                          float* db1, void* dW2, float* db2, float* dbg, float* dw, float* loss,
+                          void* ws, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!Wg || !offsets || !W1 || !W2 || !dWg || !dW1 || !db1 || !dW2 || !db2 || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!dy || !x || !idx || !w || !slot_row || !dx)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!row_token || !Xp || !A || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = *cfg;
+    cudaStream_t s = (cudaStream_t)stream;
+    BackwardScratch b;
+    carve_backward(c, ws, &b);
+    float* dwp = dw ? dw : b.dw;
+
+    // combine backward: dYp, dw, per-row loss terms (padding rows of dYp zeroed)
+    MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossrow, s));
+    // experts backward
+    RowGemmArgs gh{};
+    gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = A; gh.out0 = b.dA;
+    gh.offsets = offsets; gh.E = c.E; gh.N = c.d_ff; gh.K = c.d; gh.rows_capacity = c.rows_capacity;
+    gh.sBe = (long long)c.d * c.d_ff; gh.sBn = 1; gh.sBk = c.d_ff;
+    MOE_TRY(row_gemm(c, gh, s));
+    RowGemmArgs gx{};
+    gx.kind = kGemmDX; gx.A = b.dA; gx.B = W1; gx.out0 = b.dXp;
+    gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;
+    gx.sBe = (long long)c.d_ff * c.d; gx.sBn = 1; gx.sBk = c.d;
+    MOE_TRY(row_gemm(c, gx, s));
+    WgradArgs w2{b.dYp, H, dW2, offsets, c.E, c.d, c.d_ff};
+    MOE_TRY(wgrad(c, w2, s));
+    WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
+    MOE_TRY(wgrad(c, w1, s));
+    MOE_TRY(launch_bias_grad(c, b.dYp, c.d, offsets, db2, s));
+    MOE_TRY(launch_bias_grad(c, b.dA, c.d_ff, offsets, db1, s));
+    // router backward: assignment sort, softmax Jacobian, dx, dWg, dbg
+    MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
+    MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
+    MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, dbg, s));
+    if (loss) MOE_TRY(launch_loss(c, b.lossrow, offsets, balance_loss, loss, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_get_error(moe_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    int* p = device_error_word();
+    if (!p) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v != kErrNone) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (v == kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    if (v == kErrBounds) return MOE_ERR_DEVICE_BOUNDS;
+    return MOE_OK;
+}
+
+const char* moe_status_str(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE_BOUNDS: return "index out of range on the device";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_version(void) { return "moe-gb300 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,380 @@
+// Combine (forward), combine backward, router backward + un-permute, gate-weight gradient,
+// bias gradients and the reported loss.
+//
+// "Native MoE training system PithTrain", section 4.1: output[mask] += expert_output *
+// routing_weight (weighted accumulate back to token order); section 4.2: loss.backward().
+// "Expert Parallelism: Scaling Mixture-of-Experts Models", section 2.2: the weights are
+// softmax(z / temperature) over the selected logits, whose Jacobian carries the gradient
+// to the gate. "PyTorch distributed MoE training", section 4.3: aux_loss_weight * balance.
+//
+// All reductions run in a fixed order (no floating-point atomics), so results are
+// bit-reproducible from run to run.
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+// y[t] = sum over kept slots of w[t,j] * Yp[slot_row[t,j]]; one warp per token.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
+               const float* __restrict__ w, int Tn, int d, int k, T* __restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    constexpr int V = Vec16<T>::N;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
+        int rows[MOE_MAX_K];
+        float ws[MOE_MAX_K];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            rows[j] = (j < k) ? slot_row[(size_t)t * k + j] : -1;
+            ws[j] = (j < k) ? w[(size_t)t * k + j] : 0.f;
+        }
+        if ((d % V) == 0) {
+            for (int c = lane * V; c < d; c += 32 * V) {
+                float acc[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_K; ++j) {
+                    if (rows[j] >= 0) {
+                        float v[V];
+                        load16(Yp + (size_t)rows[j] * d + c, v);
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[i] = fmaf(ws[j], v[i], acc[i]);
+                    }
+                }
+                store16(y + (size_t)t * d + c, acc);
+            }
+        } else {
+            for (int c = lane; c < d; c += 32) {
+                float acc = 0.f;
+                for (int j = 0; j < k; ++j)
+                    if (rows[j] >= 0) acc = fmaf(ws[j], ld_f(Yp + (size_t)rows[j] * d + c), acc);
+                st_f(y + (size_t)t * d + c, acc);
+            }
+        }
+    }
+}
+
+// Row-parallel combine backward, one warp per bucket row r < offsets[E]:
+//   kept row of (t, j): dYp[r] = w[t,j] * dy[t], dw[t,j] = <dy[t], Yp[r]>, lossrow[r] = w*dw
+//   padding row:        dYp[r] = 0, lossrow[r] = 0
+// (dw of dropped slots is zeroed beforehand.) sum_r lossrow[r] = sum_t <y[t], dy[t]>.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
+                   const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
+                   const int32_t* __restrict__ slot_row, int d, int k, int rows_cap,
+                   T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossrow) {
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nrows = min(offsets[E], rows_cap);
+    constexpr int V = Vec16<T>::N;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += nwarps) {
+        const int t = row_token[r];
+        T* out = dYp + (size_t)r * d;
+        if (t < 0) {
+            if ((d % V) == 0) {
+                float z[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) z[i] = 0.f;
+                for (int c = lane * V; c < d; c += 32 * V) store16(out + c, z);
+            } else {
+                for (int c = lane; c < d; c += 32) st_f(out + c, 0.f);
+            }
+            if (lane == 0) lossrow[r] = 0.f;
+            continue;
+        }
+        int jj = 0;
+        for (int j = 0; j < k; ++j)
+            if (slot_row[(size_t)t * k + j] == r) jj = j;
+        const float wv = w[(size_t)t * k + jj];
+        float dot = 0.f;
+        if ((d % V) == 0) {
+            for (int c = lane * V; c < d; c += 32 * V) {
+                float g[V], yv[V], o[V];
+                load16(dy + (size_t)t * d + c, g);
+                load16(Yp + (size_t)r * d + c, yv);
+#pragma unroll
+                for (int i = 0; i < V; ++i) { dot = fmaf(g[i], yv[i], dot); o[i] = wv * g[i]; }
+                store16(out + c, o);
+            }
+        } else {
+            for (int c = lane; c < d; c += 32) {
+                const float g = ld_f(dy + (size_t)t * d + c);
+                dot = fmaf(g, ld_f(Yp + (size_t)r * d + c), dot);
+                st_f(out + c, wv * g);
+            }
+        }
+        dot = warp_sum(dot);
+        if (lane == 0) {
+            dw[(size_t)t * k + jj] = dot;
+            lossrow[r] = wv * dot;
+        }
+    }
+}
+
+// Router backward + un-permute, one warp per token:
+//   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature          (softmax Jacobian)
+//   dx[t] = sum_{kept j} dXp[slot_row[t,j]] + sum_j dz_j Wg[idx[t,j]]
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
+                  const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
+                  const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
+                  int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    constexpr int V = Vec16<T>::N;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
+        float wj[MOE_MAX_K], dzj[MOE_MAX_K];
+        int rows[MOE_MAX_K], ex[MOE_MAX_K];
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            wj[j] = (j < k) ? w[(size_t)t * k + j] : 0.f;
+            dzj[j] = (j < k) ? dw[(size_t)t * k + j] : 0.f;
+            rows[j] = (j < k) ? slot_row[(size_t)t * k + j] : -1;
+            ex[j] = (j < k) ? idx[(size_t)t * k + j] : 0;
+            ex[j] = min(max(ex[j], 0), E - 1);
+            s = fmaf(wj[j], dzj[j], s);
+        }
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) dzj[j] = wj[j] * (dzj[j] - s) * inv_temp;
+        if (lane < k) {
+            float mine = 0.f;
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_K; ++j)
+                if (j == lane) mine = dzj[j];
+            dz[(size_t)t * k + lane] = mine;
+        }
+        if ((d % V) == 0) {
+            for (int c = lane * V; c < d; c += 32 * V) {
+                float acc[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_K; ++j) {
+                    if (j < k) {
+                        float v[V];
+                        if (rows[j] >= 0) {
+                            load16(dXp + (size_t)rows[j] * d + c, v);
+#pragma unroll
+                            for (int i = 0; i < V; ++i) acc[i] += v[i];
+                        }
+                        load16(Wg + (size_t)ex[j] * d + c, v);
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[i] = fmaf(dzj[j], v[i], acc[i]);
+                    }
+                }
+                store16(dx + (size_t)t * d + c, acc);
+            }
+        } else {
+            for (int c = lane; c < d; c += 32) {
+                float acc = 0.f;
+                for (int j = 0; j < k; ++j) {
+                    if (rows[j] >= 0) acc += ld_f(dXp + (size_t)rows[j] * d + c);
+                    acc = fmaf(dzj[j], ld_f(Wg + (size_t)ex[j] * d + c), acc);
+                }
+                st_f(dx + (size_t)t * d + c, acc);
+            }
+        }
+    }
+}
+
+// dWg partials: block (e, chunk) sums dz[a] * x[token(a)] over the assignments of expert e
+// whose position in e's segment is congruent to chunk (mod nchunk), in segment order.
+template <typename T>
+__global__ void __launch_bounds__(256)
+dwg_partial_kernel(const T* __restrict__ x, const float* __restrict__ dz,
+                   const int32_t* __restrict__ assign_off, const int32_t* __restrict__ assign_tok,
+                   int d, int k, int nchunk, float* __restrict__ part) {
+    const int e = blockIdx.y, chunk = blockIdx.x;
+    const int a0 = assign_off[e], a1 = assign_off[e + 1];
+    float* out = part + ((size_t)e * nchunk + chunk) * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        float acc = 0.f;
+        for (int a = a0 + chunk; a < a1; a += nchunk) {
+            const int at = assign_tok[a];
+            acc = fmaf(dz[at], ld_f(x + (size_t)(at / k) * d + c), acc);
+        }
+        out[c] = acc;
+    }
+}
+
+// dWg[e, c] = sum over chunks of the partials (fixed order); dbg[e] = sum of dz over e's
+// assignments (one block per expert, fixed reduction tree).
+__global__ void __launch_bounds__(256)
+dwg_reduce_kernel(const float* __restrict__ part, int d, int nchunk, float* __restrict__ dWg) {
+    const int e = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= d) return;
+    float acc = 0.f;
+    for (int ch = 0; ch < nchunk; ++ch) acc += part[((size_t)e * nchunk + ch) * d + c];
+    dWg[(size_t)e * d + c] = acc;
+}
+
+__global__ void __launch_bounds__(256)
+dbg_kernel(const float* __restrict__ dz, const int32_t* __restrict__ assign_off,
+           const int32_t* __restrict__ assign_tok, float* __restrict__ dbg) {
+    __shared__ float red[256];
+    const int e = blockIdx.x;
+    float acc = 0.f;
+    for (int a = assign_off[e] + threadIdx.x; a < assign_off[e + 1]; a += blockDim.x)
+        acc += dz[assign_tok[a]];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dbg[e] = red[0];
+}
+
+// db[e, c] = sum over the rows of bucket e of M[r, c] (padding rows of M are zero).
+template <typename T>
+__global__ void __launch_bounds__(256)
+bias_grad_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets,
+                 float* __restrict__ db) {
+    const int e = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= width) return;
+    const int r0 = offsets[e], r1 = offsets[e + 1];
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int r = r0;
+    for (; r + 4 <= r1; r += 4) {
+        acc0 += ld_f(M + (size_t)r * width + c);
+        acc1 += ld_f(M + (size_t)(r + 1) * width + c);
+        acc2 += ld_f(M + (size_t)(r + 2) * width + c);
+        acc3 += ld_f(M + (size_t)(r + 3) * width + c);
+    }
+    for (; r < r1; ++r) acc0 += ld_f(M + (size_t)r * width + c);
+    db[(size_t)e * width + c] = (acc0 + acc1) + (acc2 + acc3);
+}
+
+// loss = sum_r lossrow[r] (fixed order) + aux_loss_weight * balance_loss.
+__global__ void __launch_bounds__(256)
+loss_kernel(const float* __restrict__ lossrow, const int32_t* __restrict__ offsets, int E,
+            int rows_cap, const float* __restrict__ balance, float aux, float* __restrict__ loss) {
+    __shared__ double red[256];
+    const int n = min(offsets[E], rows_cap);
+    double acc = 0.0;
+    for (int r = threadIdx.x; r < n; r += blockDim.x) acc += (double)lossrow[r];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *loss = (float)(red[0] + (balance ? (double)aux * (double)*balance : 0.0));
+}
+
+int warp_grid(long long items, int warps_per_block = 8) {
+    long long b = (items + warps_per_block - 1) / warps_per_block;
+    return (int)std::max(1LL, std::min(b, (long long)num_sms() * 16));
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,
+                           const float* w, void* y, cudaStream_t s) {
+    if (c.T == 0) return cudaSuccess;
+    const int grid = warp_grid(c.T);
+    if (c.dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)Yp, slot_row, w, c.T,
+                                                           c.d, c.k, (__nv_bfloat16*)y);
+    else
+        combine_kernel<float><<<grid, 256, 0, s>>>((const float*)Yp, slot_row, w, c.T, c.d, c.k, (float*)y);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void* Yp,
+                               const float* w, const int32_t* offsets, const int32_t* row_token,
+                               const int32_t* slot_row, void* dYp, float* dw, float* lossrow,
+                               cudaStream_t s) {
+    if (c.T > 0) {
+        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)c.T * c.k, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (c.rows_capacity == 0) return cudaSuccess;
+    const int grid = warp_grid(c.rows_capacity);
+    if (c.dtype == MOE_BF16)
+        combine_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16*)dy, (const __nv_bfloat16*)Yp, w, offsets, c.E, row_token, slot_row,
+            c.d, c.k, c.rows_capacity, (__nv_bfloat16*)dYp, dw, lossrow);
+    else
+        combine_bwd_kernel<float><<<grid, 256, 0, s>>>((const float*)dy, (const float*)Yp, w, offsets,
+                                                       c.E, row_token, slot_row, c.d, c.k,
+                                                       c.rows_capacity, (float*)dYp, dw, lossrow);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
+                              const int32_t* idx, const int32_t* slot_row, const void* Wg,
+                              const void* dXp, float* dz, void* dx, cudaStream_t s) {
+    if (c.T == 0) return cudaSuccess;
+    const int grid = warp_grid(c.T);
+    const float inv_temp = 1.0f / c.temperature;
+    if (c.dtype == MOE_BF16)
+        router_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
+            c.E, inv_temp, dz, (__nv_bfloat16*)dx);
+    else
+        router_bwd_kernel<float><<<grid, 256, 0, s>>>(w, dw, idx, slot_row, (const float*)Wg,
+                                                      (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp,
+                                                      dz, (float*)dx);
+    count_launch();
+    return cudaGetLastError();
+}
+
+int dwg_chunks(const moe_config_t& c) {
+    // enough blocks to cover the GPU about twice, each walking a strided share of a segment
+    int n = ceil_div(2LL * num_sms(), c.E);
+    return std::max(1, std::min(n, 64));
+}
+
+cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
+                       const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s) {
+    const int nchunk = dwg_chunks(c);
+    dim3 g1(nchunk, c.E);
+    if (c.dtype == MOE_BF16)
+        dwg_partial_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>((const __nv_bfloat16*)x, dz, srt.assign_off,
+                                                             srt.assign_tok, c.d, c.k, nchunk, part);
+    else
+        dwg_partial_kernel<float><<<g1, 256, 0, s>>>((const float*)x, dz, srt.assign_off,
+                                                     srt.assign_tok, c.d, c.k, nchunk, part);
+    count_launch();
+    dim3 g2(ceil_div(c.d, 256), c.E);
+    dwg_reduce_kernel<<<g2, 256, 0, s>>>(part, c.d, nchunk, dWg);
+    count_launch();
+    if (dbg) {
+        dbg_kernel<<<c.E, 256, 0, s>>>(dz, srt.assign_off, srt.assign_tok, dbg);
+        count_launch();
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
+                             const int32_t* offsets, float* db, cudaStream_t s) {
+    dim3 g(ceil_div(width, 256), c.E);
+    if (c.dtype == MOE_BF16)
+        bias_grad_kernel<__nv_bfloat16><<<g, 256, 0, s>>>((const __nv_bfloat16*)M, width, offsets, db);
+    else
+        bias_grad_kernel<float><<<g, 256, 0, s>>>((const float*)M, width, offsets, db);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_loss(const moe_config_t& c, const float* lossrow, const int32_t* offsets,
+                        const float* balance_loss, float* loss, cudaStream_t s) {
+    loss_kernel<<<1, 256, 0, s>>>(lossrow, offsets, c.E, c.rows_capacity, balance_loss,
+                                  c.aux_loss_weight, loss);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

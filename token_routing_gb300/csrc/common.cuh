@@ -1,0 +1,114 @@
+// Shared device/host helpers of the MoE library (element types, vector IO, error word,
+// bounded waits, launch accounting). Nothing here knows about the layer's arithmetic.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <atomic>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- device error word
+enum : int { kErrNone = 0, kErrTimeout = 1, kErrBounds = 2 };
+
+__device__ __forceinline__ void raise_error(int* err, int code) {
+    if (err) atomicCAS(err, kErrNone, code);
+}
+
+// Cycle budget of every spin-wait (~2 s at 2 GHz): a wait that runs out records
+// kErrTimeout and returns false so the kernel can unwind instead of hanging.
+constexpr long long kSpinBudgetCycles = 4000000000LL;
+
+// ---------------------------------------------------------------- element types
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <typename T> __device__ __forceinline__ float ld_f(const T* p) { return Elem<T>::to_f(*p); }
+template <typename T> __device__ __forceinline__ void st_f(T* p, float v) { *p = Elem<T>::from_f(v); }
+
+// 16-byte vector of elements: 8 bf16 or 4 fp32.
+template <typename T> struct Vec16 { static constexpr int N = 16 / sizeof(T); };
+
+template <typename T>
+__device__ __forceinline__ void load16(const T* p, float* out) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    } else {
+        out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+        out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(T* p, const float* in) {
+    uint4 u;
+    if constexpr (sizeof(T) == 2) {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+    } else {
+        u.x = __float_as_uint(in[0]); u.y = __float_as_uint(in[1]);
+        u.z = __float_as_uint(in[2]); u.w = __float_as_uint(in[3]);
+    }
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// GELU(a) = a * Phi(a) with the exact erf form; derivative Phi(a) + a * phi(a).
+__device__ __forceinline__ float gelu_f(float a) {
+    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_grad_f(float a) {
+    const float Phi = 0.5f * (1.0f + erff(a * 0.70710678118654752f));
+    const float phi = 0.39894228040143268f * __expf(-0.5f * a * a);
+    return Phi + a * phi;
+}
+
+// ---------------------------------------------------------------- host side
+extern std::atomic<uint64_t> g_launches;
+inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Device address of the error word of the current device (cached per device).
+int* device_error_word();
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Sub-buffers carved out of the caller's workspace.
+struct Workspace {
+    char* base;
+    size_t used;
+    template <typename T> T* take(size_t count) {
+        used = align_up(used, 256);
+        T* p = reinterpret_cast<T*>(base ? base + used : nullptr);
+        used += count * sizeof(T);
+        return p;
+    }
+};
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,90 @@
+// Internal interfaces between the translation units of the MoE library.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Epilogues of the grouped GEMMs over expert buckets (rows of one 128-row tile always belong
+// to a single expert because buckets are padded to MOE_ROW_ALIGN rows).
+enum GemmKind : int {
+    kGemmFfn1 = 0,   // A = Xp W1_e^T + b1_e, H = GELU(A)          (store A and H)
+    kGemmFfn2 = 1,   // Yp = H W2_e^T + b2_e
+    kGemmDH = 2,     // dA = (dYp W2_e) * GELU'(A)
+    kGemmDX = 3,     // dXp = dA W1_e
+    kGemmWgrad = 4,  // dW_e = P_e^T Q_e over the rows of bucket e (dW2: P=dYp,Q=H; dW1: P=dA,Q=Xp)
+};
+
+struct RowGemmArgs {
+    int kind;
+    const void* A;          // [rows, K] row-major activations
+    const void* B;          // expert weights (layout per kind)
+    const void* bias;       // [E, N] (Ffn1, Ffn2)
+    const void* aux;        // [rows, N] A of the forward (DH)
+    void* out0;             // [rows, N]
+    void* out1;             // [rows, N] (H of Ffn1)
+    const int32_t* offsets; // [E+1] bucket starts
+    int E, N, K;
+    int rows_capacity;
+    long long sBe, sBn, sBk; // element strides of B: expert, output column, reduction index
+};
+
+struct WgradArgs {
+    const void* P;          // [rows, M] row-major
+    const void* Q;          // [rows, N] row-major
+    void* C;                // [E, M, N]
+    const int32_t* offsets;
+    int E, M, N;
+};
+
+// router.cu
+cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
+                         int32_t* idx, float* w, int32_t* counts, float* balance_loss,
+                         cudaStream_t s);
+
+// dispatch.cu: stable counting sort of the assignments by expert
+struct SortScratch {
+    int32_t* blk_hist;     // [nblk, E]
+    int32_t* blk_base;     // [nblk, E]
+    int32_t* assign_off;   // [E+1] exclusive scan of counts
+    int32_t* assign_tok;   // [T*k] assignment (t*k+j) in expert-major, token-minor order
+    int32_t* counts;       // [E]
+};
+int sort_blocks(int T);
+void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s);
+// kept/offsets/row_token/slot_row/n_dropped may be null (assignment sort only).
+cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScratch& s,
+                        int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                        int32_t* n_dropped, cudaStream_t st);
+cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* offsets,
+                          const int32_t* row_token, void* Xp, cudaStream_t st);
+
+// gemm_simt.cu (fp32, and bf16 shapes the tensor-core kernel does not take)
+cudaError_t launch_row_gemm_simt(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
+cudaError_t launch_wgrad_simt(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
+
+// gemm_tc.cu (bf16 on tcgen05 tensor cores; returns cudaErrorNotSupported for shapes it
+// does not take)
+bool tc_gemm_supported(const moe_config_t& c);
+cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
+cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,
+                           const float* w, void* y, cudaStream_t s);
+cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void* Yp,
+                               const float* w, const int32_t* offsets, const int32_t* row_token,
+                               const int32_t* slot_row, void* dYp, float* dw, float* lossrow,
+                               cudaStream_t s);
+cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
+                              const int32_t* idx, const int32_t* slot_row, const void* Wg,
+                              const void* dXp, float* dz, void* dx, cudaStream_t s);
+int dwg_chunks(const moe_config_t& c);
+cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
+                       const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s);
+cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
+                             const int32_t* offsets, float* db, cudaStream_t s);
+cudaError_t launch_loss(const moe_config_t& c, const float* lossrow, const int32_t* offsets,
+                        const float* balance_loss, float* loss, cudaStream_t s);
+
+}  // namespace moe
