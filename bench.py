@@ -1,0 +1,338 @@
+"""Throughput of the MoE layer (forward + backward) on GB300, through the C ABI.
+
+One step = route -> dispatch -> expert_ffn -> combine -> backward over one batch of the
+workload (default: top-2 over 16 experts, T=8192, d=1024, d_ff=4096, capacity 1.0, bf16).
+Inputs are resident in HBM when the timed region starts; L2 is flushed (a 256 MB write)
+before every timed step, outside the step's events. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent replica on its
+own batch (the layer has no exchange step on one device); value = all tokens / max time.
+`--impl reference` times the fp64 CPU oracle instead, on bounded token samples.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % BF16 peak; permute GB/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_counts(cfg, kept_rows):
+    """Per-step algorithmic work: expert FLOPs and the permute / router / combine bytes
+    (units: kept assignments N, tokens T)."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.d_ff
+    N = kept_rows
+    return dict(
+        ffn_fwd_flops=4.0 * N * d * f,
+        ffn_bwd_flops=8.0 * N * d * f,
+        permute_bytes=T * d * es + N * d * es + 4.0 * (N + T * k),
+        router_bytes=T * d * es + E * d * es + T * k * 8.0,
+        combine_bytes=N * d * es + T * d * es + T * k * 8.0,
+    )
+
+
+def oracle_step(cfg, npin):
+    from oracle import moe_oracle as O
+    C = O.capacity(cfg.capacity_factor, cfg.T, cfg.k, cfg.E)
+    fwd = O.forward(npin, cfg.k, cfg.temperature, C)
+    O.backward(npin, fwd, npin["dy"])
+    return fwd
+
+
+def oracle_sample_inputs(cfg, tokens):
+    import synth
+    sample = cfg.with_(T=min(tokens, cfg.T))
+    inp = synth.make_inputs(sample)
+    return sample, {k: (None if v is None else v.double().numpy()) for k, v in inp.items()}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, tokens):
+    """The fp64 oracle, as it stands, on one batch of `tokens` tokens of the same workload."""
+    sample, npin = oracle_sample_inputs(cfg, tokens)
+    t0 = time.perf_counter()
+    oracle_step(sample, npin)
+    dt = time.perf_counter() - t0
+    return {"value": sample.T / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"one fwd+bwd step of a {sample.T}-token batch of {cfg.name} "
+                      f"(numpy fp64, BLAS threads = host cores), {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    sample, npin = oracle_sample_inputs(cfg, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_step(sample, npin)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(sample, npin)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = sample.T / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+                       "d_ff": cfg.d_ff, "capacity_factor": cfg.capacity_factor,
+                       "temperature": cfg.temperature, "sample_tokens_per_step": sample.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{sample.T}-token batches of {cfg.name} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cfg):
+    import torch
+    import synth
+    import token_routing_gb300 as moe
+
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load()
+
+    # each replica draws its own batch (seed = rank); weights are the same recipe
+    inp = synth.make_inputs(cfg, seed=cfg.seed + rank)
+    d_in = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    c = moe.config_from(cfg)
+    b = moe.alloc_buffers(c, device=dev, backward=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    names = ["route", "dispatch", "expert_ffn", "combine", "backward"]
+
+    def step(evs=None):
+        if evs: evs[0].record(stream)
+        moe.route(c, d_in["x"], d_in["Wg"], d_in["bg"], b, stream)
+        if evs: evs[1].record(stream)
+        moe.dispatch(c, b["idx"], d_in["x"], b, stream)
+        if evs: evs[2].record(stream)
+        moe.expert_ffn(c, b["Xp"], b["offsets"], d_in["W1"], d_in["b1"], d_in["W2"], d_in["b2"], b, stream)
+        if evs: evs[3].record(stream)
+        moe.combine(c, b["Yp"], b["slot_row"], b["w"], b["y"], stream)
+        if evs: evs[4].record(stream)
+        moe.backward(c, d_in["dy"], d_in["x"], d_in["Wg"], d_in["W1"], d_in["W2"], b, stream)
+        if evs: evs[5].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    moe.get_error(stream)
+    kept = int(b["kept"].sum().item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    launches0 = moe.kernel_launches()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    launches = moe.kernel_launches() - launches0
+    clocks = sampler.stop()
+    moe.get_error(stream)
+    if world > 1:
+        torch.distributed.barrier()
+
+    stage_ms = {n: 0.0 for n in names}
+    step_ms = []
+    for e in evs:
+        step_ms.append(e[0].elapsed_time(e[5]))
+        for j, n in enumerate(names):
+            stage_ms[n] += e[j].elapsed_time(e[j + 1])
+    stage_ms = {n: v / args.steps for n, v in stage_ms.items()}
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: pinned host inputs -> device, step, loss -> host
+    x_h = inp["x"].pin_memory()
+    dy_h = inp["dy"].pin_memory()
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        d_in["x"].copy_(x_h, non_blocking=True)
+        d_in["dy"].copy_(dy_h, non_blocking=True)
+        step()
+        loss_h.copy_(b["loss"], non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(t.item())
+
+    if rank == 0:
+        peaks = _peaks()
+        work = algorithmic_counts(cfg, kept)
+        ffn_s = stage_ms["expert_ffn"] * 1e-3
+        gemm_tflops = work["ffn_fwd_flops"] / ffn_s / 1e12
+        peak_tc = peaks["bf16_tflops_sustained"]
+        permute_gbs = work["permute_bytes"] / (stage_ms["dispatch"] * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": cfg.T * world / (ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+                       "d_ff": cfg.d_ff, "capacity_factor": cfg.capacity_factor,
+                       "temperature": cfg.temperature, "kept_assignments": kept,
+                       "l2": "flushed (256 MB write) before every timed step, outside its events",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"kernel": "tcgen05 grouped GEMM, forward pair (GEMM1+GELU, GEMM2)",
+                         "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / peak_tc,
+                         "peak_source": f"{peaks['src']} bf16 sustained", "traffic": None},
+            "grouped_gemm_pct_bf16_peak": 100.0 * gemm_tflops / peak_tc,
+            "permute_gbs": permute_gbs,
+            "permute_frac_hbm": permute_gbs / peaks["hbm_gbs"],
+            "stage_ms": stage_ms,
+            "e2e": {"value": cfg.T * world / (e2e * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": int(launches),
+            "wall_s_timed": t_wall,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_tokens)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    import synth
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=synth.HEADLINE)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=8192, help="tokens in the oracle's timed batch")
+    ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    cfg = synth.get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
