@@ -127,6 +127,28 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, c
                           int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
                           int32_t* n_dropped, void* Xp, void* ws, moe_stream_t stream);
 
+/* moe_dispatch for callers that cannot allocate device memory. The pages have no
+ * counterpart: this entry point exists for code that may not call cudaMalloc (it runs
+ * inside a memory budget or a host framework that owns every allocation, or it is a plugin
+ * given only its input and output buffers) and so cannot provide the `ws` scratch.
+ * Same arguments, results and errors as moe_dispatch, minus `ws`: the sort scratch is a
+ * fixed array of MOE_NOALLOC_SCRATCH_BYTES in the library's device memory, reserved on
+ * every GPU that loads the library until the process exits. The call allocates nothing.
+ * Limits: T <= MOE_NOALLOC_MAX_TOKENS and T*k <= MOE_NOALLOC_MAX_ASSIGNMENTS; larger
+ * configurations return MOE_ERR_UNSUPPORTED (use moe_dispatch with a workspace).
+ * The first call on a device looks up the array's device address (once per device); make
+ * that first call before any stream capture. All calls share the one array: calls that
+ * may overlap on the GPU (other streams, other host threads) race and must be serialised
+ * by the caller. Nothing in the array needs to start at zero; each call writes what it
+ * reads. */
+#define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define MOE_NOALLOC_MAX_TOKENS 65536
+#define MOE_NOALLOC_MAX_ASSIGNMENTS 262144
+MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx, const void* x,
+                                          int32_t* kept, int32_t* offsets, int32_t* row_token,
+                                          int32_t* slot_row, int32_t* n_dropped, void* Xp,
+                                          moe_stream_t stream);
+
 /* Per-expert FFN over the buckets: A = Xp W1_e^T + b1_e, H = GELU(A), Yp = H W2_e^T + b2_e.
  *   Xp [rows_capacity,d], offsets [E+1] (from moe_dispatch), W1 [E,d_ff,d], b1 [E,d_ff],
  *   W2 [E,d,d_ff], b2 [E,d] -> A, H [rows_capacity,d_ff], Yp [rows_capacity,d] (all act;

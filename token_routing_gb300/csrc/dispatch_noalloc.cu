@@ -1,0 +1,76 @@
+// moe_dispatch_noalloc: the dispatch step (capacity, counting sort into expert buckets,
+// gather of x) for callers that cannot allocate device memory.
+//
+// Some callers have no way to allocate: code running where cudaMalloc is not allowed
+// (inside a pre-allocated memory budget or a host framework that owns every allocation),
+// or plugins that are handed only their input and output buffers. For them this entry
+// point takes no workspace argument. Its sort scratch is a fixed array in the library's
+// own device memory, reserved on every GPU that loads the library until the process
+// exits. The arithmetic is that of moe_dispatch (same kernels, same results).
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+// The library's own dispatch scratch. In host code this name is only a stand-in for the
+// device symbol: host code must use the address cudaGetSymbolAddress returns.
+static __device__ __align__(256) unsigned char g_dispatch_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDev] = {};
+
+// Device address of the scratch array on the current device, resolved once per device.
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx,
+                                                     const void* x, int32_t* kept, int32_t* offsets,
+                                                     int32_t* row_token, int32_t* slot_row,
+                                                     int32_t* n_dropped, void* Xp, moe_stream_t stream) {
+    // a config that moe_config_init did not accept has no workspace size
+    if (moe_workspace_bytes(cfg) == 0) return MOE_ERR_INVALID_ARG;
+    if (!kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > MOE_NOALLOC_MAX_TOKENS || (int64_t)cfg->T * cfg->k > MOE_NOALLOC_MAX_ASSIGNMENTS)
+        return MOE_ERR_UNSUPPORTED;
+    Workspace probe{nullptr, 0};
+    SortScratch srt;
+    sort_scratch_take(probe, *cfg, &srt);
+    if (probe.used > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+    // Every scratch word the sort reads is written earlier in the same call, so the
+    // previous call's leftovers need no clearing.
+    Workspace ws{static_cast<char*>(base), 0};
+    sort_scratch_take(ws, *cfg, &srt);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_gather(*cfg, x, offsets, row_token, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
