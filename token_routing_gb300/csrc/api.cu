@@ -80,8 +80,9 @@ struct BackwardScratch {
     void* dXp;
     float* dw;
     float* dz;
-    float* lossrow;
+    float* lossblk;
     float* dwg_part;
+    float* colsum_part;
 };
 
 size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
@@ -94,8 +95,9 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     b->dXp = ws.take<char>(R * c.d * es);
     b->dw = ws.take<float>((size_t)c.T * c.k + 1);
     b->dz = ws.take<float>((size_t)c.T * c.k + 1);
-    b->lossrow = ws.take<float>(R + 1);
+    b->lossblk = ws.take<float>((size_t)combine_bwd_blocks(c) + 1);
     b->dwg_part = ws.take<float>((size_t)c.E * dwg_chunks(c) * c.d);
+    b->colsum_part = ws.take<float>((R / MOE_ROW_ALIGN) * (size_t)std::max(c.d, c.d_ff) + 1);
     return align_up(ws.used, 256);
 }
 
@@ -233,7 +235,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     float* dwp = dw ? dw : b.dw;
 
     // combine backward: dYp, dw, per-row loss terms (padding rows of dYp zeroed)
-    MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossrow, s));
+    MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossblk, s));
     // experts backward
     RowGemmArgs gh{};
     gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = A; gh.out0 = b.dA;
@@ -249,13 +251,13 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     MOE_TRY(wgrad(c, w2, s));
     WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
     MOE_TRY(wgrad(c, w1, s));
-    MOE_TRY(launch_bias_grad(c, b.dYp, c.d, offsets, db2, s));
-    MOE_TRY(launch_bias_grad(c, b.dA, c.d_ff, offsets, db1, s));
+    MOE_TRY(launch_bias_grad(c, b.dYp, c.d, offsets, b.colsum_part, db2, s));
+    MOE_TRY(launch_bias_grad(c, b.dA, c.d_ff, offsets, b.colsum_part, db1, s));
     // router backward: assignment sort, softmax Jacobian, dx, dWg, dbg
     MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
     MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
     MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, dbg, s));
-    if (loss) MOE_TRY(launch_loss(c, b.lossrow, offsets, balance_loss, loss, s));
+    if (loss) MOE_TRY(launch_loss(c, b.lossblk, balance_loss, loss, s));
     return MOE_OK;
 }
 

@@ -67,11 +67,13 @@ __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
                    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
                    const int32_t* __restrict__ slot_row, int d, int k, int rows_cap,
-                   T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossrow) {
+                   T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossblk) {
+    __shared__ float s_warp[8];
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nrows = min(offsets[E], rows_cap);
     constexpr int V = Vec16<T>::N;
+    float wloss = 0.f;  // this warp's sum of w * dw over its rows, in row order
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += nwarps) {
         const int t = row_token[r];
         T* out = dYp + (size_t)r * d;
@@ -84,7 +86,6 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
             } else {
                 for (int c = lane; c < d; c += 32) st_f(out + c, 0.f);
             }
-            if (lane == 0) lossrow[r] = 0.f;
             continue;
         }
         int jj = 0;
@@ -109,10 +110,15 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
             }
         }
         dot = warp_sum(dot);
-        if (lane == 0) {
-            dw[(size_t)t * k + jj] = dot;
-            lossrow[r] = wv * dot;
-        }
+        if (lane == 0) dw[(size_t)t * k + jj] = dot;
+        wloss = fmaf(wv, dot, wloss);
+    }
+    if (lane == 0) s_warp[threadIdx.x >> 5] = wloss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b += s_warp[i];
+        lossblk[blockIdx.x] = b;
     }
 }
 
@@ -184,23 +190,72 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
     }
 }
 
-// dWg partials: block (e, chunk) sums dz[a] * x[token(a)] over the assignments of expert e
-// whose position in e's segment is congruent to chunk (mod nchunk), in segment order.
+// dWg partials: block (e, chunk) sums dz[a] * x[token(a)] over a contiguous piece of expert
+// e's assignment segment, in segment order. The piece's token ids and dz values are staged in
+// shared memory; each thread owns V consecutive columns and keeps 8 row loads in flight.
 template <typename T>
 __global__ void __launch_bounds__(256)
 dwg_partial_kernel(const T* __restrict__ x, const float* __restrict__ dz,
                    const int32_t* __restrict__ assign_off, const int32_t* __restrict__ assign_tok,
                    int d, int k, int nchunk, float* __restrict__ part) {
+    constexpr int V = Vec16<T>::N;
+    constexpr int PIECE = 256;
+    __shared__ int s_tok[PIECE];
+    __shared__ float s_dz[PIECE];
     const int e = blockIdx.y, chunk = blockIdx.x;
-    const int a0 = assign_off[e], a1 = assign_off[e + 1];
+    const int seg0 = assign_off[e], seg1 = assign_off[e + 1];
+    const int per = (seg1 - seg0 + nchunk - 1) / nchunk;
+    const int a0 = seg0 + chunk * per, a1 = min(seg1, a0 + per);
     float* out = part + ((size_t)e * nchunk + chunk) * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-        float acc = 0.f;
-        for (int a = a0 + chunk; a < a1; a += nchunk) {
-            const int at = assign_tok[a];
-            acc = fmaf(dz[at], ld_f(x + (size_t)(at / k) * d + c), acc);
+    const bool vec = (d % V) == 0;
+    const int step = vec ? V : 1;
+    // every thread runs the same number of passes: the barriers below are block-wide
+    const int passes = (d + (int)blockDim.x * step - 1) / ((int)blockDim.x * step);
+    for (int pass = 0; pass < passes; ++pass) {
+        const int cg = (pass * (int)blockDim.x + (int)threadIdx.x) * step;
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        const bool active = cg < d;
+        for (int p0 = a0; p0 < a1; p0 += PIECE) {
+            const int n = min(PIECE, a1 - p0);
+            __syncthreads();
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int at = assign_tok[p0 + i];
+                s_tok[i] = at / k;
+                s_dz[i] = dz[at];
+            }
+            __syncthreads();
+            if (!active) continue;
+            if (vec) {
+                int i = 0;
+                for (; i + 8 <= n; i += 8) {
+                    float v[8][V];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) load16(x + (size_t)s_tok[i + u] * d + cg, v[u]);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+#pragma unroll
+                        for (int q = 0; q < V; ++q) acc[q] = fmaf(s_dz[i + u], v[u][q], acc[q]);
+                }
+                for (; i < n; ++i) {
+                    float v[V];
+                    load16(x + (size_t)s_tok[i] * d + cg, v);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[q] = fmaf(s_dz[i], v[q], acc[q]);
+                }
+            } else {
+                for (int i = 0; i < n; ++i) acc[0] = fmaf(s_dz[i], ld_f(x + (size_t)s_tok[i] * d + cg), acc[0]);
+            }
         }
-        out[c] = acc;
+        if (active) {
+            if (vec) {
+#pragma unroll
+                for (int q = 0; q < V; ++q) out[cg + q] = acc[q];
+            } else {
+                out[cg] = acc[0];
+            }
+        }
     }
 }
 
@@ -233,35 +288,61 @@ dbg_kernel(const float* __restrict__ dz, const int32_t* __restrict__ assign_off,
     if (threadIdx.x == 0) dbg[e] = red[0];
 }
 
-// db[e, c] = sum over the rows of bucket e of M[r, c] (padding rows of M are zero).
+// Column sums of one 128-row tile (tiles never straddle buckets; padding rows are zero):
+// part[tile, c] = sum of M[r, c] over the tile's rows, rows in order.
 template <typename T>
 __global__ void __launch_bounds__(256)
-bias_grad_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets,
-                 float* __restrict__ db) {
+colsum_tile_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets, int E,
+                   float* __restrict__ part) {
+    constexpr int V = Vec16<T>::N;
+    const int tile = blockIdx.y;
+    const int r0 = tile * MOE_ROW_ALIGN;
+    if (r0 >= offsets[E]) return;
+    if (width % V == 0) {
+        const int c = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+        if (c >= width) return;
+        float acc[V];
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < MOE_ROW_ALIGN; ++r) {
+            float v[V];
+            load16(M + (size_t)(r0 + r) * width + c, v);
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[q] += v[q];
+        }
+#pragma unroll
+        for (int q = 0; q < V; ++q) part[(size_t)tile * width + c + q] = acc[q];
+    } else {
+        for (int c = blockIdx.x * blockDim.x * V + threadIdx.x; c < min(width, (int)((blockIdx.x + 1) * blockDim.x * V));
+             c += blockDim.x) {
+            float acc = 0.f;
+            for (int r = 0; r < MOE_ROW_ALIGN; ++r) acc += ld_f(M + (size_t)(r0 + r) * width + c);
+            part[(size_t)tile * width + c] = acc;
+        }
+    }
+}
+
+// db[e, c] = sum over the tiles of bucket e of part[tile, c], tiles in order.
+__global__ void __launch_bounds__(256)
+bias_reduce_kernel(const float* __restrict__ part, int width, const int32_t* __restrict__ offsets,
+                   float* __restrict__ db) {
     const int e = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= width) return;
-    const int r0 = offsets[e], r1 = offsets[e + 1];
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int r = r0;
-    for (; r + 4 <= r1; r += 4) {
-        acc0 += ld_f(M + (size_t)r * width + c);
-        acc1 += ld_f(M + (size_t)(r + 1) * width + c);
-        acc2 += ld_f(M + (size_t)(r + 2) * width + c);
-        acc3 += ld_f(M + (size_t)(r + 3) * width + c);
-    }
-    for (; r < r1; ++r) acc0 += ld_f(M + (size_t)r * width + c);
-    db[(size_t)e * width + c] = (acc0 + acc1) + (acc2 + acc3);
+    const int t0 = offsets[e] / MOE_ROW_ALIGN, t1 = offsets[e + 1] / MOE_ROW_ALIGN;
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t) acc += part[(size_t)t * width + c];
+    db[(size_t)e * width + c] = acc;
 }
 
-// loss = sum_r lossrow[r] (fixed order) + aux_loss_weight * balance_loss.
+// loss = sum of the combine-backward block partials (fixed order) + aux * balance_loss.
 __global__ void __launch_bounds__(256)
-loss_kernel(const float* __restrict__ lossrow, const int32_t* __restrict__ offsets, int E,
-            int rows_cap, const float* __restrict__ balance, float aux, float* __restrict__ loss) {
+loss_kernel(const float* __restrict__ lossblk, int nblk, const float* __restrict__ balance, float aux,
+            float* __restrict__ loss) {
     __shared__ double red[256];
-    const int n = min(offsets[E], rows_cap);
     double acc = 0.0;
-    for (int r = threadIdx.x; r < n; r += blockDim.x) acc += (double)lossrow[r];
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) acc += (double)lossblk[i];
     red[threadIdx.x] = acc;
     __syncthreads();
     for (int o = 128; o > 0; o >>= 1) {
@@ -291,24 +372,25 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t*
     return cudaGetLastError();
 }
 
+int combine_bwd_blocks(const moe_config_t& c) { return warp_grid(std::max(c.rows_capacity, 1)); }
+
 cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void* Yp,
                                const float* w, const int32_t* offsets, const int32_t* row_token,
-                               const int32_t* slot_row, void* dYp, float* dw, float* lossrow,
+                               const int32_t* slot_row, void* dYp, float* dw, float* lossblk,
                                cudaStream_t s) {
     if (c.T > 0) {
         cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)c.T * c.k, s);
         if (e != cudaSuccess) return e;
     }
-    if (c.rows_capacity == 0) return cudaSuccess;
-    const int grid = warp_grid(c.rows_capacity);
+    const int grid = combine_bwd_blocks(c);
     if (c.dtype == MOE_BF16)
         combine_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             (const __nv_bfloat16*)dy, (const __nv_bfloat16*)Yp, w, offsets, c.E, row_token, slot_row,
-            c.d, c.k, c.rows_capacity, (__nv_bfloat16*)dYp, dw, lossrow);
+            c.d, c.k, c.rows_capacity, (__nv_bfloat16*)dYp, dw, lossblk);
     else
         combine_bwd_kernel<float><<<grid, 256, 0, s>>>((const float*)dy, (const float*)Yp, w, offsets,
                                                        c.E, row_token, slot_row, c.d, c.k,
-                                                       c.rows_capacity, (float*)dYp, dw, lossrow);
+                                                       c.rows_capacity, (float*)dYp, dw, lossblk);
     count_launch();
     return cudaGetLastError();
 }
@@ -332,8 +414,8 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
 }
 
 int dwg_chunks(const moe_config_t& c) {
-    // enough blocks to cover the GPU about twice, each walking a strided share of a segment
-    int n = ceil_div(2LL * num_sms(), c.E);
+    // about four blocks per SM in total, each on a contiguous piece of one expert's segment
+    int n = ceil_div(4LL * num_sms(), c.E);
     return std::max(1, std::min(n, 64));
 }
 
@@ -341,12 +423,14 @@ cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
                        const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s) {
     const int nchunk = dwg_chunks(c);
     dim3 g1(nchunk, c.E);
+    const int V = c.dtype == MOE_BF16 ? 8 : 4;
+    const int threads = std::max(32, std::min(256, (ceil_div(c.d, V) + 31) / 32 * 32));
     if (c.dtype == MOE_BF16)
-        dwg_partial_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>((const __nv_bfloat16*)x, dz, srt.assign_off,
-                                                             srt.assign_tok, c.d, c.k, nchunk, part);
+        dwg_partial_kernel<__nv_bfloat16><<<g1, threads, 0, s>>>((const __nv_bfloat16*)x, dz, srt.assign_off,
+                                                                 srt.assign_tok, c.d, c.k, nchunk, part);
     else
-        dwg_partial_kernel<float><<<g1, 256, 0, s>>>((const float*)x, dz, srt.assign_off,
-                                                     srt.assign_tok, c.d, c.k, nchunk, part);
+        dwg_partial_kernel<float><<<g1, threads, 0, s>>>((const float*)x, dz, srt.assign_off,
+                                                         srt.assign_tok, c.d, c.k, nchunk, part);
     count_launch();
     dim3 g2(ceil_div(c.d, 256), c.E);
     dwg_reduce_kernel<<<g2, 256, 0, s>>>(part, c.d, nchunk, dWg);
@@ -359,20 +443,26 @@ cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
 }
 
 cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
-                             const int32_t* offsets, float* db, cudaStream_t s) {
-    dim3 g(ceil_div(width, 256), c.E);
-    if (c.dtype == MOE_BF16)
-        bias_grad_kernel<__nv_bfloat16><<<g, 256, 0, s>>>((const __nv_bfloat16*)M, width, offsets, db);
-    else
-        bias_grad_kernel<float><<<g, 256, 0, s>>>((const float*)M, width, offsets, db);
+                             const int32_t* offsets, float* part, float* db, cudaStream_t s) {
+    const int tiles = c.rows_capacity / MOE_ROW_ALIGN;
+    if (tiles > 0) {
+        const int V = c.dtype == MOE_BF16 ? 8 : 4;
+        dim3 g1(ceil_div(width, 256 * V), tiles);
+        if (c.dtype == MOE_BF16)
+            colsum_tile_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>((const __nv_bfloat16*)M, width, offsets, c.E, part);
+        else
+            colsum_tile_kernel<float><<<g1, 256, 0, s>>>((const float*)M, width, offsets, c.E, part);
+        count_launch();
+    }
+    dim3 g2(ceil_div(width, 256), c.E);
+    bias_reduce_kernel<<<g2, 256, 0, s>>>(part, width, offsets, db);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_loss(const moe_config_t& c, const float* lossrow, const int32_t* offsets,
-                        const float* balance_loss, float* loss, cudaStream_t s) {
-    loss_kernel<<<1, 256, 0, s>>>(lossrow, offsets, c.E, c.rows_capacity, balance_loss,
-                                  c.aux_loss_weight, loss);
+cudaError_t launch_loss(const moe_config_t& c, const float* lossblk, const float* balance_loss,
+                        float* loss, cudaStream_t s) {
+    loss_kernel<<<1, 256, 0, s>>>(lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss);
     count_launch();
     return cudaGetLastError();
 }

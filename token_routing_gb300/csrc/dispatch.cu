@@ -85,40 +85,55 @@ scan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int T, int k,
     }
 }
 
-// Ranks inside a block: thread e walks the block's tokens in order and numbers the
-// assignments to expert e. Writes the expert-major assignment list and, when the bucket
-// outputs are requested, slot_row / row_token.
+// Ranks inside a block, without any order-dependent step: every (token, slot) sets its
+// token's bit in a per-expert 256-bit mask, then the rank of token t among the block's
+// tokens that picked e is the population count of e's mask below bit t. Writes the
+// expert-major assignment list and, when the bucket outputs are requested, slot_row and
+// row_token.
 __global__ void __launch_bounds__(kSortTok)
 rank_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int C,
             const int32_t* __restrict__ blk_base, const int32_t* __restrict__ assign_off,
             const int32_t* __restrict__ offsets, int32_t* __restrict__ assign_tok,
             int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token) {
-    __shared__ int32_t s_idx[kSortTok * MOE_MAX_K];
-    const int t0 = blockIdx.x * kSortTok;
-    const int nt = min(kSortTok, T - t0);
-    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) s_idx[i] = idx[(size_t)t0 * k + i];
+    constexpr int W = kSortTok / 32;
+    __shared__ uint32_t s_mask[MOE_MAX_EXPERTS * W];
+    for (int i = threadIdx.x; i < E * W; i += blockDim.x) s_mask[i] = 0u;
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int rank = blk_base[(size_t)blockIdx.x * E + e];
-        const int abase = assign_off[e];
-        const int bstart = offsets ? offsets[e] : 0;
-        for (int i = 0; i < nt * k; ++i) {
-            if (s_idx[i] != e) continue;
-            bool dup = false;  // a repeated expert inside one token was rejected by the histogram
-            for (int i2 = (i / k) * k; i2 < i; ++i2) dup = dup || (s_idx[i2] == e);
-            if (dup) continue;
-            const int t = t0 + i / k;
-            assign_tok[abase + rank] = t0 * k + i;
-            if (slot_row) {
-                if (rank < C) {
-                    const int row = bstart + rank;
-                    slot_row[(size_t)t0 * k + i] = row;
-                    row_token[row] = t;
-                } else {
-                    slot_row[(size_t)t0 * k + i] = -1;
-                }
+    const int t = blockIdx.x * kSortTok + threadIdx.x;
+    const int word = threadIdx.x >> 5;
+    const uint32_t bit = 1u << (threadIdx.x & 31);
+    int mine[MOE_MAX_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
+    if (t < T) {
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[(size_t)t * k + j];
+            bool ok = (e >= 0 && e < E);
+            for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);  // repeats were rejected by the histogram
+            if (ok) {
+                mine[j] = e;
+                atomicOr(&s_mask[e * W + word], bit);
             }
-            ++rank;
+        }
+    }
+    __syncthreads();
+    if (t >= T) return;
+    for (int j = 0; j < k; ++j) {
+        const int e = mine[j];
+        if (e < 0) continue;
+        const uint32_t* m = s_mask + e * W;
+        int local = __popc(m[word] & (bit - 1u));
+        for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
+        const int rank = blk_base[(size_t)blockIdx.x * E + e] + local;
+        assign_tok[assign_off[e] + rank] = t * k + j;
+        if (slot_row) {
+            if (rank < C) {
+                const int row = offsets[e] + rank;
+                slot_row[(size_t)t * k + j] = row;
+                row_token[row] = t;
+            } else {
+                slot_row[(size_t)t * k + j] = -1;
+            }
         }
     }
 }

@@ -9,23 +9,21 @@
 // ones (dH with the GELU derivative fused, dX, and the weight gradients whose reduction runs
 // over the bucket rows).
 //
-// CTA = 6 warps: warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs (one
-// thread), warps 2..5 drain the accumulator (tcgen05.ld) and run the epilogue. The
+// CTA = 10 warps: warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs (one
+// thread), warps 2..9 drain the accumulator (tcgen05.ld) and run the epilogue (two warps
+// per TMEM lane quarter, each on half of the tile's columns). The
 // accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the MMAs of the next. Tiles are 128 x 256 x 64 (bf16, fp32 accumulate).
 //
 // Every wait is bounded: a wait that runs out records a device error, the roles unwind,
 // in-flight copies and MMAs are drained, and TMEM is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
@@ -36,8 +34,9 @@ constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;         // two accumulator buffers
-constexpr int THREADS = 192;
-constexpr int EPI_THREADS = 128;
+constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, each on half the columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int kMaxOffsets = MOE_MAX_EXPERTS + 1;
 
 struct TcParams {
@@ -51,96 +50,6 @@ struct TcParams {
     __nv_bfloat16* out1;
     int* err;
 };
-
-// ------------------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait on a barrier phase; false (and a device error) when the budget runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-    if (mbar_try(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try(bar, parity)) {
-        if (clock64() - t0 > kSpinBudgetCycles) {
-            raise_error(err, kErrTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns of the accumulator (lane i <-> TMEM lane base+i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: version 1 at bit 46,
-// swizzle mode 2 at bits 61-63). lbo/sbo in bytes.
-__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
 
 // Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M = 128, N = BN.
 __host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_major) {
@@ -195,7 +104,7 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v) 
 
 template <int KIND>
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Tile& t, int row_in_tile,
-                                               int c, const uint32_t (&acc)[32]) {
+                                               int c, const uint32_t (&acc)[32], const float (&a)[32]) {
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
@@ -220,9 +129,6 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Tile& t,
             store_row32(p.out1 + o, v);
         }
     } else if (KIND == kGemmDH) {
-        float a[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) load16(p.aux + o + 8 * q, a + 8 * q);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
         store_row32(p.out0 + o, v);
@@ -232,14 +138,14 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Tile& t,
 }
 
 template <int KIND>
-__device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile) {
+__device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
     // an expert with no rows: its weight-gradient tile is zero
     float z[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = 0.f;
     const int m = t.m0 + row_in_tile;
     if (m >= p.M) return;
-    for (int c = 0; c < BN; c += 32)
+    for (int c = c_lo; c < c_lo + BN / 2; c += 32)
         if (t.n0 + c < p.N) store_row32(p.out0 + ((size_t)t.e * p.M + m) * p.N + t.n0 + c, z);
 }
 
@@ -369,14 +275,15 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             mbar_wait(drain, 0, p.err);
         }
     } else {
-        // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+        // ---------------- epilogue warps 2..9: TMEM lane quarter = warp % 4, column half
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
+        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
         uint32_t tl = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Tile t = decode_tile<WGRAD>(p, s_off, tile);
             if (t.kblocks == 0) {
-                if (WGRAD) epilogue_zero<KIND>(p, t, row_in_tile);
+                if (WGRAD) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
                 continue;
             }
             const int buf = tl & 1;
@@ -385,12 +292,20 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
                 if (t.n0 + c >= p.N) break;
+                float a[32];
+                if (KIND == kGemmDH) {
+                    // forward pre-activation of this row's 32 columns, fetched before the
+                    // accumulator so the two latencies overlap
+                    const size_t o = (size_t)(t.m0 + row_in_tile) * p.N + t.n0 + c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) load16(p.aux + o + 8 * q, a + 8 * q);
+                }
                 uint32_t acc[32];
                 tmem_ld32(taddr + c, acc);
                 tmem_ld_wait();
-                epilogue_chunk<KIND>(p, t, row_in_tile, c, acc);
+                epilogue_chunk<KIND>(p, t, row_in_tile, c, acc, a);
             }
             tc_fence_before();
             mbar_arrive(tempty + buf);
@@ -402,6 +317,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                      : "memory");
     }
@@ -411,33 +327,6 @@ constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 16 *
                               16 + kMaxOffsets * sizeof(int);
 
 // ------------------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2D bf16 tensor [outer, inner] row-major, box {64, box_outer}, 128-byte swizzle, zero fill.
-bool make_map(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    auto fn = encode_fn();
-    if (!fn || outer == 0) return false;  // no silent fallback: the caller reports the failure
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int KIND, bool A_MN, bool B_MN>
 cudaError_t launch_kernel(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b, int grid,
                           cudaStream_t s) {

@@ -42,6 +42,11 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
                          int32_t* idx, float* w, int32_t* counts, float* balance_loss,
                          cudaStream_t s);
 
+// router_tc.cu: gate GEMM on tcgen05 + top-k + softmax + counts (bf16, d % 64 == 0)
+bool tc_route_supported(const moe_config_t& c);
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
+                            int32_t* idx, float* w, int32_t* counts, cudaStream_t s);
+
 // dispatch.cu: stable counting sort of the assignments by expert
 struct SortScratch {
     int32_t* blk_hist;     // [nblk, E]
@@ -74,17 +79,19 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t*
                            const float* w, void* y, cudaStream_t s);
 cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void* Yp,
                                const float* w, const int32_t* offsets, const int32_t* row_token,
-                               const int32_t* slot_row, void* dYp, float* dw, float* lossrow,
+                               const int32_t* slot_row, void* dYp, float* dw, float* lossblk,
                                cudaStream_t s);
+int combine_bwd_blocks(const moe_config_t& c);
 cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg,
                               const void* dXp, float* dz, void* dx, cudaStream_t s);
 int dwg_chunks(const moe_config_t& c);
 cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
                        const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s);
+// part: (rows_capacity / MOE_ROW_ALIGN) x width floats of scratch
 cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
-                             const int32_t* offsets, float* db, cudaStream_t s);
-cudaError_t launch_loss(const moe_config_t& c, const float* lossrow, const int32_t* offsets,
-                        const float* balance_loss, float* loss, cudaStream_t s);
+                             const int32_t* offsets, float* part, float* db, cudaStream_t s);
+cudaError_t launch_loss(const moe_config_t& c, const float* lossblk, const float* balance_loss,
+                        float* loss, cudaStream_t s);
 
 }  // namespace moe

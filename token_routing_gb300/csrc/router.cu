@@ -154,7 +154,10 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
                          cudaStream_t s) {
     cudaError_t st = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
     if (st != cudaSuccess) return st;
-    if (c.T > 0) {
+    if (c.T > 0 && tc_route_supported(c)) {
+        st = launch_route_tc(c, x, Wg, bg, idx, w, counts, s);
+        if (st != cudaSuccess) return st;
+    } else if (c.T > 0) {
         const size_t smem = sizeof(float) * ((size_t)kRouteTok * (kRouteKc + 1) +
                                              (size_t)c.E * (kRouteKc + 1) + (size_t)kRouteTok * c.E);
         const int grid = ceil_div(c.T, kRouteTok);

@@ -1,0 +1,221 @@
+// Router on the tensor cores: the gate linear z = x Wg^T as a tcgen05 GEMM (bf16 operands
+// staged by TMA, fp32 accumulation in TMEM), fused with the bias, the top-k selection
+// (ties -> lower expert id), the softmax over the k selected logits divided by the
+// temperature, and the per-expert counts.
+//
+// "Native MoE training system PithTrain", section 4.1 (gate, torch.topk, softmax over the
+// selected values); "Expert Parallelism: Scaling Mixture-of-Experts Models", section 2.2
+// (softmax(gate(x) / temperature), top-8 pre-selection) and section 5.5 (routing in FP32:
+// the logits stay fp32 from the accumulator to the softmax).
+//
+// One CTA per 128-token tile: warp 0 streams x and Wg tiles with TMA, warp 1 issues the
+// MMAs (N = E rounded up to 32), warps 2..5 read one token's E logits each from TMEM and
+// keep a sorted top-k list in registers. The kernel is bound by reading x from HBM.
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int RBM = 128;
+constexpr int RBK = 64;
+constexpr int RSTAGES = 4;
+constexpr int RTHREADS = 192;
+
+struct RouteTcParams {
+    int T, d, E, E_pad;
+    float inv_temp;
+    const float* bg;
+    int32_t* idx;
+    float* w;
+    int32_t* counts;
+    int* err;
+};
+
+__host__ __device__ constexpr int route_stage_bytes(int E_pad) { return RBM * RBK * 2 + E_pad * RBK * 2; }
+
+template <int K>
+__global__ void __launch_bounds__(RTHREADS, 1)
+route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmW) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stage_bytes = route_stage_bytes(p.E_pad);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * stage_bytes);
+    uint64_t* empty = full + RSTAGES;
+    uint64_t* tfull = empty + RSTAGES;
+    uint64_t* drain = tfull + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* s_cnt = reinterpret_cast<int*>(tmem_slot + 4);
+    float* s_bias = reinterpret_cast<float*>(s_cnt + MOE_MAX_EXPERTS);
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tok0 = blockIdx.x * RBM;
+    const int kblocks = (p.d + RBK - 1) / RBK;
+    const uint32_t ncols = p.E_pad <= 32 ? 32 : p.E_pad <= 64 ? 64 : p.E_pad <= 128 ? 128 : 256;
+
+    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) {
+        s_cnt[e] = 0;
+        s_bias[e] = (p.bg && e < p.E) ? p.bg[e] : 0.f;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RSTAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+        mbar_init(tfull, 1);
+        mbar_init(drain, 1);
+        s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, ncols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int kb = 0;
+            for (; kb < kblocks; ++kb) {
+                const int s = kb % RSTAGES;
+                const uint32_t ph = (kb / RSTAGES) & 1;
+                if (!mbar_wait(empty + s, ph ^ 1, p.err)) { ok = false; break; }
+                const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                mbar_expect_tx(full + s, stage_bytes);
+                tma_load_2d(sa, &tmX, kb * RBK, tok0, full + s);
+                tma_load_2d(sa + RBM * RBK * 2, &tmW, kb * RBK, 0, full + s);
+            }
+            if (!ok) {
+                s_fail = 1;
+                for (int j = kb > RSTAGES ? kb - RSTAGES : 0; j < kb; ++j)
+                    mbar_wait(full + j % RSTAGES, (j / RSTAGES) & 1, p.err);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(RBM, p.E_pad, false, false);
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                const int s = kb % RSTAGES;
+                const uint32_t ph = (kb / RSTAGES) & 1;
+                if (!mbar_wait(full + s, ph, p.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                const uint32_t sb = sa + RBM * RBK * 2;
+#pragma unroll
+                for (int kk = 0; kk < RBK / 16; ++kk)
+                    tc_mma(tmem_base, make_desc(sa + kk * 32, 16, 1024), make_desc(sb + kk * 32, 16, 1024), idesc,
+                           (kb > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(empty + s);
+            }
+            if (ok) tc_commit(tfull);
+            else s_fail = 1;
+            tc_commit(drain);
+            mbar_wait(drain, 0, p.err);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int tok = tok0 + row;
+        if (mbar_wait(tfull, 0, p.err)) {
+            tc_fence_after();
+            float tv[K];
+            int te[K];
+#pragma unroll
+            for (int j = 0; j < K; ++j) { tv[j] = -INFINITY; te[j] = -1; }
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+            for (int c = 0; c < p.E_pad; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(taddr + c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    int e = c + i;
+                    if (e < p.E) {
+                        float v = __uint_as_float(r[i]) + s_bias[e];
+                        // insert into the list sorted by (logit desc, id asc); experts arrive in
+                        // ascending id, so an equal logit never displaces an earlier one
+#pragma unroll
+                        for (int j = 0; j < K; ++j) {
+                            if (te[j] < 0 || v > tv[j]) {
+                                const float ov = tv[j];
+                                const int oe = te[j];
+                                tv[j] = v; te[j] = e;
+                                v = ov; e = oe;
+                            }
+                        }
+                    }
+                }
+            }
+            if (tok < p.T) {
+                float pr[K], s = 0.f;
+#pragma unroll
+                for (int j = 0; j < K; ++j) { pr[j] = expf((tv[j] - tv[0]) * p.inv_temp); s += pr[j]; }
+                const float inv = 1.f / s;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    p.idx[(size_t)tok * K + j] = te[j];
+                    p.w[(size_t)tok * K + j] = pr[j] * inv;
+                    atomicAdd(&s_cnt[te[j]], 1);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+        if (s_cnt[e]) atomicAdd(p.counts + e, s_cnt[e]);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, ncols);
+    }
+}
+
+template <int K>
+cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtensorMap& tw, size_t smem,
+                     cudaStream_t s) {
+    auto kern = route_tc_kernel<K>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<ceil_div(p.T, RBM), RTHREADS, smem, s>>>(p, tx, tw);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_route_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && c.d % 64 == 0; }
+
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
+                            int32_t* idx, float* w, int32_t* counts, cudaStream_t s) {
+    RouteTcParams p{};
+    p.T = c.T; p.d = c.d; p.E = c.E;
+    p.E_pad = (c.E + 31) / 32 * 32;
+    p.inv_temp = 1.0f / c.temperature;
+    p.bg = c.has_gate_bias ? bg : nullptr;
+    p.idx = idx; p.w = w; p.counts = counts;
+    p.err = device_error_word();
+    CUtensorMap tx, tw;
+    if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, RBM)) return cudaErrorInvalidValue;
+    if (!make_map(&tw, Wg, (uint64_t)c.d, (uint64_t)c.E, (uint32_t)p.E_pad)) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)RSTAGES * route_stage_bytes(p.E_pad) + 16 * sizeof(uint64_t) + 16 +
+                        2 * MOE_MAX_EXPERTS * sizeof(int);
+    switch (c.k) {
+        case 1: return launch_k<1>(p, tx, tw, smem, s);
+        case 2: return launch_k<2>(p, tx, tw, smem, s);
+        case 3: return launch_k<3>(p, tx, tw, smem, s);
+        case 4: return launch_k<4>(p, tx, tw, smem, s);
+        case 5: return launch_k<5>(p, tx, tw, smem, s);
+        case 6: return launch_k<6>(p, tx, tw, smem, s);
+        case 7: return launch_k<7>(p, tx, tw, smem, s);
+        case 8: return launch_k<8>(p, tx, tw, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe
