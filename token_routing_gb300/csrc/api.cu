@@ -82,7 +82,8 @@ struct BackwardScratch {
     float* dz;
     float* lossblk;
     float* dwg_part;
-    float* colsum_part;
+    float* colsum_d;    // column-sum partials of dYp (db2)
+    float* colsum_f;    // column-sum partials of dA (db1)
 };
 
 size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
@@ -97,7 +98,8 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     b->dz = ws.take<float>((size_t)c.T * c.k + 1);
     b->lossblk = ws.take<float>((size_t)combine_bwd_blocks(c) + 1);
     b->dwg_part = ws.take<float>((size_t)c.E * dwg_chunks(c) * c.d);
-    b->colsum_part = ws.take<float>((R / MOE_ROW_ALIGN) * (size_t)std::max(c.d, c.d_ff) + 1);
+    b->colsum_d = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d + 1);
+    b->colsum_f = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d_ff + 1);
     return align_up(ws.used, 256);
 }
 
@@ -239,6 +241,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     // experts backward
     RowGemmArgs gh{};
     gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = A; gh.out0 = b.dA;
+    gh.colsum = use_tc(c) ? b.colsum_f : nullptr;  // the tensor-core epilogue sums dA columns
     gh.offsets = offsets; gh.E = c.E; gh.N = c.d_ff; gh.K = c.d; gh.rows_capacity = c.rows_capacity;
     gh.sBe = (long long)c.d * c.d_ff; gh.sBn = 1; gh.sBk = c.d_ff;
     MOE_TRY(row_gemm(c, gh, s));
@@ -251,8 +254,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     MOE_TRY(wgrad(c, w2, s));
     WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
     MOE_TRY(wgrad(c, w1, s));
-    MOE_TRY(launch_bias_grad(c, b.dYp, c.d, offsets, b.colsum_part, db2, s));
-    MOE_TRY(launch_bias_grad(c, b.dA, c.d_ff, offsets, b.colsum_part, db1, s));
+    MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, s));
+    MOE_TRY(launch_bias_reduce(c, b.colsum_d, c.d, offsets, db2, s));
+    if (!use_tc(c)) MOE_TRY(launch_colsum(c, b.dA, c.d_ff, offsets, b.colsum_f, s));
+    MOE_TRY(launch_bias_reduce(c, b.colsum_f, c.d_ff, offsets, db1, s));
     // router backward: assignment sort, softmax Jacobian, dx, dWg, dbg
     MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
     MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));

@@ -288,15 +288,16 @@ dbg_kernel(const float* __restrict__ dz, const int32_t* __restrict__ assign_off,
     if (threadIdx.x == 0) dbg[e] = red[0];
 }
 
-// Column sums of one 128-row tile (tiles never straddle buckets; padding rows are zero):
-// part[tile, c] = sum of M[r, c] over the tile's rows, rows in order.
+// Column sums of one 32-row quarter of a 128-row tile (tiles never straddle buckets;
+// padding rows are zero): part[tile * 4 + quarter, c] = sum of M[r, c] over the quarter's rows.
 template <typename T>
 __global__ void __launch_bounds__(256)
-colsum_tile_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets, int E,
-                   float* __restrict__ part) {
+colsum_quarter_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets, int E,
+                      float* __restrict__ part) {
     constexpr int V = Vec16<T>::N;
-    const int tile = blockIdx.y;
-    const int r0 = tile * MOE_ROW_ALIGN;
+    constexpr int QROWS = MOE_ROW_ALIGN / kColsumParts;
+    const int pq = blockIdx.y;  // tile * 4 + quarter
+    const int r0 = pq * QROWS;
     if (r0 >= offsets[E]) return;
     if (width % V == 0) {
         const int c = (blockIdx.x * blockDim.x + threadIdx.x) * V;
@@ -305,34 +306,34 @@ colsum_tile_kernel(const T* __restrict__ M, int width, const int32_t* __restrict
 #pragma unroll
         for (int q = 0; q < V; ++q) acc[q] = 0.f;
 #pragma unroll 8
-        for (int r = 0; r < MOE_ROW_ALIGN; ++r) {
+        for (int r = 0; r < QROWS; ++r) {
             float v[V];
             load16(M + (size_t)(r0 + r) * width + c, v);
 #pragma unroll
             for (int q = 0; q < V; ++q) acc[q] += v[q];
         }
 #pragma unroll
-        for (int q = 0; q < V; ++q) part[(size_t)tile * width + c + q] = acc[q];
+        for (int q = 0; q < V; ++q) part[(size_t)pq * width + c + q] = acc[q];
     } else {
-        for (int c = blockIdx.x * blockDim.x * V + threadIdx.x; c < min(width, (int)((blockIdx.x + 1) * blockDim.x * V));
-             c += blockDim.x) {
+        const int cend = min(width, (int)((blockIdx.x + 1) * blockDim.x * V));
+        for (int c = blockIdx.x * blockDim.x * V + threadIdx.x; c < cend; c += blockDim.x) {
             float acc = 0.f;
-            for (int r = 0; r < MOE_ROW_ALIGN; ++r) acc += ld_f(M + (size_t)(r0 + r) * width + c);
-            part[(size_t)tile * width + c] = acc;
+            for (int r = 0; r < QROWS; ++r) acc += ld_f(M + (size_t)(r0 + r) * width + c);
+            part[(size_t)pq * width + c] = acc;
         }
     }
 }
 
-// db[e, c] = sum over the tiles of bucket e of part[tile, c], tiles in order.
+// db[e, c] = sum over the quarters of bucket e's tiles of part[., c], in order.
 __global__ void __launch_bounds__(256)
 bias_reduce_kernel(const float* __restrict__ part, int width, const int32_t* __restrict__ offsets,
                    float* __restrict__ db) {
     const int e = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= width) return;
-    const int t0 = offsets[e] / MOE_ROW_ALIGN, t1 = offsets[e + 1] / MOE_ROW_ALIGN;
+    const int q0 = offsets[e] / MOE_ROW_ALIGN * kColsumParts, q1 = offsets[e + 1] / MOE_ROW_ALIGN * kColsumParts;
     float acc = 0.f;
-    for (int t = t0; t < t1; ++t) acc += part[(size_t)t * width + c];
+    for (int q = q0; q < q1; ++q) acc += part[(size_t)q * width + c];
     db[(size_t)e * width + c] = acc;
 }
 
@@ -442,20 +443,25 @@ cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
     return cudaGetLastError();
 }
 
-cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
-                             const int32_t* offsets, float* part, float* db, cudaStream_t s) {
-    const int tiles = c.rows_capacity / MOE_ROW_ALIGN;
-    if (tiles > 0) {
-        const int V = c.dtype == MOE_BF16 ? 8 : 4;
-        dim3 g1(ceil_div(width, 256 * V), tiles);
-        if (c.dtype == MOE_BF16)
-            colsum_tile_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>((const __nv_bfloat16*)M, width, offsets, c.E, part);
-        else
-            colsum_tile_kernel<float><<<g1, 256, 0, s>>>((const float*)M, width, offsets, c.E, part);
-        count_launch();
-    }
-    dim3 g2(ceil_div(width, 256), c.E);
-    bias_reduce_kernel<<<g2, 256, 0, s>>>(part, width, offsets, db);
+cudaError_t launch_colsum(const moe_config_t& c, const void* M, int width, const int32_t* offsets,
+                          float* part, cudaStream_t s) {
+    const int quarters = c.rows_capacity / MOE_ROW_ALIGN * kColsumParts;
+    if (quarters == 0) return cudaSuccess;
+    const int V = c.dtype == MOE_BF16 ? 8 : 4;
+    const int threads = std::max(32, std::min(256, (ceil_div(width, V) + 31) / 32 * 32));
+    dim3 g(ceil_div(width, threads * V), quarters);
+    if (c.dtype == MOE_BF16)
+        colsum_quarter_kernel<__nv_bfloat16><<<g, threads, 0, s>>>((const __nv_bfloat16*)M, width, offsets, c.E, part);
+    else
+        colsum_quarter_kernel<float><<<g, threads, 0, s>>>((const float*)M, width, offsets, c.E, part);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bias_reduce(const moe_config_t& c, const float* part, int width,
+                               const int32_t* offsets, float* db, cudaStream_t s) {
+    dim3 g(ceil_div(width, 256), c.E);
+    bias_reduce_kernel<<<g, 256, 0, s>>>(part, width, offsets, db);
     count_launch();
     return cudaGetLastError();
 }

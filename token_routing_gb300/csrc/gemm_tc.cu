@@ -38,6 +38,10 @@ constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, each 
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int kMaxOffsets = MOE_MAX_EXPERTS + 1;
+// Epilogue staging: per epilogue warp two 2 KB buffers of 32 rows x 64 bytes (64-byte
+// swizzle) from which TMA stores write coalesced 32x32 bf16 boxes.
+constexpr int STG_BYTES = 2048;
+constexpr int EPI_SMEM = EPI_WARPS * 2 * STG_BYTES;
 
 struct TcParams {
     int kind;                 // GemmKind
@@ -48,6 +52,7 @@ struct TcParams {
     const __nv_bfloat16* aux;    // [rows, N] (A of the forward, for dH)
     __nv_bfloat16* out0;
     __nv_bfloat16* out1;
+    float* colsum;               // dH: per-(tile, lane quarter) column sums of dA, or null
     int* err;
 };
 
@@ -102,40 +107,107 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v) 
     for (int q = 0; q < 4; ++q) store16(dst + 8 * q, v + 8 * q);
 }
 
-template <int KIND>
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Tile& t, int row_in_tile,
-                                               int c, const uint32_t (&acc)[32], const float (&a)[32]) {
-    float v[32];
+// 32 bf16 (64 bytes) as raw vectors: fetched one chunk ahead of their use.
+struct Raw32 {
+    uint4 q[4];
+};
+__device__ __forceinline__ void load_raw32(Raw32& r, const __nv_bfloat16* src) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-    const int n = t.n0 + c;
-    if (KIND == kGemmWgrad) {
-        const int m = t.m0 + row_in_tile;
-        if (m < p.M) store_row32(p.out0 + ((size_t)t.e * p.M + m) * p.N + n, v);
-        return;
-    }
-    const size_t o = (size_t)(t.m0 + row_in_tile) * p.N + n;
-    if (KIND == kGemmFfn1 || KIND == kGemmFfn2) {
-        const __nv_bfloat16* b = p.bias + (size_t)t.e * p.N + n;
-        float bv[32];
+    for (int i = 0; i < 4; ++i) r.q[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+}
+__device__ __forceinline__ void unpack_raw32(const Raw32& r, float* out) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) load16(b + 8 * q, bv + 8 * q);
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.q[i]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] += bv[i];
-        store_row32(p.out0 + o, v);
-        if (KIND == kGemmFfn1) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
-            store_row32(p.out1 + o, v);
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            out[8 * i + 2 * j] = f.x;
+            out[8 * i + 2 * j + 1] = f.y;
         }
-    } else if (KIND == kGemmDH) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
-        store_row32(p.out0 + o, v);
-    } else {
-        store_row32(p.out0 + o, v);
     }
 }
+
+// Column sums of a warp's 32 rows x 32 columns (one row per lane, v[i] = column i):
+// a butterfly that halves the columns each lane carries; lane l ends with column l.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool hi = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = hi ? v[i] : v[i + s];
+            const float keep = hi ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+template <int KIND>
+constexpr bool has_bias() { return KIND == kGemmFfn1 || KIND == kGemmFfn2; }
+
+__device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int j) {
+    return base + row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
+}
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return u;
+}
+__device__ __forceinline__ void unpack8(const uint4& u, float* out) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// One epilogue warp's staging buffers and store count (buffer = count & 1).
+struct Stager {
+    uint32_t base;
+    int count;
+    // Returns the next buffer once the TMA store that last read it has finished.
+    __device__ __forceinline__ uint32_t acquire(int lane) {
+        if (lane == 0 && count >= 2) bulk_wait_read1();
+        __syncwarp();
+        return base + (count & 1) * STG_BYTES;
+    }
+    // Writes the lane's row (32 values) into `buf`, then one TMA store of the 32x32 box.
+    __device__ __forceinline__ void store(int lane, uint32_t buf, const float* v, const CUtensorMap* tm, int x, int y) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf, lane, j), pack8(v + 8 * j));
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, buf, x, y);
+            bulk_commit();
+        }
+        ++count;
+    }
+};
 
 template <int KIND>
 __device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
@@ -153,18 +225,20 @@ __device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, 
 template <int KIND, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
-               const __grid_constant__ CUtensorMap tmB) {
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO0,
+               const __grid_constant__ CUtensorMap tmO1) {
     constexpr bool WGRAD = (KIND == kGemmWgrad);
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* stg_smem = smem + STAGES * STAGE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg_smem + EPI_SMEM);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* s_fail = reinterpret_cast<volatile int*>(tmem_slot + 1);  // a role gave up
     int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
-    __shared__ int s_fail;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -174,7 +248,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         for (int s = 0; s < STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, EPI_THREADS); }
         mbar_init(drain, 1);
-        s_fail = 0;
+        *s_fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -227,7 +301,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                 }
             }
             if (!ok) {
-                s_fail = 1;
+                *s_fail = 1;
                 // let every copy already issued land before shared memory goes away
                 const uint32_t first = it > STAGES ? it - STAGES : 0;
                 for (uint32_t j = first; j < it; ++j) mbar_wait(full + j % STAGES, (j / STAGES) & 1, p.err);
@@ -269,7 +343,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                 if (!ok) break;
                 tc_commit(tfull + buf);    // accumulator ready for the epilogue
             }
-            if (!ok) s_fail = 1;
+            if (!ok) *s_fail = 1;
             // drain: every MMA issued so far has completed before TMEM is released
             tc_commit(drain);
             mbar_wait(drain, 0, p.err);
@@ -279,6 +353,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
         const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
         uint32_t tl = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Tile t = decode_tile<WGRAD>(p, s_off, tile);
@@ -289,28 +364,84 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             const int buf = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            // side input of the first chunk, fetched while the accumulator is being produced:
+            // the bias row (same for every lane) or, for dH, the forward pre-activation A read
+            // coalesced (lane l: row (l>>2)+8i of the warp's 32 rows, 16-byte segment l&3)
+            const size_t aux_row0 = (size_t)(t.m0 + quarter * 32 + (lane >> 2));
+            Raw32 next;
+            if (t.n0 + c_lo < p.N) {
+                if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
+                if (KIND == kGemmDH)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + t.n0 + c_lo + (lane & 3) * 8));
+            }
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
             for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
                 if (t.n0 + c >= p.N) break;
-                float a[32];
-                if (KIND == kGemmDH) {
-                    // forward pre-activation of this row's 32 columns, fetched before the
-                    // accumulator so the two latencies overlap
-                    const size_t o = (size_t)(t.m0 + row_in_tile) * p.N + t.n0 + c;
+                const int n = t.n0 + c;
+                const Raw32 cur = next;
+                const bool more = c + 32 < c_lo + BN / 2 && n + 32 < p.N;
+                if (more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
+                if (more && KIND == kGemmDH)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) load16(p.aux + o + 8 * q, a + 8 * q);
-                }
+                    for (int i = 0; i < 4; ++i)
+                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
                 uint32_t acc[32];
                 tmem_ld32(taddr + c, acc);
                 tmem_ld_wait();
-                epilogue_chunk<KIND>(p, t, row_in_tile, c, acc, a);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                const int y = t.m0 + quarter * 32;
+                if (KIND == kGemmWgrad) {
+                    const uint32_t b = st.acquire(lane);
+                    if (t.m0 + quarter * 32 < p.M) st.store(lane, b, v, &tmO0, n, t.e * p.M + y);
+                } else if (KIND == kGemmFfn1 || KIND == kGemmFfn2) {
+                    float bv[32];
+                    unpack_raw32(cur, bv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] += bv[i];
+                    uint32_t b = st.acquire(lane);
+                    st.store(lane, b, v, &tmO0, n, y);
+                    if (KIND == kGemmFfn1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+                        b = st.acquire(lane);
+                        st.store(lane, b, v, &tmO1, n, y);
+                    }
+                } else if (KIND == kGemmDH) {
+                    // transpose the coalesced A chunk through the staging buffer: lane = row
+                    const uint32_t b = st.acquire(lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sts128(sw64_addr(b, (lane >> 2) + 8 * i, lane & 3), cur.q[i]);
+                    __syncwarp();
+                    float a[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) unpack8(lds128(sw64_addr(b, lane, j)), a + 8 * j);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
+                    st.store(lane, b, v, &tmO0, n, y);
+                    if (p.colsum) {
+                        // db1 partial of this tile's lane quarter (32 rows), fixed-order butterfly
+                        const float sum = warp_colsum32(v, lane);
+                        p.colsum[((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n + lane] = sum;
+                    }
+                } else {
+                    const uint32_t b = st.acquire(lane);
+                    st.store(lane, b, v, &tmO0, n, y);
+                }
             }
             tc_fence_before();
             mbar_arrive(tempty + buf);
-            if (s_fail) break;
+            if (*s_fail) break;
         }
+        // every TMA store has finished before the CTA's shared memory is released
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -323,17 +454,17 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     }
 }
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 16 * sizeof(uint64_t) +
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_SMEM + 16 * sizeof(uint64_t) +
                               16 + kMaxOffsets * sizeof(int);
 
 // ------------------------------------------------------------------------- host side
 template <int KIND, bool A_MN, bool B_MN>
-cudaError_t launch_kernel(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b, int grid,
-                          cudaStream_t s) {
+cudaError_t launch_kernel(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                          const CUtensorMap& o1, int grid, cudaStream_t s) {
     auto kern = tc_gemm_kernel<KIND, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, kSmemBytes, s>>>(p, a, b);
+    kern<<<grid, THREADS, kSmemBytes, s>>>(p, a, b, o0, o1);
     count_launch();
     return cudaGetLastError();
 }
@@ -357,6 +488,7 @@ cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cuda
     p.aux = static_cast<const __nv_bfloat16*>(a.aux);
     p.out0 = static_cast<__nv_bfloat16*>(a.out0);
     p.out1 = static_cast<__nv_bfloat16*>(a.out1);
+    p.colsum = a.colsum;
     p.err = device_error_word();
     CUtensorMap ta, tb;
     // A: activations [rows, K], K-major tiles of 128 rows
@@ -369,13 +501,23 @@ cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cuda
         // B(n, k) = W[e*K + k][n]: N-major, [E*K, N], boxes of 64 n x 64 k
         if (!make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.E * a.K, BK)) return cudaErrorInvalidValue;
     }
+    // epilogue stores: 32 x 32 boxes, 64-byte swizzle (matches the staging layout)
+    CUtensorMap to0, to1;
+    if (!make_map_ex(&to0, a.out0, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    if (a.kind == kGemmFfn1) {
+        if (!make_map_ex(&to1, a.out1, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else {
+        to1 = to0;
+    }
     const long long max_tiles = (long long)p.m_tiles * p.n_tiles;
     const int grid = (int)std::max(1LL, std::min<long long>(max_tiles, num_sms()));
     switch (a.kind) {
-        case kGemmFfn1: return launch_kernel<kGemmFfn1, false, false>(p, ta, tb, grid, s);
-        case kGemmFfn2: return launch_kernel<kGemmFfn2, false, false>(p, ta, tb, grid, s);
-        case kGemmDH: return launch_kernel<kGemmDH, false, true>(p, ta, tb, grid, s);
-        case kGemmDX: return launch_kernel<kGemmDX, false, true>(p, ta, tb, grid, s);
+        case kGemmFfn1: return launch_kernel<kGemmFfn1, false, false>(p, ta, tb, to0, to1, grid, s);
+        case kGemmFfn2: return launch_kernel<kGemmFfn2, false, false>(p, ta, tb, to0, to1, grid, s);
+        case kGemmDH: return launch_kernel<kGemmDH, false, true>(p, ta, tb, to0, to1, grid, s);
+        case kGemmDX: return launch_kernel<kGemmDX, false, true>(p, ta, tb, to0, to1, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -394,9 +536,12 @@ cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStrea
     // A(m, k=row) = P[row][m]: M-major, boxes of 64 m x 64 rows; B(n, k=row) = Q[row][n]
     if (!make_map(&ta, a.P, (uint64_t)a.M, rows, BK)) return cudaErrorInvalidValue;
     if (!make_map(&tb, a.Q, (uint64_t)a.N, rows, BK)) return cudaErrorInvalidValue;
+    CUtensorMap to0;
+    if (!make_map_ex(&to0, a.C, (uint64_t)a.N, (uint64_t)a.E * a.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     const long long tiles = (long long)a.E * p.m_tiles * p.n_tiles;
     const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms()));
-    return launch_kernel<kGemmWgrad, true, true>(p, ta, tb, grid, s);
+    return launch_kernel<kGemmWgrad, true, true>(p, ta, tb, to0, to0, grid, s);
 }
 
 }  // namespace moe

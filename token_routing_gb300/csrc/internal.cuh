@@ -24,6 +24,7 @@ struct RowGemmArgs {
     void* out0;             // [rows, N]
     void* out1;             // [rows, N] (H of Ffn1)
     const int32_t* offsets; // [E+1] bucket starts
+    float* colsum;          // DH on tensor cores: column-sum partials of dA [tiles*4, N], or null
     int E, N, K;
     int rows_capacity;
     long long sBe, sBn, sBk; // element strides of B: expert, output column, reduction index
@@ -88,9 +89,13 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
 int dwg_chunks(const moe_config_t& c);
 cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
                        const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s);
-// part: (rows_capacity / MOE_ROW_ALIGN) x width floats of scratch
-cudaError_t launch_bias_grad(const moe_config_t& c, const void* M, int width,
-                             const int32_t* offsets, float* part, float* db, cudaStream_t s);
+// Bias gradients: column sums of a bucketed matrix. Partials hold one row per 32-row quarter
+// of every 128-row tile: part [(rows_capacity / MOE_ROW_ALIGN) * 4, width] floats.
+constexpr int kColsumParts = 4;
+cudaError_t launch_colsum(const moe_config_t& c, const void* M, int width, const int32_t* offsets,
+                          float* part, cudaStream_t s);
+cudaError_t launch_bias_reduce(const moe_config_t& c, const float* part, int width,
+                               const int32_t* offsets, float* db, cudaStream_t s);
 cudaError_t launch_loss(const moe_config_t& c, const float* lossblk, const float* balance_loss,
                         float* loss, cudaStream_t s);
 

@@ -144,18 +144,24 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D bf16 tensor [outer, inner] row-major, box {64, box_outer}, 128-byte swizzle, zero fill.
-inline bool make_map(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// 2D bf16 tensor [outer, inner] row-major, box {box_inner, box_outer}, zero fill.
+inline bool make_map_ex(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer, CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn || outer == 0) return false;  // no silent fallback: the caller reports the failure
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Operand tiles: box {64, box_outer}, 128-byte swizzle.
+inline bool make_map(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    return make_map_ex(tm, base, inner, outer, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 
