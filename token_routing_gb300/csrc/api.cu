@@ -109,7 +109,7 @@ cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s
     return use_tc(c) ? launch_row_gemm_tc(c, a, s) : launch_row_gemm_simt(c, a, s);
 }
 cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
-    return use_tc(c) ? launch_wgrad_tc(c, a, s) : launch_wgrad_simt(c, a, s);
+    return use_tc(c) ? launch_wgrad_tc_pair(c, a, s) : launch_wgrad_simt(c, a, s);
 }
 
 }  // namespace

@@ -1,0 +1,369 @@
+// Grouped expert GEMMs on CTA pairs: tcgen05.mma.cta_group::2 over 256 x 256 x 64 tiles.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile: each CTA stages its own
+// 128 rows of A and its half (128 columns) of B, so a stage is 32 KB instead of 48 KB and six
+// stages fit where four fitted before (about 1.5x deeper lookahead per SM, half the B traffic).
+// The leader CTA (cluster rank 0) issues the MMAs for the pair; the accumulator rows of each
+// CTA land in its own TMEM, and each CTA drains and stores its own 128 rows.
+//
+// Synchronisation: both CTAs' TMA loads complete on the leader's "full" barrier (the leader
+// expects the pair's bytes); the leader's commits arrive on both CTAs' "empty" and
+// "accumulator full" barriers (multicast); both CTAs' epilogue threads arrive on the leader's
+// "accumulator empty" barrier. Every wait is bounded and records a device error on expiry.
+// Cluster barriers order the barrier initialisation before any remote access, and the end of
+// all work in both CTAs before the pair releases its TMEM.
+//
+// The arithmetic per kind is the same as the one-CTA kernel (gemm_tc.cu): the expert FFN
+// Linear(d, d_ff) -> GELU -> Linear(d_ff, d) ("PyTorch distributed MoE training", section 3.2)
+// and its backward.
+#include "tc_gemm_common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int P_BM = 256;                           // pair tile rows (128 per CTA)
+constexpr int P_HALF = 128;
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = P_HALF * BK * 2;          // 16 KB per CTA
+constexpr int P_B_BYTES = P_HALF * BK * 2;          // 16 KB per CTA: half of B's 256 columns
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t o;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(o) : "r"(addr), "r"(rank));
+    return o;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA tile load into this CTA's shared memory that completes on the leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                                 uint32_t mbar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(mbar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// Arrives on the barrier at this shared-memory offset in both CTAs of the pair once the
+// leader's MMAs issued so far have completed.
+__device__ __forceinline__ void commit_pair_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+__device__ __forceinline__ void commit_pair_local(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+struct PairTile {
+    int e, m0, n0, row0, kblocks;
+};
+
+template <bool WGRAD>
+__device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const int* s_off, int tile) {
+    PairTile t;
+    const int nt = tile % p.n_tiles;
+    const int rest = tile / p.n_tiles;
+    t.n0 = nt * BN;
+    if (WGRAD) {
+        t.m0 = (rest % p.m_tiles) * P_BM;
+        t.e = rest / p.m_tiles;
+        t.row0 = s_off[t.e];
+        t.kblocks = (s_off[t.e + 1] - s_off[t.e]) / BK;
+    } else {
+        t.m0 = rest * P_BM;          // buckets are 256-row aligned on this path
+        t.e = bucket_of(s_off, p.E, t.m0);
+        t.row0 = t.m0;
+        t.kblocks = p.K / BK;
+    }
+    return t;
+}
+
+template <int KIND, bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1) {
+    constexpr bool WGRAD = (KIND == kGemmWgrad);
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stg_smem = smem + P_STAGES * P_STAGE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg_smem + EPI_SMEM);
+    uint64_t* empty = full + P_STAGES;
+    uint64_t* tfull = empty + P_STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* s_fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = (rank == 0);
+    const int cluster_id = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, 2 * EPI_THREADS); }
+        mbar_init(drain, 1);
+        *s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive or complete_tx
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = WGRAD ? p.E * p.m_tiles * p.n_tiles : (s_off[p.E] / P_BM) * p.n_tiles;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs): own A rows, own half of B
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
+                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, tile);
+                const int mr = t.m0 + (int)rank * P_HALF;   // this CTA's rows of the tile
+                const int nh = t.n0 + (int)rank * P_HALF;   // this CTA's half of B's columns
+                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const int s = it % P_STAGES;
+                    const uint32_t ph = (it / P_STAGES) & 1;
+                    if (!mbar_wait(empty + s, ph ^ 1, p.err)) { ok = false; break; }
+                    const uint32_t sa = smem_u32(smem + s * P_STAGE_BYTES);
+                    const uint32_t sb = sa + P_A_BYTES;
+                    const uint32_t fb = map_to_rank(smem_u32(full + s), 0);
+                    if (leader) mbar_expect_tx(full + s, 2 * P_STAGE_BYTES);
+                    const int k0 = kb * BK;
+                    if (!A_MN) {
+                        tma_load_2d_pair(sa, &tmA, k0, WGRAD ? t.row0 + (mr - t.m0) : mr, fb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < P_HALF / 64; ++j)
+                            tma_load_2d_pair(sa + j * (BK * 128), &tmA, mr + 64 * j, t.row0 + k0, fb);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d_pair(sb, &tmB, k0, t.e * p.N + nh, fb);
+                    } else if (WGRAD) {
+#pragma unroll
+                        for (int j = 0; j < P_HALF / 64; ++j)
+                            tma_load_2d_pair(sb + j * (BK * 128), &tmB, nh + 64 * j, t.row0 + k0, fb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < P_HALF / 64; ++j)
+                            tma_load_2d_pair(sb + j * (BK * 128), &tmB, nh + 64 * j, t.e * p.K + k0, fb);
+                    }
+                }
+            }
+            if (!ok) *s_fail = 1;
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: one thread of the leader CTA drives the pair
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_bf16(P_BM, BN, A_MN, B_MN);
+            uint32_t it = 0, tl = 0;
+            bool ok = true;
+            for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
+                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, tile);
+                if (t.kblocks == 0) continue;
+                const int buf = tl & 1;
+                const uint32_t aph = (tl >> 1) & 1;
+                ++tl;
+                if (!mbar_wait(tempty + buf, aph ^ 1, p.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const int s = it % P_STAGES;
+                    const uint32_t ph = (it / P_STAGES) & 1;
+                    if (!mbar_wait(full + s, ph, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * P_STAGE_BYTES);
+                    const uint32_t sb = sa + P_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = A_MN ? make_desc(sa + kk * UMMA_K * 128, BK * 128, 1024)
+                                                 : make_desc(sa + kk * UMMA_K * 2, 16, 1024);
+                        const uint64_t bd = B_MN ? make_desc(sb + kk * UMMA_K * 128, BK * 128, 1024)
+                                                 : make_desc(sb + kk * UMMA_K * 2, 16, 1024);
+                        mma_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    commit_pair_both(empty + s);   // frees the stage in both CTAs
+                }
+                if (!ok) break;
+                commit_pair_both(tfull + buf);     // both CTAs' accumulator rows are ready
+            }
+            if (!ok) *s_fail = 1;
+            commit_pair_local(drain);
+            mbar_wait(drain, 0, p.err);
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
+        const int quarter = warp & 3;
+        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
+        const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(tempty), 0), map_to_rank(smem_u32(tempty + 1), 0)};
+        uint32_t tl = 0;
+        for (int tile = cluster_id; tile < num_tiles; tile += nclusters) {
+            const PairTile pt = decode_pair_tile<WGRAD>(p, s_off, tile);
+            Tile t;
+            t.e = pt.e; t.n0 = pt.n0; t.row0 = pt.row0; t.kblocks = pt.kblocks;
+            t.m0 = pt.m0 + (int)rank * P_HALF;  // this CTA's rows
+            const int row_in_tile = quarter * 32 + lane;
+            if (t.kblocks == 0) {
+                if (WGRAD) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
+                continue;
+            }
+            const int buf = tl & 1;
+            const uint32_t aph = (tl >> 1) & 1;
+            ++tl;
+            const size_t aux_row0 = (size_t)(t.m0 + quarter * 32 + (lane >> 2));
+            Raw32 next;
+            if (t.n0 + c_lo < p.N) {
+                if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
+                if (KIND == kGemmDH)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + t.n0 + c_lo + (lane & 3) * 8));
+            }
+            if (!mbar_wait(tfull + buf, aph, p.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
+            for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
+                if (t.n0 + c >= p.N) break;
+                const int n = t.n0 + c;
+                const Raw32 cur = next;
+                const bool more = c + 32 < c_lo + BN / 2 && n + 32 < p.N;
+                if (more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
+                if (more && KIND == kGemmDH)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
+                uint32_t acc[32];
+                tmem_ld32(taddr + c, acc);
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                const int y = t.m0 + quarter * 32;
+                if (KIND == kGemmWgrad) {
+                    const uint32_t b = st.acquire(lane);
+                    if (y < p.M) st.store(lane, b, v, &tmO0, n, t.e * p.M + y);
+                } else if (KIND == kGemmFfn1 || KIND == kGemmFfn2) {
+                    float bv[32];
+                    unpack_raw32(cur, bv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] += bv[i];
+                    uint32_t b = st.acquire(lane);
+                    st.store(lane, b, v, &tmO0, n, y);
+                    if (KIND == kGemmFfn1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+                        b = st.acquire(lane);
+                        st.store(lane, b, v, &tmO1, n, y);
+                    }
+                } else if (KIND == kGemmDH) {
+                    const uint32_t b = st.acquire(lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sts128(sw64_addr(b, (lane >> 2) + 8 * i, lane & 3), cur.q[i]);
+                    __syncwarp();
+                    float a[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) unpack8(lds128(sw64_addr(b, lane, j)), a + 8 * j);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
+                    st.store(lane, b, v, &tmO0, n, y);
+                    if (p.colsum) {
+                        const float sum = warp_colsum32(v, lane);
+                        p.colsum[((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n + lane] = sum;
+                    }
+                } else {
+                    const uint32_t b = st.acquire(lane);
+                    st.store(lane, b, v, &tmO0, n, y);
+                }
+            }
+            tc_fence_before();
+            if (leader) mbar_arrive(tempty + buf);
+            else mbar_arrive_cluster(tempty_leader[buf]);
+            if (*s_fail) break;
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // all work of both CTAs is done before the pair releases its TMEM
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+constexpr size_t kPairSmemBytes = 1024 + P_STAGES * P_STAGE_BYTES + EPI_SMEM + 16 * sizeof(uint64_t) + 16 +
+                                  kMaxOffsets * sizeof(int);
+
+template <int KIND, bool A_MN, bool B_MN>
+cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                        const CUtensorMap& o1, int clusters, cudaStream_t s) {
+    auto kern = tc_gemm_pair_kernel<KIND, A_MN, B_MN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<2 * clusters, THREADS, kPairSmemBytes, s>>>(p, a, b, o0, o1);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
+    TcParams p{};
+    p.kind = kGemmWgrad;
+    p.offsets = a.offsets;
+    p.E = a.E; p.N = a.N; p.M = a.M; p.K = 0;
+    p.n_tiles = ceil_div(a.N, BN);
+    p.m_tiles = ceil_div(a.M, P_BM);
+    p.out0 = static_cast<__nv_bfloat16*>(a.C);
+    p.err = device_error_word();
+    CUtensorMap ta, tb, to0;
+    const uint64_t rows = (uint64_t)std::max(c.rows_capacity, 1);
+    if (!make_map(&ta, a.P, (uint64_t)a.M, rows, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, a.Q, (uint64_t)a.N, rows, BK)) return cudaErrorInvalidValue;
+    if (!make_map_ex(&to0, a.C, (uint64_t)a.N, (uint64_t)a.E * a.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    const long long tiles = (long long)a.E * p.m_tiles * p.n_tiles;
+    const int clusters = (int)std::max(1LL, std::min<long long>(tiles, num_sms() / 2));
+    return launch_pair<kGemmWgrad, true, true>(p, ta, tb, to0, to0, clusters, s);
+}
+
+}  // namespace moe

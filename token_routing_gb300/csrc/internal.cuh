@@ -74,6 +74,8 @@ cudaError_t launch_wgrad_simt(const moe_config_t& c, const WgradArgs& a, cudaStr
 bool tc_gemm_supported(const moe_config_t& c);
 cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
 cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
+// gemm_tc_pair.cu: weight gradients on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles)
+cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,

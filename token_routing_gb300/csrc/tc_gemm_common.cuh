@@ -1,0 +1,210 @@
+// Pieces shared by the tcgen05 grouped-GEMM kernels (one-CTA and CTA-pair variants): tile
+// geometry, kernel parameters, bucket lookup, and the epilogue's staging / TMA-store helpers.
+#pragma once
+
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                    // one 128-byte swizzle atom of bf16 along K
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_BYTES = BN * BK * 2;      // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;         // two accumulator buffers
+constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, each on half the columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int kMaxOffsets = MOE_MAX_EXPERTS + 1;
+// Epilogue staging: per epilogue warp two 2 KB buffers of 32 rows x 64 bytes (64-byte
+// swizzle) from which TMA stores write coalesced 32x32 bf16 boxes.
+constexpr int STG_BYTES = 2048;
+constexpr int EPI_SMEM = EPI_WARPS * 2 * STG_BYTES;
+
+struct TcParams {
+    int kind;                 // GemmKind
+    const int32_t* offsets;   // [E+1] bucket starts
+    int E, N, K, M;           // row GEMMs: out [rows, N], K reduction; wgrad: C_e [M, N]
+    int n_tiles, m_tiles;
+    const __nv_bfloat16* bias;   // [E, N]
+    const __nv_bfloat16* aux;    // [rows, N] (A of the forward, for dH)
+    __nv_bfloat16* out0;
+    __nv_bfloat16* out1;
+    float* colsum;               // dH: per-(tile, lane quarter) column sums of dA, or null
+    int* err;
+};
+
+// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M = 128, N = BN.
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                      // D format fp32
+         | (1u << 7)                      // A format bf16
+         | (1u << 10)                     // B format bf16
+         | ((a_mn_major ? 1u : 0u) << 15) // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16) // B major-ness
+         | ((uint32_t)(BN >> 3) << 17)    // N >> 3
+         | ((uint32_t)(BM >> 4) << 24);   // M >> 4
+}
+
+// ------------------------------------------------------------------------- tile decode
+struct Tile {
+    int e, m0, n0, row0, kblocks;
+};
+
+__device__ __forceinline__ int bucket_of(const int* s_off, int E, int row) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <bool WGRAD>
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* s_off, int tile) {
+    Tile t;
+    const int nt = tile % p.n_tiles;
+    const int rest = tile / p.n_tiles;
+    t.n0 = nt * BN;
+    if (WGRAD) {
+        t.m0 = (rest % p.m_tiles) * BM;
+        t.e = rest / p.m_tiles;
+        t.row0 = s_off[t.e];
+        t.kblocks = (s_off[t.e + 1] - s_off[t.e]) / BK;
+    } else {
+        t.m0 = rest * BM;
+        t.e = bucket_of(s_off, p.E, t.m0);
+        t.row0 = t.m0;
+        t.kblocks = p.K / BK;
+    }
+    return t;
+}
+
+// ------------------------------------------------------------------------- epilogue
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) store16(dst + 8 * q, v + 8 * q);
+}
+
+// 32 bf16 (64 bytes) as raw vectors: fetched one chunk ahead of their use.
+struct Raw32 {
+    uint4 q[4];
+};
+__device__ __forceinline__ void load_raw32(Raw32& r, const __nv_bfloat16* src) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.q[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+}
+__device__ __forceinline__ void unpack_raw32(const Raw32& r, float* out) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.q[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            out[8 * i + 2 * j] = f.x;
+            out[8 * i + 2 * j + 1] = f.y;
+        }
+    }
+}
+
+// Column sums of a warp's 32 rows x 32 columns (one row per lane, v[i] = column i):
+// a butterfly that halves the columns each lane carries; lane l ends with column l.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool hi = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = hi ? v[i] : v[i + s];
+            const float keep = hi ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+template <int KIND>
+constexpr bool has_bias() { return KIND == kGemmFfn1 || KIND == kGemmFfn2; }
+
+__device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int j) {
+    return base + row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
+}
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return u;
+}
+__device__ __forceinline__ void unpack8(const uint4& u, float* out) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// One epilogue warp's staging buffers and store count (buffer = count & 1).
+struct Stager {
+    uint32_t base;
+    int count;
+    // Returns the next buffer once the TMA store that last read it has finished.
+    __device__ __forceinline__ uint32_t acquire(int lane) {
+        if (lane == 0 && count >= 2) bulk_wait_read1();
+        __syncwarp();
+        return base + (count & 1) * STG_BYTES;
+    }
+    // Writes the lane's row (32 values) into `buf`, then one TMA store of the 32x32 box.
+    __device__ __forceinline__ void store(int lane, uint32_t buf, const float* v, const CUtensorMap* tm, int x, int y) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf, lane, j), pack8(v + 8 * j));
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, buf, x, y);
+            bulk_commit();
+        }
+        ++count;
+    }
+};
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
+    // an expert with no rows: its weight-gradient tile is zero
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+    const int m = t.m0 + row_in_tile;
+    if (m >= p.M) return;
+    for (int c = c_lo; c < c_lo + BN / 2; c += 32)
+        if (t.n0 + c < p.N) store_row32(p.out0 + ((size_t)t.e * p.M + m) * p.N + t.n0 + c, z);
+}
+
+
+}  // namespace
+}  // namespace moe
