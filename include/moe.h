@@ -35,9 +35,10 @@
  *   type selected by cfg->dtype: fp32 (MOE_F32) or bf16 (MOE_BF16) for x, weights,
  *   activations and their gradients. Routing weights, logits and bias gradients are fp32.
  * - Permuted rows live in expert buckets: bucket e holds rows [offsets[e], offsets[e+1]),
- *   offsets[e] is a multiple of MOE_ROW_ALIGN, the first kept[e] rows are expert e's tokens
- *   in ascending token order and the rest of the bucket is padding (row_token = -1, zero
- *   rows in Xp). Buffers of permuted rows have cfg->rows_capacity rows.
+ *   offsets[e] is a multiple of cfg->row_align (128 or 256, chosen by moe_config_init), the
+ *   first kept[e] rows are expert e's tokens in ascending token order and the rest of the
+ *   bucket is padding (row_token = -1, zero rows in Xp). Buffers of permuted rows have
+ *   cfg->rows_capacity rows.
  * - Calls are asynchronous on `stream` and never synchronise the host (except
  *   moe_get_error). Nothing that depends on data (counts, offsets) is read back.
  * - Host-side validation failures return MOE_ERR_INVALID_ARG (bad value, null pointer) or
@@ -75,7 +76,7 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
-#define MOE_ROW_ALIGN 128   /* rows per expert bucket are padded to a multiple of this */
+#define MOE_ROW_ALIGN 128   /* minimum bucket alignment (rows); cfg->row_align is 128 or 256 */
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_K 8
 
@@ -94,6 +95,9 @@ typedef struct {
     /* derived by moe_config_init */
     int32_t capacity;          /* ceil(capacity_factor*T*k/E) in double, or INT32_MAX */
     int32_t rows_capacity;     /* rows of every permuted buffer (Xp, A, H, Yp) */
+    int32_t row_align;         /* bucket alignment: 256 when the average bucket can reach 1024
+                                  rows (min(T*k, E*C)/E >= 1024; the GEMMs then run 256-row
+                                  tiles on CTA pairs), else 128 */
 } moe_config_t;
 
 /* Validates the caller's fields and fills the derived ones. Must be called before any
@@ -117,7 +121,7 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const voi
 /* Capacity, stable counting sort into expert buckets and the gather of x.
  *   idx [T,k] int32, x [T,d] act
  *   -> kept [E] int32 (= min(counts, capacity)), offsets [E+1] int32 (bucket starts,
- *      multiples of MOE_ROW_ALIGN, offsets[E] = rows in use), row_token [rows_capacity]
+ *      multiples of cfg->row_align, offsets[E] = rows in use), row_token [rows_capacity]
  *      int32 (token of each row; -1 on padding; rows >= offsets[E] unspecified),
  *      slot_row [T,k] int32 (row of assignment (t,j), -1 if dropped), n_dropped [1] int32,
  *      Xp [rows_capacity, d] act (rows >= offsets[E] unspecified).

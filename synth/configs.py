@@ -96,6 +96,9 @@ SMALL_CASES = {
     "small-fp32-bwd": LayerConfig(
         name="small-fp32-bwd", T=300, d=96, E=8, k=2, d_ff=160, capacity_factor=1.0,
         dtype="f32"),
+    # average bucket >= 1024 rows: 256-row buckets and GEMM tiles on CTA pairs
+    "small-pair-tiles": LayerConfig(
+        name="small-pair-tiles", T=2500, d=256, E=4, k=2, d_ff=384, capacity_factor=1.0),
     "small-max-e256-k8": LayerConfig(
         name="small-max-e256-k8", T=513, d=128, E=256, k=8, d_ff=128, capacity_factor=None,
         temperature=0.5),

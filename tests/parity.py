@@ -52,9 +52,11 @@ def oracle_capacity(cfg):
     return O.capacity(cfg.capacity_factor, cfg.T, cfg.k, cfg.E)
 
 
-def oracle_run(cfg, npin, dy=None):
+def oracle_run(cfg, npin, dy=None, align=128):
+    """Oracle forward (+ backward) with buckets padded to `align` rows (the library's
+    cfg.row_align, so that the bucket layouts compare bit for bit)."""
     C = oracle_capacity(cfg)
-    fwd = O.forward(npin, cfg.k, cfg.temperature, C, align=128)
+    fwd = O.forward(npin, cfg.k, cfg.temperature, C, align=align)
     bwd = O.backward(npin, fwd, dy) if dy is not None else None
     return fwd, bwd
 

@@ -55,14 +55,17 @@ def test_capacity_matches_oracle(moe_lib, cf, T, k, E):
 
 def test_rows_capacity_bounds_every_bucket_layout(moe_lib):
     for T, k, E, cf in [(1000, 2, 8, 1.0), (1000, 2, 8, 0.0), (5, 1, 256, 0.0), (0, 2, 8, 1.0),
-                        (300, 8, 256, 0.0), (600, 2, 8, 0.25)]:
+                        (300, 8, 256, 0.0), (600, 2, 8, 0.25), (8192, 2, 16, 1.0), (2500, 2, 4, 1.0),
+                        (16384, 8, 128, 0.0)]:
         c = _cfg(moe_lib, T=T, k=k, E=E, capacity_factor=cf)
         assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
         C = c.capacity
         n_max = min(T * k, E * C)
-        # worst case: every bucket wastes 127 rows of padding
-        worst = n_max + 127 * min(E, n_max)
-        assert c.rows_capacity >= worst and c.rows_capacity % 128 == 0
+        # 256-row buckets only when an average bucket can reach 1024 rows
+        assert c.row_align == (256 if n_max >= 1024 * E else 128)
+        # worst case: every bucket wastes row_align - 1 rows of padding
+        worst = n_max + (c.row_align - 1) * min(E, n_max)
+        assert c.rows_capacity >= worst and c.rows_capacity % c.row_align == 0
         if cf <= 0:
             assert C == 2 ** 31 - 1
 

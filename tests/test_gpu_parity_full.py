@@ -63,7 +63,7 @@ def test_full_size(name, moe_lib, cuda_device):
     # ---------------- oracle routing and bucket layout (whole batch)
     r = O.route(x, Wg, bg, cfg.k, cfg.temperature)
     C = O.capacity(cfg.capacity_factor, cfg.T, cfg.k, cfg.E)
-    dsp = O.dispatch(r["idx"], cfg.E, C, align=moe.MOE_ROW_ALIGN)
+    dsp = O.dispatch(r["idx"], cfg.E, C, align=moe.config_from(cfg).row_align)
     ok = P.nontie_tokens(r)
 
     # ---------------- GPU, same entry points and launch configuration as the benchmark

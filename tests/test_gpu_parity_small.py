@@ -28,7 +28,9 @@ def _prepare(name, cases):
     cfg = synth.get(name)
     inp = synth.make_inputs(cfg)
     npin = P.np_inputs(inp)
-    fwd, bwd = P.oracle_run(cfg, npin, npin["dy"] if cfg.backward else None)
+    import token_routing_gb300 as moe
+    align = moe.config_from(cfg).row_align
+    fwd, bwd = P.oracle_run(cfg, npin, npin["dy"] if cfg.backward else None, align=align)
     cases[name] = (cfg, inp, npin, fwd, bwd)
     return cases[name]
 

@@ -31,6 +31,7 @@ class MoeConfig(ctypes.Structure):
         ("temperature", ctypes.c_float), ("aux_loss_weight", ctypes.c_float),
         ("has_gate_bias", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("capacity", ctypes.c_int32), ("rows_capacity", ctypes.c_int32),
+        ("row_align", ctypes.c_int32),
     ]
 
     def __repr__(self):

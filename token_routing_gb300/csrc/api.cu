@@ -32,12 +32,22 @@ int64_t derived_capacity(const moe_config_t& c) {
     return cap > (double)INT32_MAX ? INT32_MAX : (int64_t)cap;
 }
 
+int64_t derived_nmax(const moe_config_t& c, int64_t cap) {
+    return std::min((int64_t)c.T * c.k, (int64_t)c.E * cap);
+}
+
+// 256-row buckets let the row GEMMs run 256-row tiles on CTA pairs; they pay up to 255 padding
+// rows per expert, so they are used only when an average bucket can reach 1024 rows.
+int32_t derived_align(const moe_config_t& c, int64_t cap) {
+    return derived_nmax(c, cap) >= 1024LL * c.E ? 256 : MOE_ROW_ALIGN;
+}
+
 int64_t derived_rows(const moe_config_t& c, int64_t cap) {
-    const int64_t assignments = (int64_t)c.T * c.k;
-    const int64_t n_max = std::min(assignments, (int64_t)c.E * cap);
+    const int64_t n_max = derived_nmax(c, cap);
+    const int64_t align = derived_align(c, cap);
     const int64_t buckets = std::min<int64_t>(c.E, n_max);
-    const int64_t rows = n_max + (int64_t)(MOE_ROW_ALIGN - 1) * buckets;
-    return (rows + MOE_ROW_ALIGN - 1) / MOE_ROW_ALIGN * MOE_ROW_ALIGN;
+    const int64_t rows = n_max + (align - 1) * buckets;
+    return (rows + align - 1) / align * align;
 }
 
 moe_status_t check_fields(const moe_config_t* c) {
@@ -61,7 +71,8 @@ moe_status_t check_config(const moe_config_t* c) {
     moe_status_t st = check_fields(c);
     if (st != MOE_OK) return st;
     const int64_t cap = derived_capacity(*c);
-    if (c->capacity != cap || c->rows_capacity != derived_rows(*c, cap)) return MOE_ERR_INVALID_ARG;
+    if (c->capacity != cap || c->rows_capacity != derived_rows(*c, cap) || c->row_align != derived_align(*c, cap))
+        return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -106,7 +117,8 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
 bool use_tc(const moe_config_t& c) { return c.dtype == MOE_BF16 && tc_gemm_supported(c); }
 
 cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
-    return use_tc(c) ? launch_row_gemm_tc(c, a, s) : launch_row_gemm_simt(c, a, s);
+    if (!use_tc(c)) return launch_row_gemm_simt(c, a, s);
+    return c.row_align == 256 ? launch_row_gemm_tc_pair(c, a, s) : launch_row_gemm_tc(c, a, s);
 }
 cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
     return use_tc(c) ? launch_wgrad_tc_pair(c, a, s) : launch_wgrad_simt(c, a, s);
@@ -148,6 +160,7 @@ moe_status_t moe_config_init(moe_config_t* cfg) {
     const int64_t cap = derived_capacity(*cfg);
     cfg->capacity = (int32_t)cap;
     cfg->rows_capacity = (int32_t)derived_rows(*cfg, cap);
+    cfg->row_align = derived_align(*cfg, cap);
     return MOE_OK;
 }
 

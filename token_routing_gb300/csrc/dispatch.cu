@@ -8,8 +8,8 @@
 //
 // The sort is deterministic: the rank of assignment (t, j) -> e is the number of earlier
 // tokens that picked e, computed as (per-block histogram -> column scan over blocks) +
-// (ordered rank inside the block). Buckets are padded to MOE_ROW_ALIGN rows so that every
-// 128-row GEMM tile belongs to exactly one expert.
+// (ordered rank inside the block). Buckets are padded to the configured alignment (128 or
+// 256 rows) so that every GEMM row tile belongs to exactly one expert.
 #include "internal.cuh"
 
 namespace moe {
@@ -41,10 +41,10 @@ hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __res
 }
 
 // One block, thread e: column scan of the block histograms, counts, kept = min(counts, C),
-// bucket offsets (exclusive scan of kept rounded up to MOE_ROW_ALIGN), assignment offsets
+// bucket offsets (exclusive scan of kept rounded up to the bucket alignment), assignment offsets
 // (exclusive scan of counts), n_dropped.
 __global__ void __launch_bounds__(MOE_MAX_EXPERTS)
-scan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int T, int k, int C,
+scan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int T, int k, int C, int align,
             int32_t* __restrict__ blk_base, int32_t* __restrict__ counts_out,
             int32_t* __restrict__ assign_off, int32_t* __restrict__ kept_out,
             int32_t* __restrict__ offsets, int32_t* __restrict__ n_dropped) {
@@ -63,7 +63,7 @@ scan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int T, int k,
     const int kept = (e < E) ? min(run, C) : 0;
     s_cnt[e] = (e < E) ? run : 0;
     s_kept[e] = kept;
-    s_pad[e] = (kept + MOE_ROW_ALIGN - 1) / MOE_ROW_ALIGN * MOE_ROW_ALIGN;
+    s_pad[e] = (kept + align - 1) / align * align;
     __syncthreads();
     if (e == 0) {
         // E <= 256 sequential prefix sums: exact and deterministic
@@ -192,7 +192,7 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
         hist_kernel<<<nblk, kSortTok, 0, st>>>(idx, c.T, c.k, c.E, s.blk_hist, err);
         count_launch();
     }
-    scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(s.blk_hist, nblk, c.E, c.T, c.k, c.capacity,
+    scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(s.blk_hist, nblk, c.E, c.T, c.k, c.capacity, c.row_align,
                                                s.blk_base, s.counts, s.assign_off, kept, offsets,
                                                n_dropped);
     count_launch();

@@ -346,6 +346,50 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorM
 
 }  // namespace
 
+cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
+    if (a.rows_capacity == 0) return cudaSuccess;
+    if (c.row_align % P_BM != 0) return cudaErrorInvalidValue;  // 256-row tiles need 256-row buckets
+    TcParams p{};
+    p.kind = a.kind;
+    p.offsets = a.offsets;
+    p.E = a.E; p.N = a.N; p.K = a.K; p.M = 0;
+    p.n_tiles = ceil_div(a.N, BN);
+    p.m_tiles = a.rows_capacity / P_BM;
+    p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+    p.aux = static_cast<const __nv_bfloat16*>(a.aux);
+    p.out0 = static_cast<__nv_bfloat16*>(a.out0);
+    p.out1 = static_cast<__nv_bfloat16*>(a.out1);
+    p.colsum = a.colsum;
+    p.err = device_error_word();
+    CUtensorMap ta, tb, to0, to1;
+    // A: activations [rows, K], each CTA its own 128 rows
+    if (!make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.rows_capacity, P_HALF)) return cudaErrorInvalidValue;
+    if (a.sBn != 1) {
+        // B(n, k) = W[e*N + n][k], K-major: each CTA its own 128 of the tile's 256 columns
+        if (!make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.E * a.N, P_HALF)) return cudaErrorInvalidValue;
+    } else {
+        // B(n, k) = W[e*K + k][n], N-major: boxes of 64 n x 64 k
+        if (!make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.E * a.K, BK)) return cudaErrorInvalidValue;
+    }
+    if (!make_map_ex(&to0, a.out0, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    if (a.kind == kGemmFfn1) {
+        if (!make_map_ex(&to1, a.out1, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else {
+        to1 = to0;
+    }
+    const long long tiles = (long long)p.m_tiles * p.n_tiles;
+    const int clusters = (int)std::max(1LL, std::min<long long>(tiles, num_sms() / 2));
+    switch (a.kind) {
+        case kGemmFfn1: return launch_pair<kGemmFfn1, false, false>(p, ta, tb, to0, to1, clusters, s);
+        case kGemmFfn2: return launch_pair<kGemmFfn2, false, false>(p, ta, tb, to0, to1, clusters, s);
+        case kGemmDH: return launch_pair<kGemmDH, false, true>(p, ta, tb, to0, to1, clusters, s);
+        case kGemmDX: return launch_pair<kGemmDX, false, true>(p, ta, tb, to0, to1, clusters, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
     TcParams p{};
     p.kind = kGemmWgrad;

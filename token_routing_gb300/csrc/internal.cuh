@@ -6,7 +6,7 @@
 namespace moe {
 
 // Epilogues of the grouped GEMMs over expert buckets (rows of one 128-row tile always belong
-// to a single expert because buckets are padded to MOE_ROW_ALIGN rows).
+// to a single expert because buckets are padded to cfg.row_align rows, a multiple of 128).
 enum GemmKind : int {
     kGemmFfn1 = 0,   // A = Xp W1_e^T + b1_e, H = GELU(A)          (store A and H)
     kGemmFfn2 = 1,   // Yp = H W2_e^T + b2_e
@@ -76,6 +76,8 @@ cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cuda
 cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
 // gemm_tc_pair.cu: weight gradients on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles)
 cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
+// row GEMMs on CTA pairs: 256-row tiles, needs cfg.row_align == 256
+cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,
