@@ -155,11 +155,12 @@ MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t
 
 /* Per-expert FFN over the buckets: A = Xp W1_e^T + b1_e, H = GELU(A), Yp = H W2_e^T + b2_e.
  *   Xp [rows_capacity,d], offsets [E+1] (from moe_dispatch), W1 [E,d_ff,d], b1 [E,d_ff],
- *   W2 [E,d,d_ff], b2 [E,d] -> A, H [rows_capacity,d_ff], Yp [rows_capacity,d] (all act;
- *   rows >= offsets[E] untouched). A is kept for the backward. fp32 accumulation. */
+ *   W2 [E,d,d_ff], b2 [E,d] -> Gp, H [rows_capacity,d_ff], Yp [rows_capacity,d] (all act;
+ *   rows >= offsets[E] untouched). Gp = GELU'(A) = Phi(A) + A phi(A) is what the backward
+ *   needs of the pre-activation, saved in place of A itself. fp32 accumulation. */
 MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* Xp, const int32_t* offsets,
                             const void* W1, const void* b1, const void* W2, const void* b2,
-                            void* A, void* H, void* Yp, void* ws, moe_stream_t stream);
+                            void* Gp, void* H, void* Yp, void* ws, moe_stream_t stream);
 
 /* Weighted combine back to token order: y[t] = sum_{j: slot_row[t,j] >= 0} w[t,j] Yp[slot_row[t,j]],
  * accumulated in fp32; a token whose slots were all dropped gets 0.  y [T,d] act. */
@@ -167,7 +168,7 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const 
                          const float* w, void* y, moe_stream_t stream);
 
 /* Backward of the layer for the gradient seed dy [T,d] act, from the forward's saved tensors.
- *   inputs : dy, x, Wg, idx, w, offsets, row_token, slot_row, Xp, A, H, Yp, W1, W2 (as above),
+ *   inputs : dy, x, Wg, idx, w, offsets, row_token, slot_row, Xp, Gp, H, Yp, W1, W2 (as above),
  *            balance_loss [1] (nullable; enters the reported loss only)
  *   outputs: dx [T,d] act, dWg [E,d] fp32, dW1 [E,d_ff,d] act, db1 [E,d_ff] fp32,
  *            dW2 [E,d,d_ff] act, db2 [E,d] fp32, dbg [E] fp32 (nullable: gate-bias
@@ -178,7 +179,7 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const 
 MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x, const void* Wg,
                           const int32_t* idx, const float* w, const int32_t* offsets,
                           const int32_t* row_token, const int32_t* slot_row, const void* Xp,
-                          const void* A, const void* H, const void* Yp, const void* W1,
+                          const void* Gp, const void* H, const void* Yp, const void* W1,
                           const void* W2, const float* balance_loss,
                           void* dx, float* dWg, void* dW1, float* db1, void* dW2, float* db2,
                           float* dbg, float* dw, float* loss, void* ws, moe_stream_t stream);

@@ -101,7 +101,7 @@ def test_full_size(name, moe_lib, cuda_device):
     toks = np.unique(np.concatenate([rng.choice(cfg.T, 48, replace=False), [0, cfg.T - 1],
                                      np.nonzero((dsp["slot_row"] < 0).any(1))[0][:8]]))
     y_o, y_g, dx_o, dx_g, dw_o, dw_g = [], [], [], [], [], []
-    rows_o, rows_g = {"A": [], "H": [], "Yp": []}, {"A": [], "H": [], "Yp": []}
+    rows_o, rows_g = {"Gp": [], "H": [], "Yp": []}, {"Gp": [], "H": [], "Yp": []}
     fr = expert_rows([(tk, j) for tk in toks for j in range(cfg.k) if dsp["slot_row"][tk, j] >= 0])
     for tk in toks:
         yk = np.zeros(cfg.d)
@@ -112,7 +112,7 @@ def test_full_size(name, moe_lib, cuda_device):
             if row < 0:
                 continue
             e, A, H, Yr = fr[(tk, j)]
-            for key, v in (("A", A), ("H", H), ("Yp", Yr)):
+            for key, v in (("Gp", O.gelu_prime(A)), ("H", H), ("Yp", Yr)):
                 rows_o[key].append(v)
                 rows_g[key].append(P.f64(b[key][row]))
             W1e, W2e = Wf(e)
@@ -126,7 +126,7 @@ def test_full_size(name, moe_lib, cuda_device):
         y_o.append(yk); y_g.append(P.f64(b["y"][tk]))
         dx_o.append(dxk); dx_g.append(P.f64(b["dx"][tk]))
         dw_o.append(dws); dw_g.append(P.f64(b["dw"][tk]))
-    for key in ("A", "H", "Yp"):
+    for key in ("Gp", "H", "Yp"):
         P.assert_close(key, np.array(rows_g[key]), np.array(rows_o[key]), t)
     P.assert_close("y", np.array(y_g), np.array(y_o), t)
     P.assert_close("dw", np.array(dw_g), np.array(dw_o), t)

@@ -89,8 +89,9 @@ def test_expert_ffn(name, cases, moe_lib, cuda_device):
     moe.expert_ffn(c, b["Xp"], offs, dev["W1"], dev["b1"], dev["W2"], dev["b2"], b)
     moe.get_error()
     kept_rows = fwd["row_token"] >= 0
-    for key in ("A", "H", "Yp"):
-        P.assert_close(key, P.f64(b[key][:n])[kept_rows], fwd[key][kept_rows], P.tol(cfg))
+    ref = {"Gp": P.O.gelu_prime(fwd["A"]), "H": fwd["H"], "Yp": fwd["Yp"]}
+    for key in ("Gp", "H", "Yp"):
+        P.assert_close(key, P.f64(b[key][:n])[kept_rows], ref[key][kept_rows], P.tol(cfg))
 
 
 @pytest.mark.parametrize("name", CASES)
@@ -121,8 +122,9 @@ def test_backward(name, cases, moe_lib, cuda_device):
     b["offsets"].copy_(P.dev_i32(fwd["offsets"]))
     b["row_token"][:n] = P.dev_i32(fwd["row_token"])
     b["slot_row"].copy_(P.dev_i32(fwd["slot_row"]))
-    for key in ("Xp", "A", "H", "Yp"):
+    for key in ("Xp", "H", "Yp"):
         b[key][:n] = P.dev_act(cfg, fwd[key])
+    b["Gp"][:n] = P.dev_act(cfg, P.O.gelu_prime(fwd["A"]))
     b["balance_loss"].fill_(fwd["balance_loss"])
     moe.backward(c, dev["dy"], dev["x"], dev["Wg"], dev["W1"], dev["W2"], b)
     moe.get_error()

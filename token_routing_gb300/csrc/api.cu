@@ -199,18 +199,18 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const voi
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* Xp, const int32_t* offsets,
-                            const void* W1, const void* b1, const void* W2, const void* b2, void* A,
+                            const void* W1, const void* b1, const void* W2, const void* b2, void* Gp,
                             void* H, void* Yp, void* ws, moe_stream_t stream) {
     (void)ws;
     moe_status_t st = check_config(cfg);
     if (st != MOE_OK) return st;
     if (!offsets || !W1 || !b1 || !W2 || !b2) return MOE_ERR_INVALID_ARG;
-    if (cfg->rows_capacity > 0 && (!Xp || !A || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!Xp || !Gp || !H || !Yp)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity == 0) return MOE_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const moe_config_t& c = *cfg;
     RowGemmArgs g1{};
-    g1.kind = kGemmFfn1; g1.A = Xp; g1.B = W1; g1.bias = b1; g1.out0 = A; g1.out1 = H;
+    g1.kind = kGemmFfn1; g1.A = Xp; g1.B = W1; g1.bias = b1; g1.out0 = Gp; g1.out1 = H;
     g1.offsets = offsets; g1.E = c.E; g1.N = c.d_ff; g1.K = c.d; g1.rows_capacity = c.rows_capacity;
     g1.sBe = (long long)c.d_ff * c.d; g1.sBn = c.d; g1.sBk = 1;
     MOE_TRY(row_gemm(c, g1, s));
@@ -233,7 +233,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const int32_t*
 moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x, const void* Wg,
                           const int32_t* idx, const float* w, const int32_t* offsets,
                           const int32_t* row_token, const int32_t* slot_row, const void* Xp,
-                          const void* A, const void* H, const void* Yp, const void* W1,
+                          const void* Gp, const void* H, const void* Yp, const void* W1,
                           const void* W2, const float* balance_loss, void* dx, float* dWg, void* dW1,
                           float* db1, void* dW2, float* db2, float* dbg, float* dw, float* loss,
                           void* ws, moe_stream_t stream) {
@@ -242,7 +242,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     if (!Wg || !offsets || !W1 || !W2 || !dWg || !dW1 || !db1 || !dW2 || !db2 || !ws)
         return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!dy || !x || !idx || !w || !slot_row || !dx)) return MOE_ERR_INVALID_ARG;
-    if (cfg->rows_capacity > 0 && (!row_token || !Xp || !A || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    if (cfg->rows_capacity > 0 && (!row_token || !Xp || !Gp || !H || !Yp)) return MOE_ERR_INVALID_ARG;
     const moe_config_t& c = *cfg;
     cudaStream_t s = (cudaStream_t)stream;
     BackwardScratch b;
@@ -253,7 +253,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossblk, s));
     // experts backward
     RowGemmArgs gh{};
-    gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = A; gh.out0 = b.dA;
+    gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = Gp; gh.out0 = b.dA;
     gh.colsum = use_tc(c) ? b.colsum_f : nullptr;  // the tensor-core epilogue sums dA columns
     gh.offsets = offsets; gh.E = c.E; gh.N = c.d_ff; gh.K = c.d; gh.rows_capacity = c.rows_capacity;
     gh.sBe = (long long)c.d * c.d_ff; gh.sBn = 1; gh.sBk = c.d_ff;

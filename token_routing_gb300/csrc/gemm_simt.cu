@@ -81,16 +81,17 @@ row_gemm_simt_kernel(RowGemmArgs a) {
             const size_t o = (size_t)r * a.N + n;
             float v = acc[i][j];
             switch (a.kind) {
-                case kGemmFfn1:
+                case kGemmFfn1: {
                     v += ld_f(bias + (size_t)e * a.N + n);
-                    st_f(out0 + o, v);
+                    st_f(out0 + o, gelu_grad_f(v));  // saved for the backward
                     st_f(out1 + o, gelu_f(v));
                     break;
+                }
                 case kGemmFfn2:
                     st_f(out0 + o, v + ld_f(bias + (size_t)e * a.N + n));
                     break;
                 case kGemmDH:
-                    st_f(out0 + o, v * gelu_grad_f(ld_f(aux + o)));
+                    st_f(out0 + o, v * ld_f(aux + o));
                     break;
                 default:
                     st_f(out0 + o, v);

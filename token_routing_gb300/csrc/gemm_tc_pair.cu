@@ -281,13 +281,18 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     unpack_raw32(cur, bv);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] += bv[i];
-                    uint32_t b = st.acquire(lane);
-                    st.store(lane, b, v, &tmO0, n, y);
                     if (KIND == kGemmFfn1) {
+                        // H = GELU(A) for the second GEMM, GELU'(A) saved for the backward
+                        float gp[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+                        for (int i = 0; i < 32; ++i) gelu_and_grad_f(v[i], v[i], gp[i]);
+                        uint32_t b = st.acquire(lane);
+                        st.store(lane, b, gp, &tmO0, n, y);
                         b = st.acquire(lane);
                         st.store(lane, b, v, &tmO1, n, y);
+                    } else {
+                        const uint32_t b = st.acquire(lane);
+                        st.store(lane, b, v, &tmO0, n, y);
                     }
                 } else if (KIND == kGemmDH) {
                     const uint32_t b = st.acquire(lane);
@@ -299,7 +304,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     for (int j = 0; j < 4; ++j) unpack8(lds128(sw64_addr(b, lane, j)), a + 8 * j);
                     __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
+                    for (int i = 0; i < 32; ++i) v[i] *= a[i];  // a = GELU'(A) saved by the forward
                     st.store(lane, b, v, &tmO0, n, y);
                     if (p.colsum) {
                         const float sum = warp_colsum32(v, lane);

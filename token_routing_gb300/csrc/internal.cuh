@@ -8,9 +8,9 @@ namespace moe {
 // Epilogues of the grouped GEMMs over expert buckets (rows of one 128-row tile always belong
 // to a single expert because buckets are padded to cfg.row_align rows, a multiple of 128).
 enum GemmKind : int {
-    kGemmFfn1 = 0,   // A = Xp W1_e^T + b1_e, H = GELU(A)          (store A and H)
+    kGemmFfn1 = 0,   // A = Xp W1_e^T + b1_e; store H = GELU(A) and Gp = GELU'(A)
     kGemmFfn2 = 1,   // Yp = H W2_e^T + b2_e
-    kGemmDH = 2,     // dA = (dYp W2_e) * GELU'(A)
+    kGemmDH = 2,     // dA = (dYp W2_e) * Gp
     kGemmDX = 3,     // dXp = dA W1_e
     kGemmWgrad = 4,  // dW_e = P_e^T Q_e over the rows of bucket e (dW2: P=dYp,Q=H; dW1: P=dA,Q=Xp)
 };
@@ -20,9 +20,9 @@ struct RowGemmArgs {
     const void* A;          // [rows, K] row-major activations
     const void* B;          // expert weights (layout per kind)
     const void* bias;       // [E, N] (Ffn1, Ffn2)
-    const void* aux;        // [rows, N] A of the forward (DH)
+    const void* aux;        // [rows, N] Gp = GELU'(A) of the forward (DH)
     void* out0;             // [rows, N]
-    void* out1;             // [rows, N] (H of Ffn1)
+    void* out1;             // [rows, N] (H of Ffn1; out0 then holds Gp)
     const int32_t* offsets; // [E+1] bucket starts
     float* colsum;          // DH on tensor cores: column-sum partials of dA [tiles*4, N], or null
     int E, N, K;

@@ -56,7 +56,7 @@ def alloc_buffers(cfg, device="cuda", backward=True):
              balance_loss=torch.empty(1, **f32), kept=torch.empty(E, **i32),
              offsets=torch.empty(E + 1, **i32), row_token=torch.empty(R, **i32),
              slot_row=torch.empty(T, k, **i32), n_dropped=torch.empty(1, **i32),
-             Xp=torch.empty(R, d, **act), A=torch.empty(R, f, **act), H=torch.empty(R, f, **act),
+             Xp=torch.empty(R, d, **act), Gp=torch.empty(R, f, **act), H=torch.empty(R, f, **act),
              Yp=torch.empty(R, d, **act), y=torch.empty(T, d, **act),
              ws=torch.empty(max(workspace_bytes(cfg), 256), dtype=torch.uint8, device=device))
     if backward:
@@ -81,7 +81,7 @@ def dispatch(cfg, idx, x, b, stream=None):
 
 def expert_ffn(cfg, Xp, offsets, W1, b1, W2, b2, b, stream=None):
     L.check("moe_expert_ffn", L.load().moe_expert_ffn(
-        ctypes.byref(cfg), _p(Xp), _p(offsets), _p(W1), _p(b1), _p(W2), _p(b2), _p(b["A"]),
+        ctypes.byref(cfg), _p(Xp), _p(offsets), _p(W1), _p(b1), _p(W2), _p(b2), _p(b["Gp"]),
         _p(b["H"]), _p(b["Yp"]), _p(b["ws"]), _s(stream)))
 
 
@@ -92,10 +92,10 @@ def combine(cfg, Yp, slot_row, w, y, stream=None):
 
 def backward(cfg, dy, x, Wg, W1, W2, b, stream=None, want_dbg=True, want_dw=True, want_loss=True):
     """Backward from the forward's saved tensors in `b` (idx, w, offsets, row_token, slot_row,
-    Xp, A, H, Yp, balance_loss); writes dx, dWg, dW1, db1, dW2, db2 (+ dbg, dw, loss)."""
+    Xp, Gp, H, Yp, balance_loss); writes dx, dWg, dW1, db1, dW2, db2 (+ dbg, dw, loss)."""
     L.check("moe_backward", L.load().moe_backward(
         ctypes.byref(cfg), _p(dy), _p(x), _p(Wg), _p(b["idx"]), _p(b["w"]), _p(b["offsets"]),
-        _p(b["row_token"]), _p(b["slot_row"]), _p(b["Xp"]), _p(b["A"]), _p(b["H"]), _p(b["Yp"]),
+        _p(b["row_token"]), _p(b["slot_row"]), _p(b["Xp"]), _p(b["Gp"]), _p(b["H"]), _p(b["Yp"]),
         _p(W1), _p(W2), _p(b["balance_loss"]), _p(b["dx"]), _p(b["dWg"]), _p(b["dW1"]),
         _p(b["db1"]), _p(b["dW2"]), _p(b["db2"]), _p(b["dbg"]) if want_dbg else None,
         _p(b["dw"]) if want_dw else None, _p(b["loss"]) if want_loss else None, _p(b["ws"]),
