@@ -172,10 +172,13 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const 
  *            balance_loss [1] (nullable; enters the reported loss only)
  *   outputs: dx [T,d] act, dWg [E,d] fp32, dW1 [E,d_ff,d] act, db1 [E,d_ff] fp32,
  *            dW2 [E,d,d_ff] act, db2 [E,d] fp32, dbg [E] fp32 (nullable: gate-bias
- *            gradient), dw [T,k] fp32 (nullable: gradient of the routing weights),
+ *            gradient, written only when cfg->has_gate_bias), dw [T,k] fp32 (nullable:
+ *            gradient of the routing weights),
  *            loss [1] fp32 (nullable: sum(y*dy) + aux_loss_weight*balance_loss).
  * Dropped assignments give dw = 0 but still enter their token's softmax Jacobian. Experts
- * with no kept rows get zero weight and bias gradients. Scratch comes from ws. */
+ * with no kept rows get zero weight and bias gradients. Scratch comes from ws. Part of the
+ * work runs on a side stream of the library that forks from and joins back into `stream`
+ * (event waits, also valid while `stream` is being captured into a CUDA graph). */
 MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x, const void* Wg,
                           const int32_t* idx, const float* w, const int32_t* offsets,
                           const int32_t* row_token, const int32_t* slot_row, const void* Xp,

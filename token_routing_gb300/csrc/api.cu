@@ -114,6 +114,36 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     return align_up(ws.used, 256);
 }
 
+// One non-blocking side stream per device for the backward's parallel branch (created on
+// first use, kept until exit).
+cudaStream_t g_side[kMaxDevices] = {};
+cudaStream_t side_stream() {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_side[dev]) {
+        cudaStream_t st = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        g_side[dev] = st;
+    }
+    return g_side[dev];
+}
+
+// Fork/join events of one call; destroyed when the call returns (pending waits still hold).
+struct EventPair {
+    cudaEvent_t a = nullptr, b = nullptr, c = nullptr;
+    bool ok = false;
+    EventPair() {
+        ok = cudaEventCreateWithFlags(&a, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&b, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&c, cudaEventDisableTiming) == cudaSuccess;
+    }
+    ~EventPair() {
+        if (a) cudaEventDestroy(a);
+        if (b) cudaEventDestroy(b);
+        if (c) cudaEventDestroy(c);
+    }
+};
+
 bool use_tc(const moe_config_t& c) { return c.dtype == MOE_BF16 && tc_gemm_supported(c); }
 
 cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
@@ -249,33 +279,49 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     carve_backward(c, ws, &b);
     float* dwp = dw ? dw : b.dw;
 
-    // combine backward: dYp, dw, per-row loss terms (padding rows of dYp zeroed)
+    // The backward is a small DAG. Main stream: combine backward -> dH -> dX -> router
+    // backward -> dWg -> loss. Side stream: dW2 and db2 (need dYp), then dW1 and db1 (need
+    // dA). The side branch forks and joins through events, which also works under stream
+    // capture; the branches write disjoint outputs, so results do not depend on the overlap.
+    cudaStream_t side = side_stream();
+    if (!side) return MOE_ERR_CUDA;
+    EventPair ev;
+    if (!ev.ok) return MOE_ERR_CUDA;
+
+    // combine backward: dYp, dw, loss partials (padding rows of dYp zeroed)
     MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossblk, s));
-    // experts backward
+    MOE_TRY(cudaEventRecord(ev.a, s));
+    MOE_TRY(cudaStreamWaitEvent(side, ev.a, 0));
+    WgradArgs w2{b.dYp, H, dW2, offsets, c.E, c.d, c.d_ff};
+    MOE_TRY(wgrad(c, w2, side));
+    MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, side));
+    MOE_TRY(launch_bias_reduce(c, b.colsum_d, c.d, offsets, db2, side));
+    // experts backward on the main stream
     RowGemmArgs gh{};
     gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = Gp; gh.out0 = b.dA;
     gh.colsum = use_tc(c) ? b.colsum_f : nullptr;  // the tensor-core epilogue sums dA columns
     gh.offsets = offsets; gh.E = c.E; gh.N = c.d_ff; gh.K = c.d; gh.rows_capacity = c.rows_capacity;
     gh.sBe = (long long)c.d * c.d_ff; gh.sBn = 1; gh.sBk = c.d_ff;
     MOE_TRY(row_gemm(c, gh, s));
+    if (!use_tc(c)) MOE_TRY(launch_colsum(c, b.dA, c.d_ff, offsets, b.colsum_f, s));
+    MOE_TRY(cudaEventRecord(ev.b, s));
+    MOE_TRY(cudaStreamWaitEvent(side, ev.b, 0));
+    WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
+    MOE_TRY(wgrad(c, w1, side));
+    MOE_TRY(launch_bias_reduce(c, b.colsum_f, c.d_ff, offsets, db1, side));
     RowGemmArgs gx{};
     gx.kind = kGemmDX; gx.A = b.dA; gx.B = W1; gx.out0 = b.dXp;
     gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;
     gx.sBe = (long long)c.d_ff * c.d; gx.sBn = 1; gx.sBk = c.d;
     MOE_TRY(row_gemm(c, gx, s));
-    WgradArgs w2{b.dYp, H, dW2, offsets, c.E, c.d, c.d_ff};
-    MOE_TRY(wgrad(c, w2, s));
-    WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
-    MOE_TRY(wgrad(c, w1, s));
-    MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, s));
-    MOE_TRY(launch_bias_reduce(c, b.colsum_d, c.d, offsets, db2, s));
-    if (!use_tc(c)) MOE_TRY(launch_colsum(c, b.dA, c.d_ff, offsets, b.colsum_f, s));
-    MOE_TRY(launch_bias_reduce(c, b.colsum_f, c.d_ff, offsets, db1, s));
     // router backward: assignment sort, softmax Jacobian, dx, dWg, dbg
     MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
     MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
-    MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, dbg, s));
+    MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, c.has_gate_bias ? dbg : nullptr, s));
     if (loss) MOE_TRY(launch_loss(c, b.lossblk, balance_loss, loss, s));
+    // join
+    MOE_TRY(cudaEventRecord(ev.c, side));
+    MOE_TRY(cudaStreamWaitEvent(s, ev.c, 0));
     return MOE_OK;
 }
 

@@ -341,16 +341,17 @@ bias_reduce_kernel(const float* __restrict__ part, int width, const int32_t* __r
 __global__ void __launch_bounds__(256)
 loss_kernel(const float* __restrict__ lossblk, int nblk, const float* __restrict__ balance, float aux,
             float* __restrict__ loss) {
-    __shared__ double red[256];
-    double acc = 0.0;
-    for (int i = threadIdx.x; i < nblk; i += blockDim.x) acc += (double)lossblk[i];
-    red[threadIdx.x] = acc;
+    __shared__ float red[8];
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) acc += lossblk[i];
+    acc = warp_sum(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int i = 0; i < 8; ++i) t += (double)red[i];
+        *loss = (float)(t + (balance ? (double)aux * (double)*balance : 0.0));
     }
-    if (threadIdx.x == 0) *loss = (float)(red[0] + (balance ? (double)aux * (double)*balance : 0.0));
 }
 
 int warp_grid(long long items, int warps_per_block = 8) {
