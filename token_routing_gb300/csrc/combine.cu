@@ -32,20 +32,36 @@ combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
             ws[j] = (j < k) ? w[(size_t)t * k + j] : 0.f;
         }
         if ((d % V) == 0) {
-            for (int c = lane * V; c < d; c += 32 * V) {
-                float acc[V];
-#pragma unroll
-                for (int i = 0; i < V; ++i) acc[i] = 0.f;
+            // two column groups per pass, every row load issued before any arithmetic
+#pragma unroll 1
+            for (int c = lane * V; c < d; c += 64 * V) {
+                const int c2 = c + 32 * V;
+                const bool two = c2 < d;
+                uint4 raw[2][MOE_MAX_K];
 #pragma unroll
                 for (int j = 0; j < MOE_MAX_K; ++j) {
-                    if (rows[j] >= 0) {
-                        float v[V];
-                        load16(Yp + (size_t)rows[j] * d + c, v);
-#pragma unroll
-                        for (int i = 0; i < V; ++i) acc[i] = fmaf(ws[j], v[i], acc[i]);
+                    if (j < k && rows[j] >= 0) {
+                        raw[0][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rows[j] * d + c));
+                        if (two) raw[1][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rows[j] * d + c2));
                     }
                 }
-                store16(y + (size_t)t * d + c, acc);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    float acc[V];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < MOE_MAX_K; ++j) {
+                        if (j < k && rows[j] >= 0) {
+                            float v[V];
+                            unpack16<T>(raw[h][j], v);
+#pragma unroll
+                            for (int i = 0; i < V; ++i) acc[i] = fmaf(ws[j], v[i], acc[i]);
+                        }
+                    }
+                    store16(y + (size_t)t * d + (h ? c2 : c), acc);
+                }
             }
         } else {
             for (int c = lane; c < d; c += 32) {

@@ -56,6 +56,23 @@ __device__ __forceinline__ void load16(const T* p, float* out) {
     }
 }
 
+// The 16 bytes of a load16, already fetched.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& u, float* out) {
+    if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    } else {
+        out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+        out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void store16(T* p, const float* in) {
     uint4 u;

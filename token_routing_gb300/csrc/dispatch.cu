@@ -7,8 +7,8 @@
 // its expert bucket's offset instead of being concatenated).
 //
 // The sort is deterministic: the rank of assignment (t, j) -> e is the number of earlier
-// tokens that picked e, computed as (per-block histogram -> column scan over blocks) +
-// (ordered rank inside the block). Buckets are padded to the configured alignment (128 or
+// tokens that picked e, computed as (per-chunk histogram -> column scan over chunks) +
+// (population count of e's token bitmask inside the chunk). Buckets are padded to the configured alignment (128 or
 // 256 rows) so that every GEMM row tile belongs to exactly one expert.
 #include "internal.cuh"
 
@@ -18,123 +18,211 @@ namespace {
 
 constexpr int kSortTok = 256;   // tokens per block in the histogram / rank kernels
 
-__global__ void __launch_bounds__(kSortTok)
-hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ blk_hist,
-            int* err) {
-    __shared__ int h[MOE_MAX_EXPERTS];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
-    __syncthreads();
-    const int t = blockIdx.x * kSortTok + threadIdx.x;
-    if (t < T) {
-        int mine[MOE_MAX_K];
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[(size_t)t * k + j];
-            bool ok = (e >= 0 && e < E);
-            for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
-            mine[j] = ok ? e : -1;
-            if (ok) atomicAdd(&h[e], 1);
-            else raise_error(err, kErrBounds);
-        }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = h[e];
+// The whole sort in one cooperative launch (all blocks co-resident, grid barriers between
+// phases; each barrier wait is bounded and records kErrTimeout if it runs out):
+//   1. per-chunk expert histograms (chunks of kSortTok tokens, checked for bad/repeated ids)
+//   2. per-expert exclusive scans over the chunks (chunk bases) and the totals (counts)
+//   3. every block derives kept / bucket offsets / assignment offsets from the counts, then
+//      ranks its chunks' assignments with per-expert token bitmasks (population counts) and
+//      writes slot_row, row_token (padding rows -1) and the expert-major assignment list.
+struct SortArgs {
+    const int32_t* idx;
+    int T, k, E, C, align, nchunk;
+    int32_t* blk_hist;
+    int32_t* blk_base;
+    int32_t* counts;
+    int32_t* assign_off;
+    int32_t* assign_tok;
+    int32_t* kept;       // bucket outputs: null in assignment-only mode
+    int32_t* offsets;
+    int32_t* row_token;
+    int32_t* slot_row;
+    int32_t* n_dropped;
+    unsigned* bar;       // zeroed before the launch
+    int* err;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// One block, thread e: column scan of the block histograms, counts, kept = min(counts, C),
-// bucket offsets (exclusive scan of kept rounded up to the bucket alignment), assignment offsets
-// (exclusive scan of counts), n_dropped.
-__global__ void __launch_bounds__(MOE_MAX_EXPERTS)
-scan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int T, int k, int C, int align,
-            int32_t* __restrict__ blk_base, int32_t* __restrict__ counts_out,
-            int32_t* __restrict__ assign_off, int32_t* __restrict__ kept_out,
-            int32_t* __restrict__ offsets, int32_t* __restrict__ n_dropped) {
-    __shared__ int s_pad[MOE_MAX_EXPERTS];
-    __shared__ int s_cnt[MOE_MAX_EXPERTS];
-    __shared__ int s_kept[MOE_MAX_EXPERTS];
-    const int e = threadIdx.x;
-    int run = 0;
-    if (e < E) {
-        for (int b = 0; b < nblk; ++b) {
-            const int v = blk_hist[(size_t)b * E + e];
-            blk_base[(size_t)b * E + e] = run;
-            run += v;
-        }
-    }
-    const int kept = (e < E) ? min(run, C) : 0;
-    s_cnt[e] = (e < E) ? run : 0;
-    s_kept[e] = kept;
-    s_pad[e] = (kept + align - 1) / align * align;
+// Grid barrier: returns false (and records a device error) if the wait ran out.
+__device__ bool grid_barrier(unsigned* bar, unsigned target, int* err) {
+    __shared__ int s_ok;
     __syncthreads();
-    if (e == 0) {
-        // E <= 256 sequential prefix sums: exact and deterministic
-        int off = 0, aoff = 0, total_kept = 0;
-        for (int i = 0; i < E; ++i) {
-            if (offsets) offsets[i] = off;
-            assign_off[i] = aoff;
-            off += s_pad[i];
-            aoff += s_cnt[i];
-            total_kept += s_kept[i];
+    if (threadIdx.x == 0) {
+        s_ok = 1;
+        __threadfence();
+        atomicAdd(bar, 1u);
+        const long long t0 = clock64();
+        while (ld_acquire_u32(bar) < target) {
+            if (clock64() - t0 > kSpinBudgetCycles) {
+                raise_error(err, kErrTimeout);
+                s_ok = 0;
+                break;
+            }
         }
-        if (offsets) offsets[E] = off;
-        assign_off[E] = aoff;
-        if (n_dropped) *n_dropped = T * k - total_kept;
+        __threadfence();
     }
-    if (e < E) {
-        counts_out[e] = run;
-        if (kept_out) kept_out[e] = kept;
-    }
+    __syncthreads();
+    return s_ok != 0;
 }
 
-// Ranks inside a block, without any order-dependent step: every (token, slot) sets its
-// token's bit in a per-expert 256-bit mask, then the rank of token t among the block's
-// tokens that picked e is the population count of e's mask below bit t. Writes the
-// expert-major assignment list and, when the bucket outputs are requested, slot_row and
-// row_token.
+// Exclusive scan of n <= blockDim.x values in shared memory (blockDim.x = 256); returns the total.
+__device__ int block_exclusive_scan(int* buf, int n) {
+    __shared__ int s_tot;
+    const int tid = threadIdx.x;
+    int v = tid < n ? buf[tid] : 0;
+    __syncthreads();
+    for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+        const int other = tid >= off ? buf[tid - off] : 0;
+        __syncthreads();
+        if (tid < n) buf[tid] = (tid >= off ? other : 0) + buf[tid];
+        __syncthreads();
+    }
+    // buf now holds inclusive sums
+    if (tid == n - 1) s_tot = buf[tid];
+    __syncthreads();
+    const int incl = tid < n ? buf[tid] : 0;
+    __syncthreads();
+    if (tid < n) buf[tid] = incl - v;
+    const int tot = n > 0 ? s_tot : 0;
+    __syncthreads();
+    return tot;
+}
+
 __global__ void __launch_bounds__(kSortTok)
-rank_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int C,
-            const int32_t* __restrict__ blk_base, const int32_t* __restrict__ assign_off,
-            const int32_t* __restrict__ offsets, int32_t* __restrict__ assign_tok,
-            int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token) {
+sort_kernel(SortArgs a) {
     constexpr int W = kSortTok / 32;
     __shared__ uint32_t s_mask[MOE_MAX_EXPERTS * W];
-    for (int i = threadIdx.x; i < E * W; i += blockDim.x) s_mask[i] = 0u;
-    __syncthreads();
-    const int t = blockIdx.x * kSortTok + threadIdx.x;
-    const int word = threadIdx.x >> 5;
-    const uint32_t bit = 1u << (threadIdx.x & 31);
-    int mine[MOE_MAX_K];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
-    if (t < T) {
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[(size_t)t * k + j];
-            bool ok = (e >= 0 && e < E);
-            for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);  // repeats were rejected by the histogram
-            if (ok) {
-                mine[j] = e;
-                atomicOr(&s_mask[e * W + word], bit);
+    __shared__ int s_h[MOE_MAX_EXPERTS];
+    __shared__ int s_scan[kSortTok];
+    __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+    __shared__ int s_aoff[MOE_MAX_EXPERTS + 1];
+    __shared__ int s_kept[MOE_MAX_EXPERTS];
+    const int tid = threadIdx.x;
+    const int G = gridDim.x;
+
+    // ---- phase 1: chunk histograms
+    for (int ch = blockIdx.x; ch < a.nchunk; ch += G) {
+        for (int e = tid; e < a.E; e += blockDim.x) s_h[e] = 0;
+        __syncthreads();
+        const int t = ch * kSortTok + tid;
+        if (t < a.T) {
+            int mine[MOE_MAX_K];
+            for (int j = 0; j < a.k; ++j) {
+                const int e = a.idx[(size_t)t * a.k + j];
+                bool ok = (e >= 0 && e < a.E);
+                for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
+                mine[j] = ok ? e : -1;
+                if (ok) atomicAdd(&s_h[e], 1);
+                else raise_error(a.err, kErrBounds);
             }
         }
+        __syncthreads();
+        for (int e = tid; e < a.E; e += blockDim.x) a.blk_hist[(size_t)ch * a.E + e] = s_h[e];
+        __syncthreads();
+    }
+    if (!grid_barrier(a.bar, (unsigned)G, a.err)) return;
+
+    // ---- phase 2: per-expert scans over the chunks
+    for (int e = blockIdx.x; e < a.E; e += G) {
+        int carry = 0;
+        for (int c0 = 0; c0 < a.nchunk; c0 += kSortTok) {
+            const int n = min(kSortTok, a.nchunk - c0);
+            s_scan[tid] = tid < n ? __ldcg(a.blk_hist + (size_t)(c0 + tid) * a.E + e) : 0;
+            const int tot = block_exclusive_scan(s_scan, n);
+            if (tid < n) a.blk_base[(size_t)(c0 + tid) * a.E + e] = carry + s_scan[tid];
+            carry += tot;
+            __syncthreads();
+        }
+        if (tid == 0) a.counts[e] = carry;
+    }
+    if (!grid_barrier(a.bar, 2u * (unsigned)G, a.err)) return;
+
+    // ---- phase 3: offsets (every block), then ranks and the bucket layout
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        const int cnt = __ldcg(a.counts + e);
+        const int kept = min(cnt, a.C);
+        s_kept[e] = kept;
+        s_scan[e] = (kept + a.align - 1) / a.align * a.align;
+        s_aoff[e] = cnt;
     }
     __syncthreads();
-    if (t >= T) return;
-    for (int j = 0; j < k; ++j) {
-        const int e = mine[j];
-        if (e < 0) continue;
-        const uint32_t* m = s_mask + e * W;
-        int local = __popc(m[word] & (bit - 1u));
-        for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
-        const int rank = blk_base[(size_t)blockIdx.x * E + e] + local;
-        assign_tok[assign_off[e] + rank] = t * k + j;
-        if (slot_row) {
-            if (rank < C) {
-                const int row = offsets[e] + rank;
-                slot_row[(size_t)t * k + j] = row;
-                row_token[row] = t;
-            } else {
-                slot_row[(size_t)t * k + j] = -1;
+    const int rows_total = block_exclusive_scan(s_scan, a.E);
+    for (int e = tid; e < a.E; e += blockDim.x) s_off[e] = s_scan[e];
+    if (tid == 0) s_off[a.E] = rows_total;
+    __syncthreads();
+    for (int e = tid; e < a.E; e += blockDim.x) s_scan[e] = s_aoff[e];
+    __syncthreads();
+    const int assign_total = block_exclusive_scan(s_scan, a.E);
+    for (int e = tid; e < a.E; e += blockDim.x) s_aoff[e] = s_scan[e];
+    if (tid == 0) s_aoff[a.E] = assign_total;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= a.E; e += blockDim.x) {
+            a.assign_off[e] = s_aoff[e];
+            if (a.offsets) a.offsets[e] = s_off[e];
+            if (a.kept && e < a.E) a.kept[e] = s_kept[e];
+        }
+        if (a.n_dropped && tid == 0) {
+            int tk = 0;
+            for (int e = 0; e < a.E; ++e) tk += s_kept[e];
+            *a.n_dropped = a.T * a.k - tk;
+        }
+    }
+    // padding rows of the buckets this block owns
+    if (a.row_token) {
+        for (int e = blockIdx.x; e < a.E; e += G)
+            for (int r = s_off[e] + s_kept[e] + tid; r < s_off[e + 1]; r += blockDim.x) a.row_token[r] = -1;
+    }
+    for (int ch = blockIdx.x; ch < a.nchunk; ch += G) {
+        for (int i = tid; i < a.E * W; i += blockDim.x) s_mask[i] = 0u;
+        __syncthreads();
+        const int t = ch * kSortTok + tid;
+        const int word = tid >> 5;
+        const uint32_t bit = 1u << (tid & 31);
+        int mine[MOE_MAX_K];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
+        if (t < a.T) {
+            for (int j = 0; j < a.k; ++j) {
+                const int e = a.idx[(size_t)t * a.k + j];
+                bool ok = (e >= 0 && e < a.E);
+                for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
+                if (ok) {
+                    mine[j] = e;
+                    atomicOr(&s_mask[e * W + word], bit);
+                }
             }
         }
+        __syncthreads();
+        if (t < a.T) {
+            for (int j = 0; j < a.k; ++j) {
+                const int e = mine[j];
+                if (e < 0) {
+                    if (a.slot_row) a.slot_row[(size_t)t * a.k + j] = -1;
+                    continue;
+                }
+                const uint32_t* m = s_mask + e * W;
+                int local = __popc(m[word] & (bit - 1u));
+                for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
+                const int rank = __ldcg(a.blk_base + (size_t)ch * a.E + e) + local;
+                a.assign_tok[s_aoff[e] + rank] = t * a.k + j;
+                if (a.slot_row) {
+                    if (rank < a.C) {
+                        const int row = s_off[e] + rank;
+                        a.slot_row[(size_t)t * a.k + j] = row;
+                        a.row_token[row] = t;
+                    } else {
+                        a.slot_row[(size_t)t * a.k + j] = -1;
+                    }
+                }
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -178,38 +266,50 @@ void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s) {
     s->assign_off = ws.take<int32_t>((size_t)c.E + 1);
     s->assign_tok = ws.take<int32_t>((size_t)c.T * c.k + 1);
     s->counts = ws.take<int32_t>((size_t)c.E);
+    s->bar = ws.take<unsigned>(1);
+}
+
+// Blocks of sort_kernel that fit on the device at once (the grid barriers need them all resident).
+static int sort_coresident_blocks() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sort_kernel, kSortTok, 0) != cudaSuccess)
+            per_sm = 1;
+        cached[dev] = std::max(1, per_sm) * num_sms();
+    }
+    return cached[dev];
 }
 
 cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScratch& s,
                         int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
                         int32_t* n_dropped, cudaStream_t st) {
-    const int nblk = sort_blocks(c.T);
-    int* err = device_error_word();
-    if (c.T == 0) {
-        cudaError_t e = cudaMemsetAsync(s.blk_hist, 0, sizeof(int32_t) * c.E, st);
-        if (e != cudaSuccess) return e;
-    } else {
-        hist_kernel<<<nblk, kSortTok, 0, st>>>(idx, c.T, c.k, c.E, s.blk_hist, err);
-        count_launch();
-    }
-    scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(s.blk_hist, nblk, c.E, c.T, c.k, c.capacity, c.row_align,
-                                               s.blk_base, s.counts, s.assign_off, kept, offsets,
-                                               n_dropped);
+    SortArgs a{};
+    a.idx = idx; a.T = c.T; a.k = c.k; a.E = c.E; a.C = c.capacity; a.align = c.row_align;
+    a.nchunk = sort_blocks(c.T);
+    a.blk_hist = s.blk_hist; a.blk_base = s.blk_base; a.counts = s.counts;
+    a.assign_off = s.assign_off; a.assign_tok = s.assign_tok;
+    a.kept = kept; a.offsets = offsets; a.row_token = row_token; a.slot_row = slot_row;
+    a.n_dropped = n_dropped; a.bar = s.bar; a.err = device_error_word();
+    cudaError_t e = cudaMemsetAsync(s.bar, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(a.nchunk, std::min(sort_coresident_blocks(), 2 * num_sms())));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kSortTok);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sort_kernel, a);
     count_launch();
-    if (row_token) {
-        cudaError_t e = cudaMemsetAsync(row_token, 0xff, sizeof(int32_t) * (size_t)c.rows_capacity, st);
-        if (e != cudaSuccess) return e;
-    }
-    if (slot_row && c.T > 0) {  // assignments rejected as invalid stay -1
-        cudaError_t e = cudaMemsetAsync(slot_row, 0xff, sizeof(int32_t) * (size_t)c.T * c.k, st);
-        if (e != cudaSuccess) return e;
-    }
-    if (c.T > 0) {
-        rank_kernel<<<nblk, kSortTok, 0, st>>>(idx, c.T, c.k, c.E, c.capacity, s.blk_base,
-                                               s.assign_off, offsets, s.assign_tok, slot_row,
-                                               row_token);
-        count_launch();
-    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

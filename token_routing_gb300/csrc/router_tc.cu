@@ -21,11 +21,12 @@ using namespace tc;
 
 constexpr int RBM = 128;
 constexpr int RBK = 64;
-constexpr int RSTAGES = 4;
+constexpr int RMAX_STAGES = 12;              // ring depth: as many stages as fit in ~200 KB
+constexpr int RSMEM_BUDGET = 200 * 1024;
 constexpr int RTHREADS = 192;
 
 struct RouteTcParams {
-    int T, d, E, E_pad;
+    int T, d, E, E_pad, stages;
     float inv_temp;
     const float* bg;
     int32_t* idx;
@@ -43,9 +44,10 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_bytes = route_stage_bytes(p.E_pad);
+    const int RSTAGES = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RSTAGES * stage_bytes);
-    uint64_t* empty = full + RSTAGES;
-    uint64_t* tfull = empty + RSTAGES;
+    uint64_t* empty = full + RMAX_STAGES;
+    uint64_t* tfull = empty + RMAX_STAGES;
     uint64_t* drain = tfull + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* s_cnt = reinterpret_cast<int*>(tmem_slot + 4);
@@ -203,8 +205,9 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     CUtensorMap tx, tw;
     if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, RBM)) return cudaErrorInvalidValue;
     if (!make_map(&tw, Wg, (uint64_t)c.d, (uint64_t)c.E, (uint32_t)p.E_pad)) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + (size_t)RSTAGES * route_stage_bytes(p.E_pad) + 16 * sizeof(uint64_t) + 16 +
-                        2 * MOE_MAX_EXPERTS * sizeof(int);
+    p.stages = std::max(2, std::min(RMAX_STAGES, RSMEM_BUDGET / route_stage_bytes(p.E_pad)));
+    const size_t smem = 1024 + (size_t)p.stages * route_stage_bytes(p.E_pad) +
+                        (2 * RMAX_STAGES + 4) * sizeof(uint64_t) + 16 + 2 * MOE_MAX_EXPERTS * sizeof(int);
     switch (c.k) {
         case 1: return launch_k<1>(p, tx, tw, smem, s);
         case 2: return launch_k<2>(p, tx, tw, smem, s);
