@@ -316,3 +316,22 @@ def dense_soft_moe(inp, temperature=1.0):
         _, _, Ye = expert_ffn(x, inp["W1"][e], inp["b1"][e], inp["W2"][e], inp["b2"][e])
         y += g[:, e:e + 1] * Ye
     return dict(z=z, g=g, y=y)
+
+
+# ----------------------------------------------------------------------------- co-selection
+
+def coselection(idx, E):
+    """Expert co-selection matrix of one batch (Expert-Parallelism page, section 3.2, step 1:
+    how often experts i and j are chosen by the same token). The page calls the matrix
+    asymmetric, which a plain co-occurrence count is not; the reading taken here: for i != j,
+    H[i][j] = number of tokens whose top-k holds i in an earlier slot (a higher logit) than
+    j, so H + H^T is the co-occurrence count; H[i][i] = number of tokens that chose i."""
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    Hm = np.zeros((E, E), dtype=np.int64)
+    for t in range(T):
+        for a in range(k):
+            Hm[idx[t, a], idx[t, a]] += 1
+            for b in range(a + 1, k):
+                Hm[idx[t, a], idx[t, b]] += 1
+    return Hm

@@ -335,3 +335,38 @@ def test_zipf_calibration_reaches_forty_percent():
     r = O.route(inp["x"].double().numpy(), inp["Wg"].double().numpy(), inp["bg"].double().numpy(), 2)
     share = (r["idx"] == 0).any(axis=1).mean()
     assert 0.37 < share < 0.43
+
+
+# ------------------------------------------------------------------ co-selection matrix
+
+def test_golden_coselection():
+    g = _load("coselection_hand.json")
+    assert O.coselection(np.array(g["idx"]), g["E"]).tolist() == g["H"]
+
+
+def test_coselection_against_one_hot_products():
+    """H + H^T off the diagonal equals A^T A of the one-hot selection matrix A [T, E]; the
+    diagonal is the per-expert count; slot order decides which triangle a pair lands in."""
+    rng = np.random.default_rng(77)
+    T, E, k = 300, 10, 4
+    z = rng.standard_normal((T, E))
+    idx, _ = O.select_topk(z, k)
+    Hm = O.coselection(idx, E)
+    A = np.zeros((T, E), dtype=np.int64)
+    np.put_along_axis(A, idx, 1, axis=1)
+    co = A.T @ A
+    off = ~np.eye(E, dtype=bool)
+    assert (np.diag(Hm) == O.expert_counts(idx, E)).all()
+    assert ((Hm + Hm.T)[off] == co[off]).all()
+    # i before j in the slots means z_i > z_j: brute force over the logits
+    ref = np.zeros((E, E), dtype=np.int64)
+    for t in range(T):
+        sel = set(idx[t].tolist())
+        for i in sel:
+            for j in sel:
+                if i != j and (z[t, i] > z[t, j] or (z[t, i] == z[t, j] and i < j)):
+                    ref[i, j] += 1
+    assert (Hm[off] == ref[off]).all()
+    # each chosen expert pairs with the k-1 others of its token
+    assert ((Hm + Hm.T).sum(axis=1) - 2 * np.diag(Hm) == np.diag(Hm) * (k - 1)).all()
+    assert (O.coselection(idx[:, :1], E)[off] == 0).all()
