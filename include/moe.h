@@ -187,6 +187,16 @@ MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const
                           void* dx, float* dWg, void* dW1, float* db1, void* dW2, float* db2,
                           float* dbg, float* dw, float* loss, void* ws, moe_stream_t stream);
 
+/* Expert co-selection matrix of a batch: "Expert Parallelism: Scaling Mixture-of-Experts
+ * Models", section 3.2, step 1 (experts chosen by the same token; the input of the page's
+ * affinity-aware placement). The page calls the matrix asymmetric; accordingly, for i != j,
+ *   H[i][j] = number of tokens whose top-k holds i in an earlier slot (higher logit) than j,
+ * so H + H^T is the co-occurrence count, and H[i][i] = number of tokens that chose i.
+ *   idx [T,k] int32 (as from moe_route) -> H [E,E] int32 (overwritten). Device pointers.
+ * Entries out of [0,E) or repeated within a token set MOE_ERR_DEVICE_BOUNDS and are skipped. */
+MOE_API moe_status_t moe_coselect(const moe_config_t* cfg, const int32_t* idx, int32_t* H,
+                                  moe_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of the current
  * device: MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS; MOE_ERR_CUDA if the
  * stream reports a CUDA error. */

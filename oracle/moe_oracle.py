@@ -103,9 +103,50 @@ def balance_loss(counts):
     return float(np.mean((load - load.mean()) ** 2))
 
 
-def route(x, Wg, bg, k, temperature=1.0):
-    """Gate linear, top-k, softmax over the k, counts and balance loss."""
+# ----------------------------------------------------------------------------- routing noise
+
+_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
+_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
+_U64 = (1 << 64) - 1
+
+
+def philox4x64_10(counter, key):
+    """Philox4x64-10 counter-based generator (Salmon, Moraes, Dror, Shaw, "Parallel random
+    numbers: as easy as 1, 2, 3", SC 2011): ten rounds of two 64x64->128-bit products with the
+    key bumped by the Weyl constants between rounds. Exact integer arithmetic."""
+    c = [int(v) & _U64 for v in counter]
+    k0, k1 = int(key[0]) & _U64, int(key[1]) & _U64
+    for _ in range(10):
+        p0 = _PHILOX_M[0] * c[0]
+        p1 = _PHILOX_M[1] * c[2]
+        c = [((p1 >> 64) ^ c[1] ^ k0) & _U64, p1 & _U64, ((p0 >> 64) ^ c[3] ^ k1) & _U64, p0 & _U64]
+        k0 = (k0 + _PHILOX_W[0]) & _U64
+        k1 = (k1 + _PHILOX_W[1]) & _U64
+    return c
+
+
+def routing_noise(T, E, seed):
+    """Standard normal noise for every (token t, expert e): Philox4x64-10 at counter
+    (t, e, 0, 0) with key (seed, 0); the top 24 bits of its first two outputs give
+    u1, u2 in (0, 1] and Box-Muller gives sqrt(-2 ln u1) cos(2 pi u2)."""
+    n = np.zeros((T, E))
+    for t in range(T):
+        for e in range(E):
+            o = philox4x64_10((t, e, 0, 0), (seed, 0))
+            u1 = ((o[0] >> 40) + 1) / float(1 << 24)
+            u2 = ((o[1] >> 40) + 1) / float(1 << 24)
+            n[t, e] = math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+    return n
+
+
+def route(x, Wg, bg, k, temperature=1.0, noise_std=0.0, noise_seed=0):
+    """Gate linear, top-k, softmax over the k, counts and balance loss. With noise_std > 0 the
+    logits get noise_std * N(0,1) before the selection and the softmax (training-time routing
+    noise, PyTorch-MoE page, section 4.3: logits + randn_like(logits) * 0.1); the noise is a
+    constant for the backward."""
     z = gate_logits(x, Wg, bg)
+    if noise_std > 0:
+        z = z + noise_std * routing_noise(z.shape[0], z.shape[1], noise_seed)
     idx, z_sel = select_topk(z, k)
     w = routing_weights(z_sel, temperature)
     counts = expert_counts(idx, z.shape[1])
@@ -211,12 +252,12 @@ def combine(Yp, w, slot_row, T):
 
 # ----------------------------------------------------------------------------- whole layer
 
-def forward(inp, k, temperature=1.0, C=None, align=1):
+def forward(inp, k, temperature=1.0, C=None, align=1, noise_std=0.0, noise_seed=0):
     """Forward of the layer. `inp` holds x, Wg, bg, W1, b1, W2, b2 (any array type)."""
     x = _f64(inp["x"])
     T = x.shape[0]
     E = np.asarray(inp["Wg"]).shape[0]
-    r = route(x, inp["Wg"], inp.get("bg"), k, temperature)
+    r = route(x, inp["Wg"], inp.get("bg"), k, temperature, noise_std, noise_seed)
     dsp = dispatch(r["idx"], E, C, align)
     Xp = permute(x, dsp["row_token"])
     f = np.asarray(inp["W1"]).shape[1]

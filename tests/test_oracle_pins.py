@@ -370,3 +370,37 @@ def test_coselection_against_one_hot_products():
     # each chosen expert pairs with the k-1 others of its token
     assert ((Hm + Hm.T).sum(axis=1) - 2 * np.diag(Hm) == np.diag(Hm) * (k - 1)).all()
     assert (O.coselection(idx[:, :1], E)[off] == 0).all()
+
+
+# ------------------------------------------------------------------ routing noise
+
+def test_philox_matches_numpy_bit_generator():
+    """The oracle's Philox4x64-10 against numpy's Philox bit generator (same published
+    algorithm; numpy advances its counter by one before each block of four outputs)."""
+    for ctr, key in [((0, 0, 0, 0), (0, 0)), ((5, 7, 0, 0), (11, 13)),
+                     ((2**62 + 3, 3, 2**61, 9), (2**63 - 5, 42)), ((123456, 255, 0, 0), (987654321, 0))]:
+        bg = np.random.Philox(counter=np.array(ctr, dtype=np.uint64), key=np.array(key, dtype=np.uint64))
+        ref = [int(v) for v in bg.random_raw(4)]
+        nxt = [ctr[0] + 1] + list(ctr[1:])
+        assert O.philox4x64_10(nxt, key) == ref
+
+
+def test_routing_noise_is_standard_normal():
+    n = O.routing_noise(400, 250, seed=3).reshape(-1)
+    assert abs(n.mean()) < 0.01
+    assert abs(n.std() - 1.0) < 0.01
+    assert abs(((n - n.mean()) ** 4).mean() / n.var() ** 2 - 3.0) < 0.1   # kurtosis of a normal
+    assert abs((n > 1.0).mean() - 0.15865525393145707) < 0.004           # 1 - Phi(1)
+    # different seeds and different (t, e) give different draws
+    assert not np.array_equal(O.routing_noise(3, 4, 1), O.routing_noise(3, 4, 2))
+
+
+def test_noisy_route_is_plain_route_of_noisy_logits():
+    inp = _rand_inputs(50, 8, 12, 4, seed=91)
+    noisy = O.route(inp["x"], inp["Wg"], None, 2, 1.0, noise_std=0.1, noise_seed=5)
+    zn = O.gate_logits(inp["x"], inp["Wg"]) + 0.1 * O.routing_noise(50, 12, 5)
+    idx, zsel = O.select_topk(zn, 2)
+    assert (noisy["idx"] == idx).all()
+    np.testing.assert_allclose(noisy["w"], O.routing_weights(zsel), atol=1e-15)
+    plain = O.route(inp["x"], inp["Wg"], None, 2, 1.0, noise_std=0.0, noise_seed=5)
+    assert (plain["idx"] == O.select_topk(O.gate_logits(inp["x"], inp["Wg"]), 2)[0]).all()

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_expert_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_backward": (ctypes.c_int, [_CFG] + [_P] * 26),
+    "moe_coselect": (ctypes.c_int, [_CFG, _P, _P, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_kernel_launches": (ctypes.c_uint64, []),

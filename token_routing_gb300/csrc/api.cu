@@ -325,6 +325,13 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     return MOE_OK;
 }
 
+moe_status_t moe_coselect(const moe_config_t* cfg, const int32_t* idx, int32_t* H, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!H || (cfg->T > 0 && !idx)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_coselect(*cfg, idx, H, (cudaStream_t)stream));
+}
+
 moe_status_t moe_get_error(moe_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;

@@ -80,6 +80,9 @@ cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cuda
 // row GEMMs on CTA pairs: 256-row tiles, needs cfg.row_align == 256
 cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
 
+// coselect.cu: expert co-selection matrix H [E, E]
+cudaError_t launch_coselect(const moe_config_t& c, const int32_t* idx, int32_t* H, cudaStream_t s);
+
 // combine.cu
 cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,
                            const float* w, void* y, cudaStream_t s);

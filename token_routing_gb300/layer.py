@@ -102,6 +102,11 @@ def backward(cfg, dy, x, Wg, W1, W2, b, stream=None, want_dbg=True, want_dw=True
         _s(stream)))
 
 
+def coselect(cfg, idx, H, stream=None):
+    """Expert co-selection matrix H [E, E] int32 of the routing indices idx [T, k]."""
+    L.check("moe_coselect", L.load().moe_coselect(ctypes.byref(cfg), _p(idx), _p(H), _s(stream)))
+
+
 def forward(cfg, p, x, b, stream=None):
     """route -> dispatch -> expert_ffn -> combine; p holds Wg, bg, W1, b1, W2, b2."""
     route(cfg, x, p["Wg"], p.get("bg"), b, stream)
