@@ -92,6 +92,13 @@ typedef struct {
     float aux_loss_weight;     /* weight of balance_loss in the reported loss (0.01 on the pages) */
     int32_t has_gate_bias;     /* 0/1: bg is added to the logits */
     int32_t dtype;             /* moe_dtype_t */
+    float noise_std;           /* >= 0: training-time routing noise, logits += noise_std * N(0,1)
+                                  before top-k and softmax ("PyTorch distributed MoE training",
+                                  section 4.3: randn_like(logits) * 0.1); 0 = off */
+    uint32_t noise_seed;       /* noise of (token t, expert e): Philox4x64-10 at counter
+                                  (t, e, 0, 0), key (noise_seed, 0); top 24 bits of the first
+                                  two outputs -> u1, u2 in (0,1]; sqrt(-2 ln u1) cos(2 pi u2).
+                                  Vary the seed from step to step. */
     /* derived by moe_config_init */
     int32_t capacity;          /* ceil(capacity_factor*T*k/E) in double, or INT32_MAX */
     int32_t rows_capacity;     /* rows of every permuted buffer (Xp, A, H, Yp) */

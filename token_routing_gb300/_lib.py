@@ -30,6 +30,7 @@ class MoeConfig(ctypes.Structure):
         ("d_ff", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
         ("temperature", ctypes.c_float), ("aux_loss_weight", ctypes.c_float),
         ("has_gate_bias", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("noise_std", ctypes.c_float), ("noise_seed", ctypes.c_uint32),
         ("capacity", ctypes.c_int32), ("rows_capacity", ctypes.c_int32),
         ("row_align", ctypes.c_int32),
     ]

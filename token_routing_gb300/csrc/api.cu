@@ -59,6 +59,7 @@ moe_status_t check_fields(const moe_config_t* c) {
     if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_loss_weight)) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->has_gate_bias != 0 && c->has_gate_bias != 1) return MOE_ERR_INVALID_ARG;
+    if (!(c->noise_std >= 0.0f) || !std::isfinite(c->noise_std)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)c->T * c->k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
     const int64_t rows = derived_rows(*c, derived_capacity(*c));
     if (rows > INT32_MAX || rows * (int64_t)std::max(c->d, c->d_ff) > ((int64_t)1 << 40))

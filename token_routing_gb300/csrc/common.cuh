@@ -123,6 +123,27 @@ __device__ __forceinline__ float gelu_grad_f(float a) {
     return Phi + a * phi;
 }
 
+// Training-time routing noise: a standard normal per (token, expert) from the Philox4x64-10
+// counter-based generator (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC 2011) at counter (t, e, 0, 0), key (seed, 0); the top 24 bits of the first two
+// outputs give u1, u2 in (0, 1] and Box-Muller gives sqrt(-2 ln u1) cos(2 pi u2).
+__device__ __forceinline__ float routing_noise(int t, int e, uint32_t seed) {
+    uint64_t c0 = (uint64_t)(uint32_t)t, c1 = (uint64_t)(uint32_t)e, c2 = 0, c3 = 0;
+    uint64_t k0 = seed, k1 = 0;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t lo0 = 0xD2E7470EE14C6C93ull * c0, hi0 = __umul64hi(0xD2E7470EE14C6C93ull, c0);
+        const uint64_t lo1 = 0xCA5A826395121157ull * c2, hi1 = __umul64hi(0xCA5A826395121157ull, c2);
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+        k0 += 0x9E3779B97F4A7C15ull;
+        k1 += 0xBB67AE8584CAA73Bull;
+    }
+    const float u1 = (float)((c0 >> 40) + 1) * 5.9604644775390625e-8f;  // 2^-24
+    const float u2 = (float)((c1 >> 40) + 1) * 5.9604644775390625e-8f;
+    return sqrtf(-2.0f * logf(u1)) * cosf(6.28318530717958648f * u2);
+}
+
 // ---------------------------------------------------------------- host side
 extern std::atomic<uint64_t> g_launches;
 inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }

@@ -30,7 +30,7 @@ __device__ __forceinline__ bool beats(float v1, int e1, float v2, int e2) {
 template <typename T>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __restrict__ bg,
-             int Tn, int d, int E, int k, float inv_temp,
+             int Tn, int d, int E, int k, float inv_temp, float noise_std, uint32_t noise_seed,
              int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts) {
     extern __shared__ float smem[];
     float* xs = smem;                                    // [kRouteTok][kRouteKc+1]
@@ -82,7 +82,11 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             const int e = tx + 32 * b;
-            if (b < nb && e < E) lg[(ty + 8 * a) * E + e] = acc[a][b] + (bg ? bg[e] : 0.f);
+            if (b < nb && e < E) {
+                float v = acc[a][b] + (bg ? bg[e] : 0.f);
+                if (noise_std > 0.f) v = fmaf(noise_std, routing_noise(tok0 + ty + 8 * a, e, noise_seed), v);
+                lg[(ty + 8 * a) * E + e] = v;
+            }
         }
     __syncthreads();
 
@@ -167,12 +171,14 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
             auto kern = route_kernel<__nv_bfloat16>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             kern<<<grid, kRouteThreads, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
-                                                   bias, c.T, c.d, c.E, c.k, inv_temp, idx, w, counts);
+                                                   bias, c.T, c.d, c.E, c.k, inv_temp, c.noise_std, c.noise_seed,
+                                                   idx, w, counts);
         } else {
             auto kern = route_kernel<float>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             kern<<<grid, kRouteThreads, smem, s>>>((const float*)x, (const float*)Wg, bias, c.T, c.d,
-                                                   c.E, c.k, inv_temp, idx, w, counts);
+                                                   c.E, c.k, inv_temp, c.noise_std, c.noise_seed, idx, w,
+                                                   counts);
         }
         count_launch();
         st = cudaGetLastError();

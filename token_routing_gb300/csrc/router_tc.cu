@@ -28,6 +28,8 @@ constexpr int RTHREADS = 192;
 struct RouteTcParams {
     int T, d, E, E_pad, stages;
     float inv_temp;
+    float noise_std;
+    uint32_t noise_seed;
     const float* bg;
     int32_t* idx;
     float* w;
@@ -138,6 +140,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     int e = c + i;
                     if (e < p.E) {
                         float v = __uint_as_float(r[i]) + s_bias[e];
+                        if (p.noise_std > 0.f) v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed), v);
                         // insert into the list sorted by (logit desc, id asc); experts arrive in
                         // ascending id, so an equal logit never displaces an earlier one
 #pragma unroll
@@ -199,6 +202,8 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.T = c.T; p.d = c.d; p.E = c.E;
     p.E_pad = (c.E + 31) / 32 * 32;
     p.inv_temp = 1.0f / c.temperature;
+    p.noise_std = c.noise_std;
+    p.noise_seed = c.noise_seed;
     p.bg = c.has_gate_bias ? bg : nullptr;
     p.idx = idx; p.w = w; p.counts = counts;
     p.err = device_error_word();

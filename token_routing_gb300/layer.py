@@ -24,21 +24,23 @@ def _s(stream=None):
 
 
 def make_config(T, d, E, k, d_ff, capacity_factor=None, temperature=1.0, aux_loss_weight=0.01,
-                has_gate_bias=False, dtype="bf16"):
+                has_gate_bias=False, dtype="bf16", noise_std=0.0, noise_seed=0):
     """Fill and validate a moe_config_t (raises MoeError on an invalid configuration)."""
     cfg = L.MoeConfig(T=T, d=d, E=E, k=k, d_ff=d_ff,
                       capacity_factor=0.0 if capacity_factor is None else float(capacity_factor),
                       temperature=float(temperature), aux_loss_weight=float(aux_loss_weight),
-                      has_gate_bias=int(bool(has_gate_bias)), dtype=MOE_DTYPE[dtype])
+                      has_gate_bias=int(bool(has_gate_bias)), dtype=MOE_DTYPE[dtype],
+                      noise_std=float(noise_std), noise_seed=int(noise_seed) & 0xFFFFFFFF)
     L.check("moe_config_init", L.load().moe_config_init(ctypes.byref(cfg)))
     return cfg
 
 
-def config_from(layer_cfg):
+def config_from(layer_cfg, noise_std=0.0, noise_seed=0):
     """moe_config_t of a synth.LayerConfig-like record."""
     return make_config(layer_cfg.T, layer_cfg.d, layer_cfg.E, layer_cfg.k, layer_cfg.d_ff,
                        layer_cfg.capacity_factor, layer_cfg.temperature,
-                       layer_cfg.aux_loss_weight, layer_cfg.gate_bias != "none", layer_cfg.dtype)
+                       layer_cfg.aux_loss_weight, layer_cfg.gate_bias != "none", layer_cfg.dtype,
+                       noise_std, noise_seed)
 
 
 def workspace_bytes(cfg):
