@@ -376,3 +376,30 @@ def coselection(idx, E):
             for b in range(a + 1, k):
                 Hm[idx[t, a], idx[t, b]] += 1
     return Hm
+
+
+# ----------------------------------------------------------------------------- soft balance loss
+
+def soft_load(z, temperature=1.0):
+    """Differentiable expert load: P_e = sum_t softmax(z_t / temperature)_e over all E experts
+    (the gate probabilities of Expert-Parallelism page 2.2, summed over the batch)."""
+    p = routing_weights(z, temperature)   # softmax over all columns
+    return p, p.sum(axis=0)
+
+
+def soft_balance_loss(P, weight):
+    """weight * mean_e (P_e - mean(P))^2: the PyTorch-MoE page 3.3 balance_loss applied to the
+    soft load instead of the integer counts, so that it has a gradient."""
+    P = _f64(P)
+    return float(weight * np.mean((P - P.mean()) ** 2))
+
+
+def soft_balance_grad(z, temperature, weight):
+    """d soft_balance_loss / d z [T, E]: g_e = weight * 2 (P_e - mean P) / E (the mean term
+    drops out since sum_e (P_e - mean P) = 0), then the softmax Jacobian per token,
+    dz_te = p_te (g_e - sum_j p_tj g_j) / temperature."""
+    p, P = soft_load(z, temperature)
+    E = P.shape[0]
+    g = weight * 2.0 * (P - P.mean()) / E
+    s = (p * g[None, :]).sum(axis=1, keepdims=True)
+    return p * (g[None, :] - s) / temperature

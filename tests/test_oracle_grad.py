@@ -90,3 +90,49 @@ def test_backward_matches_torch_autograd():
     np.testing.assert_allclose(fwd["y"], y.detach().numpy(), atol=1e-12)
     for p, gname in {"x": "dx", "Wg": "dWg", "bg": "dbg", "W1": "dW1", "b1": "db1", "W2": "dW2", "b2": "db2"}.items():
         np.testing.assert_allclose(g[gname], tt[p].grad.numpy(), atol=1e-11, err_msg=gname)
+
+
+def test_soft_balance_gradient_matches_central_differences():
+    """The soft balance loss w.r.t. x, Wg and bg through z = x Wg^T + bg."""
+    rng = np.random.default_rng(123)
+    T, d, E, temp, lam = 9, 4, 6, 0.7, 0.3
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, d)) * 0.5
+    bg = rng.standard_normal(E) * 0.2
+
+    def loss(x_, Wg_, bg_):
+        _, P = O.soft_load(O.gate_logits(x_, Wg_, bg_), temp)
+        return O.soft_balance_loss(P, lam)
+
+    dZ = O.soft_balance_grad(O.gate_logits(x, Wg, bg), temp, lam)
+    grads = {"x": dZ @ Wg, "Wg": dZ.T @ x, "bg": dZ.sum(axis=0)}
+    h = 1e-6
+    for name, arr in (("x", x), ("Wg", Wg), ("bg", bg)):
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            o = arr[i]
+            arr[i] = o + h
+            lp = loss(x, Wg, bg)
+            arr[i] = o - h
+            lm = loss(x, Wg, bg)
+            arr[i] = o
+            fd[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grads[name], fd, atol=1e-8, rtol=1e-6, err_msg=name)
+
+
+def test_soft_balance_closed_forms():
+    T, E = 12, 4
+    z = np.zeros((T, E))                       # uniform probabilities: P_e = T/E, loss 0
+    _, P = O.soft_load(z)
+    np.testing.assert_allclose(P, T / E)
+    assert O.soft_balance_loss(P, 0.5) == 0.0
+    np.testing.assert_allclose(O.soft_balance_grad(z, 1.0, 0.5), 0.0, atol=1e-15)
+    z = np.full((T, E), -50.0)
+    z[:, 2] = 50.0                             # every token certain of expert 2
+    _, P = O.soft_load(z)
+    np.testing.assert_allclose(P, [0, 0, T, 0], atol=1e-12)
+    assert O.soft_balance_loss(P, 1.0) == pytest.approx(T ** 2 * (E - 1) / E ** 2, rel=1e-12)
+    # sum over experts of each token's gradient vanishes (softmax Jacobian rows sum to 0)
+    rng = np.random.default_rng(4)
+    zz = rng.standard_normal((T, E))
+    np.testing.assert_allclose(O.soft_balance_grad(zz, 0.5, 2.0).sum(axis=1), 0.0, atol=1e-12)
