@@ -119,11 +119,13 @@ MOE_API size_t moe_workspace_bytes(const moe_config_t* cfg);
 /* Gate linear + top-k + softmax over the k + expert counts + balance loss.
  *   x [T,d] act, Wg [E,d] act, bg [E] fp32 (read iff cfg->has_gate_bias, else may be NULL)
  *   -> idx [T,k] int32 (slot j = j-th largest logit), w [T,k] fp32 (rows sum to 1),
- *      counts [E] int32 (pre-capacity choices, sum = T*k), balance_loss [1] fp32.
+ *      counts [E] int32 (pre-capacity choices, sum = T*k), balance_loss [1] fp32,
+ *      logits [T,E] fp32 (nullable: the routing logits z = x Wg^T + bg + noise; needed by
+ *      moe_soft_balance).
  * Logits are accumulated in fp32. All pointers are device pointers. */
 MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
                        int32_t* idx, float* w, int32_t* counts, float* balance_loss,
-                       void* ws, moe_stream_t stream);
+                       float* logits, void* ws, moe_stream_t stream);
 
 /* Capacity, stable counting sort into expert buckets and the gather of x.
  *   idx [T,k] int32, x [T,d] act
@@ -193,6 +195,26 @@ MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const
                           const void* W2, const float* balance_loss,
                           void* dx, float* dWg, void* dW1, float* db1, void* dW2, float* db2,
                           float* dbg, float* dw, float* loss, void* ws, moe_stream_t stream);
+
+/* Differentiable balance loss on the soft expert load. The integer counts of balance_loss
+ * ("PyTorch distributed MoE training", section 3.3) have no gradient; here the same
+ * squared-deviation form is applied to the soft load of the gate probabilities
+ * ("Expert Parallelism: Scaling Mixture-of-Experts Models", sections 2.2-2.3):
+ *   P_e = sum_t softmax(logits_t / temperature)_e,  loss = weight * mean_e (P_e - T/E)^2.
+ *   logits [T,E] fp32 (from moe_route) -> P [E] fp32, loss [1] fp32. Fixed-order sums.
+ * Scratch from ws (moe_workspace_bytes covers it). */
+MOE_API moe_status_t moe_soft_balance(const moe_config_t* cfg, const float* logits, float weight,
+                                      float* P, float* loss, void* ws, moe_stream_t stream);
+
+/* Gradient of moe_soft_balance's loss, ADDED to the layer gradients:
+ *   dz_te = p_te (g_e - sum_j p_tj g_j) / temperature, g_e = weight * 2 (P_e - T/E) / E,
+ *   dx += dz Wg, dWg += dz^T x, dbg += sum_t dz (dbg nullable).
+ *   logits [T,E], P [E] (from moe_soft_balance), x [T,d] act, Wg [E,d] act;
+ *   dx [T,d] act, dWg [E,d] fp32, dbg [E] fp32 are read and updated in place. */
+MOE_API moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const float* logits,
+                                               const float* P, float weight, const void* x,
+                                               const void* Wg, void* dx, float* dWg, float* dbg,
+                                               void* ws, moe_stream_t stream);
 
 /* Expert co-selection matrix of a batch: "Expert Parallelism: Scaling Mixture-of-Experts
  * Models", section 3.2, step 1 (experts chosen by the same token; the input of the page's

@@ -91,7 +91,7 @@ def test_entry_points_reject_uninitialised_config(moe_lib):
     lib = moe_lib.load()
     c = _cfg(moe_lib)  # moe_config_init not called: derived fields are 0
     p = ctypes.c_void_p(1)
-    assert lib.moe_route(ctypes.byref(c), p, p, None, p, p, p, p, p, None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(c), p, p, None, p, p, p, p, None, p, None) == moe_lib.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_bytes(ctypes.byref(c)) == 0
 
 
@@ -102,7 +102,7 @@ def test_entry_points_reject_null_pointers(moe_lib):
     p = ctypes.c_void_p(16)
     cfg = ctypes.byref(c)
     inval = moe_lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_route(cfg, None, p, None, p, p, p, p, p, None) == inval
+    assert lib.moe_route(cfg, None, p, None, p, p, p, p, None, p, None) == inval
     assert lib.moe_dispatch(cfg, p, p, p, p, p, p, None, p, p, None) == inval
     assert lib.moe_expert_ffn(cfg, p, p, p, p, None, p, p, p, p, p, None) == inval
     assert lib.moe_combine(cfg, p, None, p, p, None) == inval
@@ -112,7 +112,7 @@ def test_entry_points_reject_null_pointers(moe_lib):
     c.has_gate_bias = 1
     c2 = _cfg(moe_lib, has_gate_bias=1)
     assert lib.moe_config_init(ctypes.byref(c2)) == 0
-    assert lib.moe_route(ctypes.byref(c2), p, p, None, p, p, p, p, p, None) == inval  # bg required
+    assert lib.moe_route(ctypes.byref(c2), p, p, None, p, p, p, p, None, p, None) == inval  # bg required
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

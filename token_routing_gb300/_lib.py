@@ -50,7 +50,9 @@ _CFG = ctypes.POINTER(MoeConfig)
 _SIGS = {
     "moe_config_init": (ctypes.c_int, [_CFG]),
     "moe_workspace_bytes": (ctypes.c_size_t, [_CFG]),
-    "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_soft_balance": (ctypes.c_int, [_CFG, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "moe_soft_balance_backward": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),

@@ -96,6 +96,7 @@ struct BackwardScratch {
     float* dwg_part;
     float* colsum_d;    // column-sum partials of dYp (db2)
     float* colsum_f;    // column-sum partials of dA (db1)
+    SoftScratch soft;   // soft balance loss
 };
 
 size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
@@ -112,6 +113,7 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     b->dwg_part = ws.take<float>((size_t)c.E * dwg_chunks(c) * c.d);
     b->colsum_d = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d + 1);
     b->colsum_f = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d_ff + 1);
+    soft_scratch_take(ws, c, &b->soft);
     return align_up(ws.used, 256);
 }
 
@@ -202,14 +204,37 @@ size_t moe_workspace_bytes(const moe_config_t* cfg) {
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
-                       int32_t* idx, float* w, int32_t* counts, float* balance_loss, void* ws,
-                       moe_stream_t stream) {
+                       int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
+                       void* ws, moe_stream_t stream) {
     (void)ws;
     moe_status_t st = check_config(cfg);
     if (st != MOE_OK) return st;
     if (!Wg || !counts || !balance_loss || (cfg->has_gate_bias && !bg)) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!x || !idx || !w)) return MOE_ERR_INVALID_ARG;
-    return cuda_status(launch_route(*cfg, x, Wg, bg, idx, w, counts, balance_loss, (cudaStream_t)stream));
+    return cuda_status(launch_route(*cfg, x, Wg, bg, idx, w, counts, balance_loss, logits, (cudaStream_t)stream));
+}
+
+moe_status_t moe_soft_balance(const moe_config_t* cfg, const float* logits, float weight, float* P,
+                              float* loss, void* ws, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!P || !ws || (cfg->T > 0 && !logits) || !std::isfinite(weight)) return MOE_ERR_INVALID_ARG;
+    BackwardScratch b;
+    carve_backward(*cfg, ws, &b);
+    return cuda_status(launch_soft_balance(*cfg, logits, weight, P, loss, b.soft, (cudaStream_t)stream));
+}
+
+moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const float* logits, const float* P,
+                                       float weight, const void* x, const void* Wg, void* dx, float* dWg,
+                                       float* dbg, void* ws, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!P || !Wg || !dWg || !ws || !std::isfinite(weight)) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!logits || !x || !dx)) return MOE_ERR_INVALID_ARG;
+    BackwardScratch b;
+    carve_backward(*cfg, ws, &b);
+    return cuda_status(launch_soft_balance_bwd(*cfg, logits, P, weight, x, Wg, dx, dWg, dbg, b.soft,
+                                               (cudaStream_t)stream));
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const void* x, int32_t* kept,

@@ -40,13 +40,13 @@ struct WgradArgs {
 
 // router.cu
 cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                         int32_t* idx, float* w, int32_t* counts, float* balance_loss,
+                         int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
                          cudaStream_t s);
 
 // router_tc.cu: gate GEMM on tcgen05 + top-k + softmax + counts (bf16, d % 64 == 0)
 bool tc_route_supported(const moe_config_t& c);
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                            int32_t* idx, float* w, int32_t* counts, cudaStream_t s);
+                            int32_t* idx, float* w, int32_t* counts, float* logits, cudaStream_t s);
 
 // dispatch.cu: stable counting sort of the assignments by expert
 struct SortScratch {
@@ -79,6 +79,21 @@ cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStrea
 cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
 // row GEMMs on CTA pairs: 256-row tiles, needs cfg.row_align == 256
 cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
+
+// soft_balance.cu: differentiable balance loss on the soft load
+struct SoftScratch {
+    float* part;     // [chunks, E] per-chunk soft loads
+    float* dz;       // [T, E] gradient of the logits
+    float* dwg_part; // [splits, E, d]
+};
+int soft_chunks(const moe_config_t& c);
+int soft_splits(const moe_config_t& c);
+void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s);
+cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, float weight, float* P,
+                                float* loss, const SoftScratch& s, cudaStream_t st);
+cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, const float* P, float weight,
+                                    const void* x, const void* Wg, void* dx, float* dWg, float* dbg,
+                                    const SoftScratch& s, cudaStream_t st);
 
 // coselect.cu: expert co-selection matrix H [E, E]
 cudaError_t launch_coselect(const moe_config_t& c, const int32_t* idx, int32_t* H, cudaStream_t s);

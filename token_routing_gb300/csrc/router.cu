@@ -31,7 +31,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __restrict__ bg,
              int Tn, int d, int E, int k, float inv_temp, float noise_std, uint32_t noise_seed,
-             int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts) {
+             int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
+             float* __restrict__ logits) {
     extern __shared__ float smem[];
     float* xs = smem;                                    // [kRouteTok][kRouteKc+1]
     float* wsm = xs + kRouteTok * (kRouteKc + 1);        // [E][kRouteKc+1]
@@ -86,6 +87,7 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
                 float v = acc[a][b] + (bg ? bg[e] : 0.f);
                 if (noise_std > 0.f) v = fmaf(noise_std, routing_noise(tok0 + ty + 8 * a, e, noise_seed), v);
                 lg[(ty + 8 * a) * E + e] = v;
+                if (logits && tok0 + ty + 8 * a < Tn) logits[(size_t)(tok0 + ty + 8 * a) * E + e] = v;
             }
         }
     __syncthreads();
@@ -154,12 +156,12 @@ __global__ void balance_loss_kernel(const int32_t* __restrict__ counts, int E, d
 }  // namespace
 
 cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                         int32_t* idx, float* w, int32_t* counts, float* balance_loss,
+                         int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
                          cudaStream_t s) {
     cudaError_t st = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
     if (st != cudaSuccess) return st;
     if (c.T > 0 && tc_route_supported(c)) {
-        st = launch_route_tc(c, x, Wg, bg, idx, w, counts, s);
+        st = launch_route_tc(c, x, Wg, bg, idx, w, counts, logits, s);
         if (st != cudaSuccess) return st;
     } else if (c.T > 0) {
         const size_t smem = sizeof(float) * ((size_t)kRouteTok * (kRouteKc + 1) +
@@ -172,13 +174,13 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             kern<<<grid, kRouteThreads, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
                                                    bias, c.T, c.d, c.E, c.k, inv_temp, c.noise_std, c.noise_seed,
-                                                   idx, w, counts);
+                                                   idx, w, counts, logits);
         } else {
             auto kern = route_kernel<float>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             kern<<<grid, kRouteThreads, smem, s>>>((const float*)x, (const float*)Wg, bias, c.T, c.d,
                                                    c.E, c.k, inv_temp, c.noise_std, c.noise_seed, idx, w,
-                                                   counts);
+                                                   counts, logits);
         }
         count_launch();
         st = cudaGetLastError();

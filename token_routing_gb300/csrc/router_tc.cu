@@ -34,6 +34,7 @@ struct RouteTcParams {
     int32_t* idx;
     float* w;
     int32_t* counts;
+    float* logits;   // [T, E] or null
     int* err;
 };
 
@@ -141,6 +142,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     if (e < p.E) {
                         float v = __uint_as_float(r[i]) + s_bias[e];
                         if (p.noise_std > 0.f) v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed), v);
+                        if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
                         // insert into the list sorted by (logit desc, id asc); experts arrive in
                         // ascending id, so an equal logit never displaces an earlier one
 #pragma unroll
@@ -197,7 +199,7 @@ cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtens
 bool tc_route_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && c.d % 64 == 0; }
 
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                            int32_t* idx, float* w, int32_t* counts, cudaStream_t s) {
+                            int32_t* idx, float* w, int32_t* counts, float* logits, cudaStream_t s) {
     RouteTcParams p{};
     p.T = c.T; p.d = c.d; p.E = c.E;
     p.E_pad = (c.E + 31) / 32 * 32;
@@ -205,7 +207,7 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.noise_std = c.noise_std;
     p.noise_seed = c.noise_seed;
     p.bg = c.has_gate_bias ? bg : nullptr;
-    p.idx = idx; p.w = w; p.counts = counts;
+    p.idx = idx; p.w = w; p.counts = counts; p.logits = logits;
     p.err = device_error_word();
     CUtensorMap tx, tw;
     if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, RBM)) return cudaErrorInvalidValue;

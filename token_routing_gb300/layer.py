@@ -69,10 +69,24 @@ def alloc_buffers(cfg, device="cuda", backward=True):
     return b
 
 
-def route(cfg, x, Wg, bg, b, stream=None):
+def route(cfg, x, Wg, bg, b, stream=None, logits=None):
+    """moe_route; `logits` (optional [T, E] fp32 tensor) receives the routing logits."""
     L.check("moe_route", L.load().moe_route(
         ctypes.byref(cfg), _p(x), _p(Wg), _p(bg), _p(b["idx"]), _p(b["w"]), _p(b["counts"]),
-        _p(b["balance_loss"]), _p(b["ws"]), _s(stream)))
+        _p(b["balance_loss"]), _p(logits), _p(b["ws"]), _s(stream)))
+
+
+def soft_balance(cfg, logits, weight, P, loss, ws, stream=None):
+    """Soft expert load P [E] and weight * mean_e (P_e - T/E)^2 into loss [1]."""
+    L.check("moe_soft_balance", L.load().moe_soft_balance(
+        ctypes.byref(cfg), _p(logits), ctypes.c_float(weight), _p(P), _p(loss), _p(ws), _s(stream)))
+
+
+def soft_balance_backward(cfg, logits, P, weight, x, Wg, dx, dWg, dbg, ws, stream=None):
+    """Adds the soft balance loss gradient into dx, dWg and (if given) dbg."""
+    L.check("moe_soft_balance_backward", L.load().moe_soft_balance_backward(
+        ctypes.byref(cfg), _p(logits), _p(P), ctypes.c_float(weight), _p(x), _p(Wg), _p(dx), _p(dWg),
+        _p(dbg), _p(ws), _s(stream)))
 
 
 def dispatch(cfg, idx, x, b, stream=None):
