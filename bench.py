@@ -103,6 +103,33 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+GEMM_SOURCES = ["token_routing_gb300/csrc/gemm_tc_pair.cu", "token_routing_gb300/csrc/gemm_tc.cu",
+                "token_routing_gb300/csrc/tc_gemm_common.cuh", "token_routing_gb300/csrc/tc_ptx.cuh",
+                "token_routing_gb300/csrc/common.cuh"]
+
+
+def gemm_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch of the forward GEMM pair from the committed ncu record, if it was
+    taken on this workload with the current GEMM sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as fh:
+            rec = json.load(fh)
+    except Exception:
+        return None
+    if rec.get("workload") != workload or rec.get("gemm_source_hash") != gemm_source_hash():
+        return None
+    return rec.get("ffn_pair_dram_bytes_per_launch")
+
+
 def algorithmic_counts(cfg, kept_rows):
     """Per-step algorithmic work: expert FLOPs and the permute / router / combine bytes
     (units: kept assignments N, tokens T)."""
@@ -177,6 +204,52 @@ def run_reference(args, cfg):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def time_extras(moe, c, cfg, d_in, b, flush, stream, steps):
+    """Device time (us) of the optional calls on the same workload, each captured as its
+    own CUDA graph: the co-selection matrix, routing with training noise, and the soft
+    balance loss forward and backward."""
+    import torch
+    dev = d_in["x"].device
+    cn = moe.config_from(cfg, noise_std=0.1, noise_seed=1)
+    H = torch.empty(cfg.E, cfg.E, dtype=torch.int32, device=dev)
+    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+    P = torch.empty(cfg.E, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    dx = torch.zeros_like(b["dx"])
+    dWg = torch.zeros_like(b["dWg"])
+    calls = {
+        "route_us": lambda st: moe.route(c, d_in["x"], d_in["Wg"], d_in["bg"], b, st),
+        "route_noisy_us": lambda st: moe.route(cn, d_in["x"], d_in["Wg"], d_in["bg"], b, st),
+        "route_with_logits_us": lambda st: moe.route(c, d_in["x"], d_in["Wg"], d_in["bg"], b, st, logits=logits),
+        "coselect_us": lambda st: moe.coselect(c, b["idx"], H, st),
+        "soft_balance_us": lambda st: moe.soft_balance(c, logits, 1e-3, P, loss, b["ws"], st),
+        "soft_balance_backward_us": lambda st: moe.soft_balance_backward(c, logits, P, 1e-3, d_in["x"], d_in["Wg"],
+                                                                         dx, dWg, None, b["ws"], st),
+    }
+    cap = torch.cuda.Stream(dev)
+    out = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g, stream=cap):
+            fn(cap)
+        tot = 0.0
+        for i in range(steps + 2):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 2:
+                tot += e0.elapsed_time(e1) * 1e3 / steps
+        out[name] = tot
+    moe.get_error(stream)
+    out["note"] = "per call, CUDA graph replay, L2 flushed before each; noise_std 0.1; soft-balance weight 1e-3"
+    return out
 
 
 def run_ours(args, cfg):
@@ -324,6 +397,8 @@ def run_ours(args, cfg):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e = float(t.item())
 
+    extras = time_extras(moe, c, cfg, d_in, b, flush, stream, args.steps) if not args.no_extras else None
+
     if rank == 0:
         peaks = _peaks()
         work = algorithmic_counts(cfg, kept)
@@ -348,7 +423,8 @@ def run_ours(args, cfg):
             "roofline": {"kernel": "tcgen05 grouped GEMM, forward pair (GEMM1+GELU, GEMM2)",
                          "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": gemm_tflops / peak_tc,
-                         "peak_source": f"{peaks['src']} bf16 sustained", "traffic": None},
+                         "peak_source": f"{peaks['src']} bf16 sustained",
+                         "traffic": measured_traffic(cfg.name)},
             "grouped_gemm_pct_bf16_peak": 100.0 * gemm_tflops / peak_tc,
             "permute_gbs": permute_gbs,
             "permute_frac_hbm": permute_gbs / peaks["hbm_gbs"],
@@ -359,6 +435,7 @@ def run_ours(args, cfg):
             "e2e": {"value": cfg.T * world / (e2e * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
                     "d2h_bytes_per_step": 4},
+            "extras": extras,
             "gpu_launches": int(launches),
             "wall_s_timed": t_wall,
             "clocks": clocks,
@@ -382,6 +459,7 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=8192, help="tokens in the oracle's timed batch")
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the optional calls")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     cfg = synth.get(args.workload)

@@ -163,13 +163,27 @@ soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, i
     if (c > d) return;
     const int per = (Tn + splits - 1) / splits;
     const int t0 = sp * per, t1 = min(Tn, t0 + per);
-    float acc = 0.f;
+    // four independent accumulators (tokens t0+4i+u), summed in a fixed order at the end, so
+    // that four row loads are in flight per thread
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int t = t0;
     if (c < d) {
-        for (int t = t0; t < t1; ++t) acc = fmaf(dz[(size_t)t * E + e], ld_f(x + (size_t)t * d + c), acc);
+        for (; t + 4 <= t1; t += 4) {
+            const float z0 = dz[(size_t)t * E + e], z1 = dz[(size_t)(t + 1) * E + e];
+            const float z2 = dz[(size_t)(t + 2) * E + e], z3 = dz[(size_t)(t + 3) * E + e];
+            const float x0 = ld_f(x + (size_t)t * d + c), x1 = ld_f(x + (size_t)(t + 1) * d + c);
+            const float x2 = ld_f(x + (size_t)(t + 2) * d + c), x3 = ld_f(x + (size_t)(t + 3) * d + c);
+            a0 = fmaf(z0, x0, a0); a1 = fmaf(z1, x1, a1); a2 = fmaf(z2, x2, a2); a3 = fmaf(z3, x3, a3);
+        }
+        for (; t < t1; ++t) a0 = fmaf(dz[(size_t)t * E + e], ld_f(x + (size_t)t * d + c), a0);
     } else {
-        for (int t = t0; t < t1; ++t) acc += dz[(size_t)t * E + e];
+        for (; t + 4 <= t1; t += 4) {
+            a0 += dz[(size_t)t * E + e]; a1 += dz[(size_t)(t + 1) * E + e];
+            a2 += dz[(size_t)(t + 2) * E + e]; a3 += dz[(size_t)(t + 3) * E + e];
+        }
+        for (; t < t1; ++t) a0 += dz[(size_t)t * E + e];
     }
-    part[((size_t)sp * E + e) * (d + 1) + c] = acc;
+    part[((size_t)sp * E + e) * (d + 1) + c] = (a0 + a1) + (a2 + a3);
 }
 
 // dWg[e, c] += sum over splits (in order); dbg[e] += the dz column sums.
@@ -191,9 +205,10 @@ int soft_chunks(const moe_config_t& c) { return std::max(1, ceil_div(c.T, kSoftT
 
 int soft_splits(const moe_config_t& c) {
     const int col_blocks = ceil_div(c.d + 1, kSoftThreads);
-    const int s = ceil_div(4LL * num_sms(), (long long)c.E * col_blocks);
+    // enough blocks for ~16 per SM; each split covers at least 64 tokens
+    const int s = ceil_div(16LL * num_sms(), (long long)c.E * col_blocks);
     const int cap = std::max(1, ceil_div(c.T, 64));
-    return std::max(1, std::min(std::min(s, 64), cap));
+    return std::max(1, std::min(std::min(s, 256), cap));
 }
 
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
