@@ -154,8 +154,10 @@ def oracle_step(cfg, npin):
 
 
 def oracle_sample_inputs(cfg, tokens):
+    """A batch of the workload holding as many expert rows (tokens x k) as a top-2 batch of
+    `tokens` tokens, so that the oracle's time stays bounded for large k (dense routing)."""
     import synth
-    sample = cfg.with_(T=min(tokens, cfg.T))
+    sample = cfg.with_(T=max(1, min(cfg.T, tokens * 2 // cfg.k)))
     inp = synth.make_inputs(sample)
     return sample, {k: (None if v is None else v.double().numpy()) for k, v in inp.items()}
 
@@ -456,8 +458,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=synth.HEADLINE)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=8192, help="tokens in the oracle's timed batch")
-    ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
+    ap.add_argument("--cpu-tokens", type=int, default=8192, help="tokens in the oracle's timed batch (scaled by 2/k)")
+    ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm; scaled by 2/k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional calls")
     args = ap.parse_args(argv)

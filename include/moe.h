@@ -6,6 +6,9 @@
  *   z   = x Wg^T (+ bg)                                   gate linear
  *   idx = top-k of z per token (ties -> lower expert id)  top-k selection
  *   w   = softmax(z[idx] / temperature) over the k        routing weights
+ *   k = E is dense soft routing (the naive soft MoE of the Expert-Parallelism page, section
+ *   2.2: every expert runs on every token): nothing is selected, slot j holds expert j and
+ *   w = softmax(z / temperature) over all E.
  *     "Native MoE training system PithTrain", section 4.1 (PithTrainMoELayer.forward:
  *     gate, torch.topk, softmax over the selected values); "Expert Parallelism: Scaling
  *     Mixture-of-Experts Models", section 2.2 (softmax(gate(x)/temperature); hybrid top-8
@@ -78,14 +81,15 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
 #define MOE_ROW_ALIGN 128   /* minimum bucket alignment (rows); cfg->row_align is 128 or 256 */
 #define MOE_MAX_EXPERTS 256
-#define MOE_MAX_K 8
+#define MOE_MAX_K 8           /* largest top-k selection; k = E (dense) is allowed for any E */
 
 typedef struct {
     /* set by the caller */
     int32_t T;                 /* tokens, >= 0 */
     int32_t d;                 /* model dim, >= 1 */
     int32_t E;                 /* experts, 1..MOE_MAX_EXPERTS */
-    int32_t k;                 /* experts per token, 1..min(E, MOE_MAX_K) */
+    int32_t k;                 /* experts per token: 1..min(E, MOE_MAX_K) (top-k), or E
+                                  (dense soft routing, slot j = expert j) */
     int32_t d_ff;              /* expert hidden dim, >= 1 */
     float capacity_factor;     /* <= 0: no capacity limit */
     float temperature;         /* > 0: softmax(z_sel / temperature) */
@@ -118,8 +122,9 @@ MOE_API size_t moe_workspace_bytes(const moe_config_t* cfg);
 
 /* Gate linear + top-k + softmax over the k + expert counts + balance loss.
  *   x [T,d] act, Wg [E,d] act, bg [E] fp32 (read iff cfg->has_gate_bias, else may be NULL)
- *   -> idx [T,k] int32 (slot j = j-th largest logit), w [T,k] fp32 (rows sum to 1),
- *      counts [E] int32 (pre-capacity choices, sum = T*k), balance_loss [1] fp32,
+ *   -> idx [T,k] int32 (slot j = j-th largest logit; with k = E, slot j = expert j),
+ *      w [T,k] fp32 (rows sum to 1), counts [E] int32 (pre-capacity choices, sum = T*k;
+ *      T each with k = E), balance_loss [1] fp32,
  *      logits [T,E] fp32 (nullable: the routing logits z = x Wg^T + bg + noise; needed by
  *      moe_soft_balance).
  * Logits are accumulated in fp32. All pointers are device pointers. */
@@ -135,7 +140,9 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const voi
  *      slot_row [T,k] int32 (row of assignment (t,j), -1 if dropped), n_dropped [1] int32,
  *      Xp [rows_capacity, d] act (rows >= offsets[E] unspecified).
  * Priority for capacity is token order. idx entries must lie in [0,E) and differ within a
- * token; a violation sets MOE_ERR_DEVICE_BOUNDS on the device. */
+ * token; a violation sets MOE_ERR_DEVICE_BOUNDS on the device. With k = E every bucket holds
+ * tokens 0..min(T,C)-1 in order and idx must be the identity (idx[t,j] = j; else
+ * MOE_ERR_DEVICE_BOUNDS); no sort runs. */
 MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const void* x,
                           int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
                           int32_t* n_dropped, void* Xp, void* ws, moe_stream_t stream);
@@ -148,7 +155,8 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, c
  * fixed array of MOE_NOALLOC_SCRATCH_BYTES in the library's device memory, reserved on
  * every GPU that loads the library until the process exits. The call allocates nothing.
  * Limits: T <= MOE_NOALLOC_MAX_TOKENS and T*k <= MOE_NOALLOC_MAX_ASSIGNMENTS; larger
- * configurations return MOE_ERR_UNSUPPORTED (use moe_dispatch with a workspace).
+ * configurations return MOE_ERR_UNSUPPORTED (use moe_dispatch with a workspace). With
+ * k = E (dense routing) no sort and no scratch are used and the limits do not apply.
  * The first call on a device looks up the array's device address (once per device); make
  * that first call before any stream capture. All calls share the one array: calls that
  * may overlap on the GPU (other streams, other host threads) race and must be serialised
@@ -222,7 +230,10 @@ MOE_API moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const fl
  *   H[i][j] = number of tokens whose top-k holds i in an earlier slot (higher logit) than j,
  * so H + H^T is the co-occurrence count, and H[i][i] = number of tokens that chose i.
  *   idx [T,k] int32 (as from moe_route) -> H [E,E] int32 (overwritten). Device pointers.
- * Entries out of [0,E) or repeated within a token set MOE_ERR_DEVICE_BOUNDS and are skipped. */
+ * Entries out of [0,E) or repeated within a token set MOE_ERR_DEVICE_BOUNDS and are skipped.
+ * With k = E > MOE_MAX_K (dense routing) idx must be the identity: H[i][j] = T for i <= j,
+ * 0 below the diagonal; a token whose row is not the identity sets MOE_ERR_DEVICE_BOUNDS and
+ * is not counted. */
 MOE_API moe_status_t moe_coselect(const moe_config_t* cfg, const int32_t* idx, int32_t* H,
                                   moe_stream_t stream);
 

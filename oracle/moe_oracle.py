@@ -24,6 +24,8 @@ Readings where the pages are silent or ambiguous (each is also listed in DESIGN.
 * weights: top-k on logits, then softmax(z_sel / temperature) over the k selected (PithTrain
   4.1; temperature 1 for plain top-k). Indices equal those of softmax-then-top-k.
 * ties in top-k go to the lower expert id; slot j holds the j-th largest logit.
+* k = E is dense soft routing (the naive soft MoE): every expert on every token, slot j
+  holds expert j, weights softmax(z / temperature) over all E.
 * capacity C = ceil(capacity_factor * T * k / E) (tokens read as routed assignments),
   evaluated in IEEE double from the fp32 value of capacity_factor.
 * drop priority: token order; assignment (t, j) -> e has rank = number of earlier tokens
@@ -68,6 +70,17 @@ def select_topk(z, k):
     order = np.argsort(-z, axis=1, kind="stable")  # stable: equal logits keep ascending id
     idx = order[:, :k].astype(np.int64)
     return idx, np.take_along_axis(z, idx, axis=1)
+
+
+def select_all(z):
+    """Dense soft routing, k = E (Expert-Parallelism page 2.2, the naive soft MoE that runs every
+    expert on every token): nothing is selected, so slot j holds expert j and z_sel = z. No
+    rounding can change the selection: the returned gap is +inf for every token.
+    Returns (idx [T,E] int64, z_sel [T,E], gap [T])."""
+    z = _f64(z)
+    T, E = z.shape
+    idx = np.broadcast_to(np.arange(E, dtype=np.int64), (T, E)).copy()
+    return idx, z.copy(), np.full(T, np.inf)
 
 
 def topk_gap(z, k):
@@ -147,10 +160,14 @@ def route(x, Wg, bg, k, temperature=1.0, noise_std=0.0, noise_seed=0):
     z = gate_logits(x, Wg, bg)
     if noise_std > 0:
         z = z + noise_std * routing_noise(z.shape[0], z.shape[1], noise_seed)
-    idx, z_sel = select_topk(z, k)
+    if k == z.shape[1]:
+        idx, z_sel, gap = select_all(z)
+    else:
+        idx, z_sel = select_topk(z, k)
+        gap = topk_gap(z, k)
     w = routing_weights(z_sel, temperature)
     counts = expert_counts(idx, z.shape[1])
-    return dict(z=z, idx=idx, z_sel=z_sel, w=w, gap=topk_gap(z, k), counts=counts,
+    return dict(z=z, idx=idx, z_sel=z_sel, w=w, gap=gap, counts=counts,
                 balance_loss=balance_loss(counts))
 
 

@@ -11,7 +11,8 @@ top-k, capacity_factor, temperature; expert FFN Linear(d, d_ff) -> GELU -> Linea
   (balance_loss), section 4.3 (aux_loss_weight = 0.01).
 * "Expert Parallelism" page, section 2.1 (skewed expert load, top expert ~40% of
   tokens), section 2.2 (temperature 0.2; hybrid top-8 pre-selection then soft
-  weighting), section 3.2 (expert co-selection).
+  weighting; the naive soft MoE runs every expert on every token), section 3.2 (expert
+  co-selection).
 
 The small cases are scaled-down versions of the same recipes: they span several
 128-row tiles, have ragged tails and finish in the oracle within seconds.
@@ -26,10 +27,10 @@ class LayerConfig:
     T: int                      # tokens in the batch
     d: int                      # model dim
     E: int                      # number of experts
-    k: int                      # experts selected per token
+    k: int                      # experts selected per token (k = E: dense soft routing)
     d_ff: int                   # expert hidden dim
     capacity_factor: Optional[float] = None   # None: no capacity limit
-    temperature: float = 1.0    # softmax temperature over the k selected logits
+    temperature: float = 1.0    # softmax temperature over the k selected logits (all E if k = E)
     dtype: str = "bf16"         # storage dtype of activations and weights: "bf16" or "f32"
     backward: bool = True       # whether the workload includes the backward pass
     x_dist: str = "normal"      # "normal": x ~ N(0,1); "clusters": centre ~ N(0,1) + N(0, noise^2)
@@ -73,6 +74,11 @@ WORKLOADS = {
     "top2-e256-clusters-cap1.0": LayerConfig(
         name="top2-e256-clusters-cap1.0", T=32768, d=1024, E=256, k=2, d_ff=2048,
         capacity_factor=1.0, x_dist="clusters", n_clusters=64, cluster_noise=0.1),
+    # naive dense soft MoE: the hybrid layer's shapes with every one of the 128 experts run
+    # on every token, softmax(z/0.2) over all 128 (k = E)
+    "dense-soft-e128-temp0.2": LayerConfig(
+        name="dense-soft-e128-temp0.2", T=16384, d=1024, E=128, k=128, d_ff=4096,
+        capacity_factor=None, temperature=0.2),
 }
 
 # The throughput workload timed by the benchmark.
@@ -102,6 +108,23 @@ SMALL_CASES = {
     "small-max-e256-k8": LayerConfig(
         name="small-max-e256-k8", T=513, d=128, E=256, k=8, d_ff=128, capacity_factor=None,
         temperature=0.5),
+    # fp32 with row lengths that are no multiple of a 16-byte vector
+    "small-fp32-ragged": LayerConfig(
+        name="small-fp32-ragged", T=123, d=37, E=5, k=3, d_ff=45, capacity_factor=1.5,
+        dtype="f32"),
+    # dense soft routing (k = E): every expert on every token
+    "small-dense-e8": LayerConfig(
+        name="small-dense-e8", T=300, d=128, E=8, k=8, d_ff=192, capacity_factor=None,
+        temperature=0.2),
+    "small-dense-e12-cap0.5": LayerConfig(
+        name="small-dense-e12-cap0.5", T=700, d=128, E=12, k=12, d_ff=128, capacity_factor=0.5,
+        gate_bias="zipf", zipf_s=1.2, zipf_c=ZIPF_C_E64),
+    "small-dense-e16-pairs": LayerConfig(
+        name="small-dense-e16-pairs", T=1100, d=128, E=16, k=16, d_ff=128, capacity_factor=None,
+        temperature=0.5),
+    "small-dense-fp32": LayerConfig(
+        name="small-dense-fp32", T=100, d=40, E=10, k=10, d_ff=24, capacity_factor=None,
+        temperature=0.7, dtype="f32"),
 }
 
 

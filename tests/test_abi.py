@@ -70,6 +70,20 @@ def test_rows_capacity_bounds_every_bucket_layout(moe_lib):
             assert C == 2 ** 31 - 1
 
 
+@pytest.mark.parametrize("T,E,cf", [(16384, 128, 0.0), (700, 12, 0.5), (5, 256, 0.0), (0, 16, 0.0),
+                                    (1100, 16, 0.0), (300, 8, 0.0)])
+def test_dense_routing_config(moe_lib, T, E, cf):
+    """k = E (dense soft routing) is accepted for any E; its bucket layout is closed-form:
+    E buckets of min(T, C) rows each, padded to row_align, all within rows_capacity."""
+    c = _cfg(moe_lib, T=T, k=E, E=E, capacity_factor=cf)
+    assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
+    kept = min(T, c.capacity)
+    B = -(-kept // c.row_align) * c.row_align
+    assert E * B <= c.rows_capacity
+    assert c.row_align == (256 if kept >= 1024 else 128)
+    assert moe_lib.load().moe_workspace_bytes(ctypes.byref(c)) > 0
+
+
 def test_unlimited_capacity_and_empty_batch(moe_lib):
     c = _cfg(moe_lib, T=0, capacity_factor=0.0)
     assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0

@@ -37,6 +37,26 @@ def test_noisy_route_matches_oracle(name, seed, moe_lib, cuda_device):
     assert (plain["idx"] != r["idx"]).any(axis=1).mean() > 0.01
 
 
+@pytest.mark.parametrize("name,seed", [("small-dense-e8", 12), ("small-dense-e12-cap0.5", 13)])
+def test_noisy_dense_route_matches_oracle(name, seed, moe_lib, cuda_device):
+    """Dense routing selects every expert, so the noise moves only the weights."""
+    moe = moe_lib
+    cfg = synth.get(name)
+    inp = synth.make_inputs(cfg, with_dy=False)
+    npin = P.np_inputs(inp)
+    r = P.O.route(npin["x"], npin["Wg"], npin["bg"], cfg.k, cfg.temperature, noise_std=NOISE, noise_seed=seed)
+    c = moe.config_from(cfg, noise_std=NOISE, noise_seed=seed)
+    dev = P.to_dev(inp)
+    b = moe.alloc_buffers(c, backward=False)
+    moe.route(c, dev["x"], dev["Wg"], dev["bg"], b)
+    moe.get_error()
+    assert (b["idx"].cpu().numpy() == r["idx"]).all()
+    w = b["w"].cpu().double().numpy()
+    P.assert_close("w", w, r["w"], 1e-4)
+    plain = P.O.route(npin["x"], npin["Wg"], npin["bg"], cfg.k, cfg.temperature)
+    assert np.abs(plain["w"] - r["w"]).max() > 1e-2
+
+
 def test_noisy_step_end_to_end(moe_lib, cuda_device):
     moe = moe_lib
     cfg = synth.get("small-top2-cap1.0")

@@ -170,7 +170,7 @@ def test_end_to_end(name, cases, moe_lib, cuda_device):
             P.assert_close(key, P.f64(b[key]), bwd[key], t)
 
 
-@pytest.mark.parametrize("name", ["small-top2-cap1.0", "small-hybrid-top8"])
+@pytest.mark.parametrize("name", ["small-top2-cap1.0", "small-hybrid-top8", "small-dense-e12-cap0.5"])
 def test_graph_replay_is_bit_identical_to_eager(name, cases, moe_lib, cuda_device):
     """The step captured in a CUDA graph gives the eager step's outputs bit for bit (every
     reduction runs in a fixed order), and so do repeated replays."""

@@ -14,7 +14,8 @@ WEIGHT = 1e-3
 
 
 @pytest.mark.parametrize("name", ["small-top2-cap1.0", "small-zipf-cap1.25", "small-max-e256-k8",
-                                  "small-fp32-bwd", "top2-e16-cap1.0"])
+                                  "small-fp32-bwd", "small-fp32-ragged", "small-dense-e12-cap0.5",
+                                  "top2-e16-cap1.0", "top2-e256-clusters-cap1.0"])
 def test_soft_balance_matches_oracle(name, moe_lib, cuda_device):
     moe = moe_lib
     cfg = synth.get(name)

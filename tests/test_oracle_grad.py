@@ -31,6 +31,8 @@ CASES = [  # T, d, E, f, k, temperature, capacity
     (7, 4, 5, 3, 2, 1.0, 2),
     (6, 3, 6, 4, 3, 0.4, None),
     (8, 3, 4, 2, 1, 1.0, 1),
+    (6, 3, 4, 3, 4, 0.5, None),   # dense soft routing (k = E): the full softmax Jacobian
+    (7, 3, 3, 2, 3, 1.0, 4),      # dense with capacity: tokens 4.. dropped by every expert
 ]
 
 

@@ -281,6 +281,63 @@ def test_hybrid_k_equals_E_is_dense_soft_moe():
         np.testing.assert_allclose(out["y"], O.dense_soft_moe(inp, temp)["y"], atol=1e-12)
 
 
+def test_golden_dense_soft_routing():
+    g = _load("dense_soft_routing_hand.json")
+    for case in g["cases"]:
+        z = np.array(case["logits"])
+        E = z.shape[1]
+        r = O.route(z, np.eye(E), None, E, case["temperature"])
+        assert r["idx"].tolist() == case["idx"]
+        np.testing.assert_allclose(r["w"], case["w"], rtol=1e-14, atol=1e-16)
+        assert r["counts"].tolist() == [z.shape[0]] * E
+        assert r["balance_loss"] == 0.0
+
+
+def test_dense_weights_are_the_full_topk_weights_reordered():
+    """k = E keeps slot j = expert j; the weight of each expert equals the one the sorted
+    top-E selection gives it."""
+    rng = np.random.default_rng(71)
+    z = rng.standard_normal((50, 7))
+    dense = O.route(z, np.eye(7), None, 7, 0.3)
+    idx, zsel = O.select_topk(z, 7)
+    wt = O.routing_weights(zsel, 0.3)
+    back = np.zeros_like(wt)
+    np.put_along_axis(back, idx, wt, axis=1)
+    np.testing.assert_allclose(dense["w"], back, rtol=0, atol=1e-15)
+    assert np.isinf(dense["gap"]).all()
+
+
+@pytest.mark.parametrize("C,align", [(None, 1), (None, 8), (9, 4), (0, 4), (40, 8)])
+def test_dense_dispatch_closed_form(C, align):
+    """Every expert receives every token in token order: kept = min(T, C), bucket e starts at
+    e * ceil(kept / align) * align, and slot (t, j) sits at row start_j + t when t < kept."""
+    T, E = 23, 5
+    idx = np.broadcast_to(np.arange(E), (T, E))
+    out = O.dispatch(idx, E, C, align)
+    kept = T if C is None else min(T, C)
+    B = -(-kept // align) * align
+    assert out["kept"].tolist() == [kept] * E
+    assert out["offsets"].tolist() == [e * B for e in range(E + 1)]
+    assert out["n_dropped"] == E * (T - kept)
+    for t in range(T):
+        for j in range(E):
+            assert out["slot_row"][t, j] == (j * B + t if t < kept else -1)
+    rt = out["row_token"]
+    for e in range(E):
+        assert rt[e * B:e * B + kept].tolist() == list(range(kept))
+        assert (rt[e * B + kept:(e + 1) * B] == -1).all()
+
+
+def test_dense_with_capacity_keeps_the_first_tokens():
+    """With capacity C < T every expert keeps tokens 0..C-1: those tokens get the naive soft
+    MoE output, the rest get 0."""
+    inp = _rand_inputs(12, 4, 3, 5, seed=33, bias=True)
+    out = O.forward(inp, 3, 0.5, C=5, align=4)
+    ref = O.dense_soft_moe(inp, 0.5)["y"]
+    np.testing.assert_allclose(out["y"][:5], ref[:5], atol=1e-12)
+    assert (out["y"][5:] == 0).all()
+
+
 def test_temperature_to_zero_approaches_hard_top1():
     inp = _rand_inputs(60, 8, 8, 6, seed=41)
     k = 4

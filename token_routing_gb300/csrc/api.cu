@@ -53,7 +53,7 @@ int64_t derived_rows(const moe_config_t& c, int64_t cap) {
 moe_status_t check_fields(const moe_config_t* c) {
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->T < 0 || c->d < 1 || c->E < 1 || c->E > MOE_MAX_EXPERTS || c->k < 1 ||
-        c->k > MOE_MAX_K || c->k > c->E || c->d_ff < 1)
+        (c->k > MOE_MAX_K && c->k != c->E) || c->k > c->E || c->d_ff < 1)
         return MOE_ERR_INVALID_ARG;
     if (!(c->temperature > 0.0f) || !std::isfinite(c->temperature)) return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_loss_weight)) return MOE_ERR_INVALID_ARG;
@@ -246,10 +246,14 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const voi
     if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    Workspace w{static_cast<char*>(ws), 0};
-    SortScratch srt;
-    sort_scratch_take(w, *cfg, &srt);
-    MOE_TRY(launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s));
+    if (dense_routing(*cfg)) {
+        MOE_TRY(launch_dense_layout(*cfg, idx, kept, offsets, row_token, slot_row, n_dropped, s));
+    } else {
+        Workspace w{static_cast<char*>(ws), 0};
+        SortScratch srt;
+        sort_scratch_take(w, *cfg, &srt);
+        MOE_TRY(launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s));
+    }
     MOE_TRY(launch_gather(*cfg, x, offsets, row_token, Xp, s));
     return MOE_OK;
 }
@@ -340,10 +344,16 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;
     gx.sBe = (long long)c.d_ff * c.d; gx.sBn = 1; gx.sBk = c.d;
     MOE_TRY(row_gemm(c, gx, s));
-    // router backward: assignment sort, softmax Jacobian, dx, dWg, dbg
-    MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
-    MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
-    MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, c.has_gate_bias ? dbg : nullptr, s));
+    // router backward: softmax Jacobian, dx, then dWg and dbg (sparse dz: from an assignment
+    // sort by expert; dense routing: dz is [T, E] and dWg = dz^T x directly)
+    if (dense_routing(c)) {
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
+        MOE_TRY(launch_dense_dwg(c, b.dz, x, dWg, c.has_gate_bias ? dbg : nullptr, false, b.soft, s));
+    } else {
+        MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
+        MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, c.has_gate_bias ? dbg : nullptr, s));
+    }
     if (loss) MOE_TRY(launch_loss(c, b.lossblk, balance_loss, loss, s));
     // join
     MOE_TRY(cudaEventRecord(ev.c, side));

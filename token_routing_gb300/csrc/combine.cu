@@ -15,7 +15,8 @@ namespace moe {
 
 namespace {
 
-// y[t] = sum over kept slots of w[t,j] * Yp[slot_row[t,j]]; one warp per token.
+// y[t] = sum over kept slots of w[t,j] * Yp[slot_row[t,j]]; one warp per token. Slots are
+// taken in groups of MOE_MAX_K (one group unless k = E > MOE_MAX_K), in slot order.
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
@@ -23,51 +24,72 @@ combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
+    constexpr int G = MOE_MAX_K;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
-        int rows[MOE_MAX_K];
-        float ws[MOE_MAX_K];
+        int rows[G];
+        float ws[G];
+        // the first group stays in registers across the column loop
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) {
+        for (int j = 0; j < G; ++j) {
             rows[j] = (j < k) ? slot_row[(size_t)t * k + j] : -1;
             ws[j] = (j < k) ? w[(size_t)t * k + j] : 0.f;
         }
         if ((d % V) == 0) {
-            // two column groups per pass, every row load issued before any arithmetic
+            // two column groups per pass, every row load of a slot group issued before any arithmetic
 #pragma unroll 1
             for (int c = lane * V; c < d; c += 64 * V) {
                 const int c2 = c + 32 * V;
                 const bool two = c2 < d;
-                uint4 raw[2][MOE_MAX_K];
+                float acc[2][V];
 #pragma unroll
-                for (int j = 0; j < MOE_MAX_K; ++j) {
-                    if (j < k && rows[j] >= 0) {
-                        raw[0][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rows[j] * d + c));
-                        if (two) raw[1][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rows[j] * d + c2));
-                    }
-                }
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !two) break;
-                    float acc[V];
+                    for (int i = 0; i < V; ++i) acc[h][i] = 0.f;
+#pragma unroll 1
+                for (int j0 = 0; j0 < k; j0 += G) {
+                    int rg[G];
+                    float wg[G];
 #pragma unroll
-                    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-#pragma unroll
-                    for (int j = 0; j < MOE_MAX_K; ++j) {
-                        if (j < k && rows[j] >= 0) {
-                            float v[V];
-                            unpack16<T>(raw[h][j], v);
-#pragma unroll
-                            for (int i = 0; i < V; ++i) acc[i] = fmaf(ws[j], v[i], acc[i]);
+                    for (int j = 0; j < G; ++j) {
+                        if (j0 == 0) { rg[j] = rows[j]; wg[j] = ws[j]; }
+                        else {
+                            rg[j] = (j0 + j < k) ? slot_row[(size_t)t * k + j0 + j] : -1;
+                            wg[j] = (j0 + j < k) ? w[(size_t)t * k + j0 + j] : 0.f;
                         }
                     }
-                    store16(y + (size_t)t * d + (h ? c2 : c), acc);
+                    uint4 raw[2][G];
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        if (rg[j] >= 0) {
+                            raw[0][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rg[j] * d + c));
+                            if (two) raw[1][j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rg[j] * d + c2));
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two) break;
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            if (rg[j] >= 0) {
+                                float v[V];
+                                unpack16<T>(raw[h][j], v);
+#pragma unroll
+                                for (int i = 0; i < V; ++i) acc[h][i] = fmaf(wg[j], v[i], acc[h][i]);
+                            }
+                        }
+                    }
                 }
+                store16(y + (size_t)t * d + c, acc[0]);
+                if (two) store16(y + (size_t)t * d + c2, acc[1]);
             }
         } else {
             for (int c = lane; c < d; c += 32) {
                 float acc = 0.f;
-                for (int j = 0; j < k; ++j)
-                    if (rows[j] >= 0) acc = fmaf(ws[j], ld_f(Yp + (size_t)rows[j] * d + c), acc);
+                for (int j = 0; j < k; ++j) {
+                    const int r = j < G ? rows[j] : slot_row[(size_t)t * k + j];
+                    const float wj = j < G ? ws[j] : w[(size_t)t * k + j];
+                    if (r >= 0) acc = fmaf(wj, ld_f(Yp + (size_t)r * d + c), acc);
+                }
                 st_f(y + (size_t)t * d + c, acc);
             }
         }
@@ -82,7 +104,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
                    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
-                   const int32_t* __restrict__ slot_row, int d, int k, int rows_cap,
+                   const int32_t* __restrict__ slot_row, int d, int k, int rows_cap, bool dense,
                    T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossblk) {
     __shared__ float s_warp[8];
     const int lane = threadIdx.x & 31;
@@ -105,8 +127,12 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
             continue;
         }
         int jj = 0;
-        for (int j = 0; j < k; ++j)
-            if (slot_row[(size_t)t * k + j] == r) jj = j;
+        if (dense) {
+            jj = r / offsets[1];   // dense routing: slot j = expert j, equal-size buckets
+        } else {
+            for (int j = 0; j < k; ++j)
+                if (slot_row[(size_t)t * k + j] == r) jj = j;
+        }
         const float wv = w[(size_t)t * k + jj];
         float dot = 0.f;
         if ((d % V) == 0) {
@@ -203,6 +229,91 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                 st_f(dx + (size_t)t * d + c, acc);
             }
         }
+    }
+}
+
+// Router backward + un-permute for k > MOE_MAX_K (dense routing, k = E): one warp per token,
+// the token's k slots staged in shared memory (s and the dz values lane-parallel), then per
+// column group the same order as router_bwd_kernel: for each slot j, add dXp[row_j], then
+// dz_j Wg[e_j]. Four slots' loads are issued before their arithmetic.
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw,
+                       const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
+                       const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
+                       int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+    __shared__ float s_dz[8][MOE_MAX_EXPERTS];
+    __shared__ int s_row[8][MOE_MAX_EXPERTS];
+    __shared__ int s_ex[8][MOE_MAX_EXPERTS];
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    constexpr int V = Vec16<T>::N;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
+        const size_t base = (size_t)t * k;
+        float s = 0.f;
+        for (int j = lane; j < k; j += 32) s = fmaf(w[base + j], dw[base + j], s);
+        s = warp_sum(s);
+        for (int j = lane; j < k; j += 32) {
+            const float v = w[base + j] * (dw[base + j] - s) * inv_temp;
+            s_dz[wid][j] = v;
+            dz[base + j] = v;
+            s_row[wid][j] = slot_row[base + j];
+            s_ex[wid][j] = min(max(idx[base + j], 0), E - 1);
+        }
+        __syncwarp();
+        const float* zj = s_dz[wid];
+        const int* rj = s_row[wid];
+        const int* ej = s_ex[wid];
+        if ((d % V) == 0) {
+            for (int c = lane * V; c < d; c += 32 * V) {
+                float acc[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] = 0.f;
+                int j = 0;
+                for (; j + 4 <= k; j += 4) {
+                    float xr[4][V], wr[4][V];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (rj[j + u] >= 0) load16(dXp + (size_t)rj[j + u] * d + c, xr[u]);
+                        else {
+#pragma unroll
+                            for (int i = 0; i < V; ++i) xr[u][i] = 0.f;
+                        }
+                        load16(Wg + (size_t)ej[j + u] * d + c, wr[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                        for (int i = 0; i < V; ++i) {
+                            if (rj[j + u] >= 0) acc[i] += xr[u][i];
+                            acc[i] = fmaf(zj[j + u], wr[u][i], acc[i]);
+                        }
+                    }
+                }
+                for (; j < k; ++j) {
+                    float v[V];
+                    if (rj[j] >= 0) {
+                        load16(dXp + (size_t)rj[j] * d + c, v);
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[i] += v[i];
+                    }
+                    load16(Wg + (size_t)ej[j] * d + c, v);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = fmaf(zj[j], v[i], acc[i]);
+                }
+                store16(dx + (size_t)t * d + c, acc);
+            }
+        } else {
+            for (int c = lane; c < d; c += 32) {
+                float acc = 0.f;
+                for (int j = 0; j < k; ++j) {
+                    if (rj[j] >= 0) acc += ld_f(dXp + (size_t)rj[j] * d + c);
+                    acc = fmaf(zj[j], ld_f(Wg + (size_t)ej[j] * d + c), acc);
+                }
+                st_f(dx + (size_t)t * d + c, acc);
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -312,11 +423,11 @@ colsum_quarter_kernel(const T* __restrict__ M, int width, const int32_t* __restr
                       float* __restrict__ part) {
     constexpr int V = Vec16<T>::N;
     constexpr int QROWS = MOE_ROW_ALIGN / kColsumParts;
-    const int pq = blockIdx.y;  // tile * 4 + quarter
+    const int pq = blockIdx.x;  // tile * 4 + quarter (x: up to 2^31 - 1 quarters)
     const int r0 = pq * QROWS;
     if (r0 >= offsets[E]) return;
     if (width % V == 0) {
-        const int c = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+        const int c = (blockIdx.y * blockDim.x + threadIdx.x) * V;
         if (c >= width) return;
         float acc[V];
 #pragma unroll
@@ -331,8 +442,8 @@ colsum_quarter_kernel(const T* __restrict__ M, int width, const int32_t* __restr
 #pragma unroll
         for (int q = 0; q < V; ++q) part[(size_t)pq * width + c + q] = acc[q];
     } else {
-        const int cend = min(width, (int)((blockIdx.x + 1) * blockDim.x * V));
-        for (int c = blockIdx.x * blockDim.x * V + threadIdx.x; c < cend; c += blockDim.x) {
+        const int cend = min(width, (int)((blockIdx.y + 1) * blockDim.x * V));
+        for (int c = blockIdx.y * blockDim.x * V + threadIdx.x; c < cend; c += blockDim.x) {
             float acc = 0.f;
             for (int r = 0; r < QROWS; ++r) acc += ld_f(M + (size_t)(r0 + r) * width + c);
             part[(size_t)pq * width + c] = acc;
@@ -404,11 +515,12 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
     if (c.dtype == MOE_BF16)
         combine_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             (const __nv_bfloat16*)dy, (const __nv_bfloat16*)Yp, w, offsets, c.E, row_token, slot_row,
-            c.d, c.k, c.rows_capacity, (__nv_bfloat16*)dYp, dw, lossblk);
+            c.d, c.k, c.rows_capacity, dense_routing(c), (__nv_bfloat16*)dYp, dw, lossblk);
     else
         combine_bwd_kernel<float><<<grid, 256, 0, s>>>((const float*)dy, (const float*)Yp, w, offsets,
                                                        c.E, row_token, slot_row, c.d, c.k,
-                                                       c.rows_capacity, (float*)dYp, dw, lossblk);
+                                                       c.rows_capacity, dense_routing(c), (float*)dYp, dw,
+                                                       lossblk);
     count_launch();
     return cudaGetLastError();
 }
@@ -419,7 +531,16 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
     if (c.T == 0) return cudaSuccess;
     const int grid = warp_grid(c.T);
     const float inv_temp = 1.0f / c.temperature;
-    if (c.dtype == MOE_BF16)
+    if (c.k > MOE_MAX_K) {
+        if (c.dtype == MOE_BF16)
+            router_bwd_wide_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+                w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
+                c.E, inv_temp, dz, (__nv_bfloat16*)dx);
+        else
+            router_bwd_wide_kernel<float><<<grid, 256, 0, s>>>(w, dw, idx, slot_row, (const float*)Wg,
+                                                               (const float*)dXp, c.T, c.d, c.k, c.E,
+                                                               inv_temp, dz, (float*)dx);
+    } else if (c.dtype == MOE_BF16)
         router_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
             c.E, inv_temp, dz, (__nv_bfloat16*)dx);
@@ -466,7 +587,7 @@ cudaError_t launch_colsum(const moe_config_t& c, const void* M, int width, const
     if (quarters == 0) return cudaSuccess;
     const int V = c.dtype == MOE_BF16 ? 8 : 4;
     const int threads = std::max(32, std::min(256, (ceil_div(width, V) + 31) / 32 * 32));
-    dim3 g(ceil_div(width, threads * V), quarters);
+    dim3 g(quarters, ceil_div(width, threads * V));
     if (c.dtype == MOE_BF16)
         colsum_quarter_kernel<__nv_bfloat16><<<g, threads, 0, s>>>((const __nv_bfloat16*)M, width, offsets, c.E, part);
     else

@@ -48,12 +48,49 @@ coselect_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* _
     }
 }
 
+// Dense routing (k = E, slot j = expert j): every valid token adds 1 to H[i][j] for all
+// i <= j. Counts the tokens whose idx row is the identity (others set MOE_ERR_DEVICE_BOUNDS)
+// into H[0][0]; coselect_dense_fill_kernel then copies the count to every cell i <= j.
+__global__ void __launch_bounds__(kCoselThreads)
+coselect_dense_count_kernel(const int32_t* __restrict__ idx, int T, int E, int32_t* __restrict__ H, int* err) {
+    __shared__ int s_n;
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    int n = 0;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+        bool ok = true;
+        for (int j = 0; j < E; ++j) ok = ok && idx[(size_t)t * E + j] == j;
+        if (ok) ++n;
+        else raise_error(err, kErrBounds);
+    }
+    if (n) atomicAdd(&s_n, n);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_n) atomicAdd(H, s_n);
+}
+
+__global__ void __launch_bounds__(kCoselThreads)
+coselect_dense_fill_kernel(int E, int32_t* __restrict__ H) {
+    const int32_t n = H[0];
+    __syncthreads();
+    for (int c = threadIdx.x; c < E * E; c += blockDim.x) {
+        const int i = c / E, j = c % E;
+        if (i <= j) H[c] = n;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_coselect(const moe_config_t& c, const int32_t* idx, int32_t* H, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(H, 0, sizeof(int32_t) * (size_t)c.E * c.E, s);
     if (e != cudaSuccess || c.T == 0) return e;
     const int grid = std::max(1, std::min(ceil_div(c.T, kCoselThreads), 2 * num_sms()));
+    if (dense_routing(c) && c.k > MOE_MAX_K) {
+        coselect_dense_count_kernel<<<grid, kCoselThreads, 0, s>>>(idx, c.T, c.E, H, device_error_word());
+        count_launch();
+        coselect_dense_fill_kernel<<<1, kCoselThreads, 0, s>>>(c.E, H);
+        count_launch();
+        return cudaGetLastError();
+    }
     if (c.E <= kCoselSmemE)
         coselect_kernel<true><<<grid, kCoselThreads, 0, s>>>(idx, c.T, c.k, c.E, H, device_error_word());
     else

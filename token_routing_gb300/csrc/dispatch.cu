@@ -226,6 +226,40 @@ sort_kernel(SortArgs a) {
     }
 }
 
+// Dense soft routing (k = E): every expert receives every token, so the sort has a closed
+// form. kept = min(T, C); bucket e starts at e * B with B = kept rounded up to the alignment;
+// slot (t, j) sits at row j * B + t when t < kept, else it is dropped. One thread per
+// (token, slot) for slot_row (checking idx[t, j] = j) and per bucket row for row_token.
+__global__ void __launch_bounds__(256)
+dense_layout_kernel(const int32_t* __restrict__ idx, int T, int E, int C, int align, int32_t* __restrict__ kept,
+                    int32_t* __restrict__ offsets, int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row,
+                    int32_t* __restrict__ n_dropped, int* err) {
+    const int kp = min(T, C);
+    const long long B = ((long long)kp + align - 1) / align * align;
+    const long long n_slot = (long long)T * E;
+    const long long n_rows = B * E;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_slot + n_rows; i += stride) {
+        if (i < n_slot) {
+            const int t = (int)(i / E), j = (int)(i % E);
+            const bool ok = idx[i] == j;
+            if (!ok) raise_error(err, kErrBounds);
+            slot_row[i] = (ok && t < kp) ? (int32_t)(j * B + t) : -1;
+        } else {
+            const long long r = i - n_slot;
+            const int rr = (int)(r % B);
+            row_token[r] = rr < kp ? rr : -1;
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            offsets[e] = (int32_t)(e * B);
+            if (e < E) kept[e] = kp;
+        }
+        if (threadIdx.x == 0) *n_dropped = (T - kp) * E;
+    }
+}
+
 // Xp[r] = x[row_token[r]] for r < offsets[E]; padding rows (row_token = -1) are zeroed.
 // One warp per row, 16-byte vectors when the row length allows.
 template <typename T>
@@ -310,6 +344,16 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     e = cudaLaunchKernelEx(&cfg, sort_kernel, a);
     count_launch();
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32_t* kept, int32_t* offsets,
+                                int32_t* row_token, int32_t* slot_row, int32_t* n_dropped, cudaStream_t st) {
+    const long long items = (long long)c.T * c.E + (long long)c.rows_capacity;
+    const int grid = (int)std::max(1LL, std::min((items + 255) / 256, (long long)num_sms() * 8));
+    dense_layout_kernel<<<grid, 256, 0, st>>>(idx, c.T, c.E, c.capacity, c.row_align, kept, offsets, row_token,
+                                              slot_row, n_dropped, device_error_word());
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -55,6 +55,14 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
     if (!kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dense_routing(*cfg)) {
+        // closed-form layout: no scratch, no size limit
+        if (launch_dense_layout(*cfg, idx, kept, offsets, row_token, slot_row, n_dropped, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (launch_gather(*cfg, x, offsets, row_token, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     if (cfg->T > MOE_NOALLOC_MAX_TOKENS || (int64_t)cfg->T * cfg->k > MOE_NOALLOC_MAX_ASSIGNMENTS)
         return MOE_ERR_UNSUPPORTED;
     Workspace probe{nullptr, 0};
@@ -68,7 +76,6 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
     // previous call's leftovers need no clearing.
     Workspace ws{static_cast<char*>(base), 0};
     sort_scratch_take(ws, *cfg, &srt);
-    cudaStream_t s = (cudaStream_t)stream;
     if (launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_gather(*cfg, x, offsets, row_token, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;

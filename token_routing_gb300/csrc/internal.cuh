@@ -5,6 +5,10 @@
 
 namespace moe {
 
+// k = E: dense soft routing (every expert on every token, slot j = expert j). The bucket
+// layout is then closed-form and no sort runs.
+inline bool dense_routing(const moe_config_t& c) { return c.k == c.E; }
+
 // Epilogues of the grouped GEMMs over expert buckets (rows of one 128-row tile always belong
 // to a single expert because buckets are padded to cfg.row_align rows, a multiple of 128).
 enum GemmKind : int {
@@ -63,6 +67,8 @@ void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s);
 cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScratch& s,
                         int32_t* kept, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
                         int32_t* n_dropped, cudaStream_t st);
+cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32_t* kept, int32_t* offsets,
+                                int32_t* row_token, int32_t* slot_row, int32_t* n_dropped, cudaStream_t st);
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* offsets,
                           const int32_t* row_token, void* Xp, cudaStream_t st);
 
@@ -91,6 +97,10 @@ int soft_splits(const moe_config_t& c);
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s);
 cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, float weight, float* P,
                                 float* loss, const SoftScratch& s, cudaStream_t st);
+// dWg (+)= dz^T x and dbg (+)= column sums of dz for a dense dz [T, E] (split-K partials in
+// s.dwg_part, fixed-order reductions); accumulate = false overwrites dWg and dbg.
+cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void* x, float* dWg, float* dbg,
+                             bool accumulate, const SoftScratch& s, cudaStream_t st);
 cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, const float* P, float weight,
                                     const void* x, const void* Wg, void* dx, float* dWg, float* dbg,
                                     const SoftScratch& s, cudaStream_t st);

@@ -92,6 +92,28 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
         }
     __syncthreads();
 
+    if (k == E) {
+        // dense soft routing: w[t, e] = softmax(z_t / temp)_e over all E, slot e = expert e
+        for (int a = 0; a < 4; ++a) {
+            const int t = ty + 8 * a;
+            const int tok = tok0 + t;
+            if (tok >= Tn) break;
+            float m = -INFINITY;
+            for (int e = tx; e < E; e += 32) m = fmaxf(m, lg[t * E + e]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float s = 0.f;
+            for (int e = tx; e < E; e += 32) s += expf((lg[t * E + e] - m) * inv_temp);
+            s = warp_sum(s);
+            const float inv = 1.f / s;
+            for (int e = tx; e < E; e += 32) {
+                idx[(size_t)tok * E + e] = e;
+                w[(size_t)tok * E + e] = expf((lg[t * E + e] - m) * inv_temp) * inv;
+            }
+        }
+        return;
+    }
+
     // top-k per token: warp ty handles tokens ty, ty+8, ty+16, ty+24
     for (int a = 0; a < 4; ++a) {
         const int t = ty + 8 * a;
@@ -140,10 +162,13 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
     }
 }
 
-// balance_loss = mean over experts of (counts[e] - T*k/E)^2, in double.
-__global__ void balance_loss_kernel(const int32_t* __restrict__ counts, int E, double mean,
+// balance_loss = mean over experts of (counts[e] - T*k/E)^2, in double. With dense routing
+// (dense_T >= 0) every expert's count is first set to dense_T, the number of tokens.
+__global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double mean, int dense_T,
                                     float* __restrict__ out) {
     if (threadIdx.x == 0 && blockIdx.x == 0) {
+        if (dense_T >= 0)
+            for (int e = 0; e < E; ++e) counts[e] = dense_T;
         double s = 0.0;
         for (int e = 0; e < E; ++e) {
             const double dv = (double)counts[e] - mean;
@@ -187,7 +212,7 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         if (st != cudaSuccess) return st;
     }
     const double mean = (double)c.T * (double)c.k / (double)c.E;
-    balance_loss_kernel<<<1, 32, 0, s>>>(counts, c.E, mean, balance_loss);
+    balance_loss_kernel<<<1, 32, 0, s>>>(counts, c.E, mean, dense_routing(c) ? c.T : -1, balance_loss);
     count_launch();
     return cudaGetLastError();
 }

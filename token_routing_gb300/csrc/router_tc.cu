@@ -10,7 +10,8 @@
 //
 // One CTA per 128-token tile: warp 0 streams x and Wg tiles with TMA, warp 1 issues the
 // MMAs (N = E rounded up to 32), warps 2..5 read one token's E logits each from TMEM and
-// keep a sorted top-k list in registers. The kernel is bound by reading x from HBM.
+// keep a sorted top-k list in registers (or, with k = E, take the softmax over all E). The
+// kernel is bound by reading x from HBM.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -125,7 +126,40 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int tok = tok0 + row;
-        if (mbar_wait(tfull, 0, p.err)) {
+        if constexpr (K == 0) {
+            // dense soft routing: w[t, e] = softmax(z_t / temp)_e over all E, slot e = expert e.
+            // Three passes over the row in TMEM (max, sum, write); the noise is recomputed.
+            if (mbar_wait(tfull, 0, p.err)) {
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+                float m = -INFINITY, ssum = 0.f;
+                for (int pass = 0; pass < 3; ++pass) {
+                    const float inv = pass == 2 ? 1.f / ssum : 0.f;
+                    for (int c = 0; c < p.E_pad; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = c + i;
+                            if (e < p.E) {
+                                float v = __uint_as_float(r[i]) + s_bias[e];
+                                if (p.noise_std > 0.f) v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed), v);
+                                if (pass == 0) {
+                                    if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
+                                    m = fmaxf(m, v);
+                                } else if (pass == 1) {
+                                    ssum += expf((v - m) * p.inv_temp);
+                                } else if (tok < p.T) {
+                                    p.idx[(size_t)tok * p.E + e] = e;
+                                    p.w[(size_t)tok * p.E + e] = expf((v - m) * p.inv_temp) * inv;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        } else if (mbar_wait(tfull, 0, p.err)) {
             tc_fence_after();
             float tv[K];
             int te[K];
@@ -215,6 +249,7 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.stages = std::max(2, std::min(RMAX_STAGES, RSMEM_BUDGET / route_stage_bytes(p.E_pad)));
     const size_t smem = 1024 + (size_t)p.stages * route_stage_bytes(p.E_pad) +
                         (2 * RMAX_STAGES + 4) * sizeof(uint64_t) + 16 + 2 * MOE_MAX_EXPERTS * sizeof(int);
+    if (dense_routing(c)) return launch_k<0>(p, tx, tw, smem, s);
     switch (c.k) {
         case 1: return launch_k<1>(p, tx, tw, smem, s);
         case 2: return launch_k<2>(p, tx, tw, smem, s);

@@ -14,8 +14,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kSoftTok = 64;      // tokens per chunk of the soft-load partial sums
+constexpr int kSoftTok = 64;        // tokens per block of the soft-load partial sums (8 per warp)
 constexpr int kSoftThreads = 256;
+constexpr int kQ = MOE_MAX_EXPERTS / 32;   // experts per lane (e = lane + 32 q)
+constexpr int kDxTok = 8;           // tokens per block of dx += dz Wg
+constexpr int kDxThreads = 128;
+constexpr int kWgE = 8;             // experts per block of the dz^T x partials
+constexpr int kWgThreads = 128;
+constexpr int kWgChunk = 32;        // tokens staged in shared memory per round
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -23,46 +29,92 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// One token's softmax normaliser: m = max_e z_e, inv = 1 / sum_e exp((z_e - m) / temp).
-__device__ __forceinline__ void token_softmax_stats(const float* z, int E, float inv_temp, int lane,
-                                                    float& m, float& inv) {
+// One token's probabilities p_e = softmax(z / temp)_e, lane-distributed: p[q] is expert
+// lane + 32 q (0 beyond E). The whole warp takes part.
+__device__ __forceinline__ void token_softmax(const float* z, int E, float inv_temp, int lane, float (&p)[kQ]) {
     float mx = -INFINITY;
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, z[e]);
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+        const int e = lane + 32 * q;
+        p[q] = e < E ? z[e] : -INFINITY;
+        mx = fmaxf(mx, p[q]);
+    }
     mx = warp_max(mx);
     float s = 0.f;
-    for (int e = lane; e < E; e += 32) s += __expf((z[e] - mx) * inv_temp);
-    s = warp_sum(s);
-    m = mx;
-    inv = 1.f / s;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+        const int e = lane + 32 * q;
+        p[q] = e < E ? __expf((p[q] - mx) * inv_temp) : 0.f;
+        s += p[q];
+    }
+    const float inv = 1.f / warp_sum(s);
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) p[q] *= inv;
 }
 
-// part[chunk, e] = sum over the chunk's tokens (in order) of softmax(z_t / temp)_e.
+// Columns [c, c + V) of a row: a 16-byte vector when the row length allows, else guarded
+// scalar loads (zero beyond d).
+template <typename T>
+__device__ __forceinline__ void load_cols(const T* row, int c, int d, float* out) {
+    constexpr int V = Vec16<T>::N;
+    if ((d % V) == 0) {
+        load16(row + c, out);
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) out[i] = c + i < d ? ld_f(row + c + i) : 0.f;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_cols(T* row, int c, int d, const float* in) {
+    constexpr int V = Vec16<T>::N;
+    if ((d % V) == 0) {
+        store16(row + c, in);
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (c + i < d) st_f(row + c + i, in[i]);
+    }
+}
+
+// part[block, e] = sum over the block's 64 tokens of softmax(z_t / temp)_e: each warp sums
+// its 8 tokens in order, then the 8 warp sums are added in warp order.
 __global__ void __launch_bounds__(kSoftThreads)
 soft_load_kernel(const float* __restrict__ logits, int T, int E, float inv_temp, float* __restrict__ part) {
-    __shared__ float s_m[kSoftTok], s_inv[kSoftTok];
-    const int t0 = blockIdx.x * kSoftTok;
-    const int nt = min(kSoftTok, T - t0);
+    __shared__ float s_part[kSoftThreads / 32][MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < nt; i += kSoftThreads / 32) {
-        float m, inv;
-        token_softmax_stats(logits + (size_t)(t0 + i) * E, E, inv_temp, lane, m, inv);
-        if (lane == 0) { s_m[i] = m; s_inv[i] = inv; }
+    const int t0 = blockIdx.x * kSoftTok + warp * (kSoftTok / (kSoftThreads / 32));
+    float acc[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
+    for (int i = 0; i < kSoftTok / (kSoftThreads / 32); ++i) {
+        const int t = t0 + i;
+        if (t >= T) break;   // warp-uniform
+        float p[kQ];
+        token_softmax(logits + (size_t)t * E, E, inv_temp, lane, p);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) acc[q] += p[q];
     }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+        if (lane + 32 * q < E) s_part[warp][lane + 32 * q] = acc[q];
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float acc = 0.f;
-        for (int i = 0; i < nt; ++i) acc += __expf((logits[(size_t)(t0 + i) * E + e] - s_m[i]) * inv_temp) * s_inv[i];
-        part[(size_t)blockIdx.x * E + e] = acc;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSoftThreads / 32; ++w) v += s_part[w][e];
+        part[(size_t)blockIdx.x * E + e] = v;
     }
 }
 
-// P[e] = sum over chunks (in order); loss = weight * mean_e (P_e - T/E)^2 in double.
+// P[e] = sum over the blocks' partials (in order); loss = weight * mean_e (P_e - T/E)^2 in double.
 __global__ void __launch_bounds__(kSoftThreads)
 soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, float weight,
                   float* __restrict__ P, float* __restrict__ loss) {
     __shared__ float s_P[MOE_MAX_EXPERTS];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float acc = 0.f;
+#pragma unroll 8
         for (int c = 0; c < nchunk; ++c) acc += part[(size_t)c * E + e];
         s_P[e] = acc;
         P[e] = acc;
@@ -79,136 +131,166 @@ soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, floa
     }
 }
 
-// Per token (one warp): dz_te = p_te (g_e - sum_j p_tj g_j) / temp, written to dz, and
-// dx[t] += sum_e dz_te Wg[e] (read-modify-write in the activation type).
+// 8 tokens per block (x), V columns per thread (y). dz_te = p_te (g_e - sum_j p_tj g_j) / temp for the block's tokens
+// (written to dz by the first column block), then dx[t, c..c+V) += sum_e dz_te Wg[e, c..c+V),
+// experts in ascending order, read-modify-write in the activation type.
 template <typename T>
-__global__ void __launch_bounds__(kSoftThreads)
-soft_dz_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, int d,
-               float inv_temp, float weight, const T* __restrict__ Wg, T* __restrict__ dx,
-               float* __restrict__ dz) {
+__global__ void __launch_bounds__(kDxThreads)
+soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, int d,
+                  float inv_temp, float weight, const T* __restrict__ Wg, T* __restrict__ dx,
+                  float* __restrict__ dz) {
+    constexpr int V = Vec16<T>::N;
     __shared__ float s_g[MOE_MAX_EXPERTS];
+    __shared__ float s_dz[kDxTok][MOE_MAX_EXPERTS];
     const float mean = (float)Tn / (float)E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_g[e] = weight * 2.f * (P[e] - mean) / (float)E;
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    constexpr int V = Vec16<T>::N;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
-        const float* z = logits + (size_t)t * E;
-        float m, inv;
-        token_softmax_stats(z, E, inv_temp, lane, m, inv);
-        float pe[MOE_MAX_EXPERTS / 32], sdot = 0.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kDxTok;
+    const int nt = min(kDxTok, Tn - t0);
+    for (int i = warp; i < nt; i += kDxThreads / 32) {
+        const int t = t0 + i;
+        float p[kQ], sdot = 0.f;
+        token_softmax(logits + (size_t)t * E, E, inv_temp, lane, p);
 #pragma unroll
-        for (int q = 0; q < MOE_MAX_EXPERTS / 32; ++q) {
-            const int e = lane + 32 * q;
-            pe[q] = e < E ? __expf((z[e] - m) * inv_temp) * inv : 0.f;
-            sdot += e < E ? pe[q] * s_g[e] : 0.f;
-        }
+        for (int q = 0; q < kQ; ++q)
+            if (lane + 32 * q < E) sdot += p[q] * s_g[lane + 32 * q];
         sdot = warp_sum(sdot);
-        float dzl[MOE_MAX_EXPERTS / 32];
 #pragma unroll
-        for (int q = 0; q < MOE_MAX_EXPERTS / 32; ++q) {
+        for (int q = 0; q < kQ; ++q) {
             const int e = lane + 32 * q;
-            dzl[q] = e < E ? pe[q] * (s_g[e] - sdot) * inv_temp : 0.f;
-            if (e < E) dz[(size_t)t * E + e] = dzl[q];
-        }
-        if ((d % V) == 0) {
-            // warp-uniform trip count: every lane takes part in the shuffles
-            for (int c0 = 0; c0 < d; c0 += 32 * V) {
-                const int c = c0 + lane * V;
-                const bool active = c < d;
-                float acc[V];
-#pragma unroll
-                for (int i = 0; i < V; ++i) acc[i] = 0.f;
-                if (active) load16(dx + (size_t)t * d + c, acc);
-                for (int e = 0; e < E; ++e) {
-                    float dze = 0.f;
-#pragma unroll
-                    for (int q = 0; q < MOE_MAX_EXPERTS / 32; ++q)
-                        if (q == (e >> 5)) dze = __shfl_sync(0xffffffffu, dzl[q], e & 31);
-                    if (active) {
-                        float wv[V];
-                        load16(Wg + (size_t)e * d + c, wv);
-#pragma unroll
-                        for (int i = 0; i < V; ++i) acc[i] = fmaf(dze, wv[i], acc[i]);
-                    }
-                }
-                if (active) store16(dx + (size_t)t * d + c, acc);
-            }
-        } else {
-            for (int c0 = 0; c0 < d; c0 += 32) {
-                const int c = c0 + lane;
-                float acc = c < d ? ld_f(dx + (size_t)t * d + c) : 0.f;
-                for (int e = 0; e < E; ++e) {
-                    float dze = 0.f;
-#pragma unroll
-                    for (int q = 0; q < MOE_MAX_EXPERTS / 32; ++q)
-                        if (q == (e >> 5)) dze = __shfl_sync(0xffffffffu, dzl[q], e & 31);
-                    if (c < d) acc = fmaf(dze, ld_f(Wg + (size_t)e * d + c), acc);
-                }
-                if (c < d) st_f(dx + (size_t)t * d + c, acc);
+            if (e < E) {
+                const float v = p[q] * (s_g[e] - sdot) * inv_temp;
+                s_dz[i][e] = v;
+                if (blockIdx.y == 0) dz[(size_t)t * E + e] = v;
             }
         }
     }
+    __syncthreads();
+    const int c = (blockIdx.y * kDxThreads + threadIdx.x) * V;
+    if (c >= d) return;
+    float acc[kDxTok][V];
+#pragma unroll
+    for (int i = 0; i < kDxTok; ++i) {
+        if (i < nt) load_cols(dx + (size_t)(t0 + i) * d, c, d, acc[i]);
+        else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[i][v] = 0.f;
+        }
+    }
+    for (int e = 0; e < E; ++e) {
+        float wv[V];
+        load_cols(Wg + (size_t)e * d, c, d, wv);
+#pragma unroll
+        for (int i = 0; i < kDxTok; ++i) {
+            const float z = s_dz[i][e];
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[i][v] = fmaf(z, wv[v], acc[i][v]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kDxTok; ++i)
+        if (i < nt) store_cols(dx + (size_t)(t0 + i) * d, c, d, acc[i]);
 }
 
 // Split-K partials of dz^T x: part[split, e, c] = sum over the split's tokens (in order) of
-// dz[t, e] * x[t, c]; split column c == d holds sum_t dz[t, e] (for dbg).
+// dz[t, e] x[t, c], for 8 experts per block and V columns per thread; part[split, e, d] =
+// sum over the split's tokens of dz[t, e] (for dbg), from the first column block.
 template <typename T>
-__global__ void __launch_bounds__(kSoftThreads)
+__global__ void __launch_bounds__(kWgThreads)
 soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Tn, int E, int d,
                         int splits, float* __restrict__ part) {
-    const int e = blockIdx.y, sp = blockIdx.z;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c > d) return;
+    constexpr int V = Vec16<T>::N;
+    __shared__ float s_dz[kWgChunk][kWgE];
+    const int e0 = blockIdx.y * kWgE, sp = blockIdx.z;
     const int per = (Tn + splits - 1) / splits;
     const int t0 = sp * per, t1 = min(Tn, t0 + per);
-    // four independent accumulators (tokens t0+4i+u), summed in a fixed order at the end, so
-    // that four row loads are in flight per thread
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int t = t0;
-    if (c < d) {
-        for (; t + 4 <= t1; t += 4) {
-            const float z0 = dz[(size_t)t * E + e], z1 = dz[(size_t)(t + 1) * E + e];
-            const float z2 = dz[(size_t)(t + 2) * E + e], z3 = dz[(size_t)(t + 3) * E + e];
-            const float x0 = ld_f(x + (size_t)t * d + c), x1 = ld_f(x + (size_t)(t + 1) * d + c);
-            const float x2 = ld_f(x + (size_t)(t + 2) * d + c), x3 = ld_f(x + (size_t)(t + 3) * d + c);
-            a0 = fmaf(z0, x0, a0); a1 = fmaf(z1, x1, a1); a2 = fmaf(z2, x2, a2); a3 = fmaf(z3, x3, a3);
+    const int c = (blockIdx.x * kWgThreads + threadIdx.x) * V;
+    const bool col_ok = c < d;
+    const bool sums = blockIdx.x == 0 && threadIdx.x < kWgE;
+    float acc[kWgE][V];
+#pragma unroll
+    for (int u = 0; u < kWgE; ++u)
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[u][v] = 0.f;
+    float colsum = 0.f;
+    for (int tc = t0; tc < t1; tc += kWgChunk) {
+        const int n = min(kWgChunk, t1 - tc);
+        __syncthreads();
+        for (int j = threadIdx.x; j < kWgChunk * kWgE; j += kWgThreads) {
+            const int i = j / kWgE, u = j % kWgE;
+            s_dz[i][u] = (i < n && e0 + u < E) ? dz[(size_t)(tc + i) * E + e0 + u] : 0.f;
         }
-        for (; t < t1; ++t) a0 = fmaf(dz[(size_t)t * E + e], ld_f(x + (size_t)t * d + c), a0);
-    } else {
-        for (; t + 4 <= t1; t += 4) {
-            a0 += dz[(size_t)t * E + e]; a1 += dz[(size_t)(t + 1) * E + e];
-            a2 += dz[(size_t)(t + 2) * E + e]; a3 += dz[(size_t)(t + 3) * E + e];
+        __syncthreads();
+        if (col_ok) {
+            for (int i = 0; i < n; ++i) {
+                float xv[V];
+                load_cols(x + (size_t)(tc + i) * d, c, d, xv);
+#pragma unroll
+                for (int u = 0; u < kWgE; ++u) {
+                    const float z = s_dz[i][u];
+#pragma unroll
+                    for (int v = 0; v < V; ++v) acc[u][v] = fmaf(z, xv[v], acc[u][v]);
+                }
+            }
         }
-        for (; t < t1; ++t) a0 += dz[(size_t)t * E + e];
+        if (sums)
+            for (int i = 0; i < n; ++i) colsum += s_dz[i][threadIdx.x];
     }
-    part[((size_t)sp * E + e) * (d + 1) + c] = (a0 + a1) + (a2 + a3);
+    const size_t pitch = (size_t)d + 1;
+#pragma unroll
+    for (int u = 0; u < kWgE; ++u) {
+        if (e0 + u >= E) break;
+        float* row = part + ((size_t)sp * E + e0 + u) * pitch;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            if (c + v < d) row[c + v] = acc[u][v];
+    }
+    if (sums && e0 + threadIdx.x < E) part[((size_t)sp * E + e0 + threadIdx.x) * pitch + d] = colsum;
 }
 
-// dWg[e, c] += sum over splits (in order); dbg[e] += the dz column sums.
+// dWg[e, c] (+)= sum over splits; dbg[e] (+)= the dz column sums. One block per (expert, 32
+// columns): warp w adds splits w, w + 8, ... in order, then the 8 warp sums are added in
+// warp order.
 __global__ void __launch_bounds__(kSoftThreads)
-soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits, float* __restrict__ dWg,
-                       float* __restrict__ dbg) {
+soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits, bool accumulate,
+                       float* __restrict__ dWg, float* __restrict__ dbg) {
+    __shared__ float s_acc[kSoftThreads / 32][32];
     const int e = blockIdx.y;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c > d) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 32 + lane;
+    const size_t pitch = (size_t)d + 1;
     float acc = 0.f;
-    for (int sp = 0; sp < splits; ++sp) acc += part[((size_t)sp * E + e) * (d + 1) + c];
-    if (c < d) dWg[(size_t)e * d + c] += acc;
-    else if (dbg) dbg[e] += acc;
+    if (c <= d) {
+#pragma unroll 4
+        for (int sp = warp; sp < splits; sp += kSoftThreads / 32) acc += part[((size_t)sp * E + e) * pitch + c];
+    }
+    s_acc[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && c <= d) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSoftThreads / 32; ++w) v += s_acc[w][lane];
+        if (c < d) dWg[(size_t)e * d + c] = accumulate ? dWg[(size_t)e * d + c] + v : v;
+        else if (dbg) dbg[e] = accumulate ? dbg[e] + v : v;
+    }
 }
 
 }  // namespace
 
 int soft_chunks(const moe_config_t& c) { return std::max(1, ceil_div(c.T, kSoftTok)); }
 
+static int dwg_col_blocks(const moe_config_t& c) {
+    const int V = c.dtype == MOE_BF16 ? 8 : 4;
+    return std::max(1, ceil_div(c.d, kWgThreads * V));
+}
+
 int soft_splits(const moe_config_t& c) {
-    const int col_blocks = ceil_div(c.d + 1, kSoftThreads);
-    // enough blocks for ~16 per SM; each split covers at least 64 tokens
-    const int s = ceil_div(16LL * num_sms(), (long long)c.E * col_blocks);
-    const int cap = std::max(1, ceil_div(c.T, 64));
-    return std::max(1, std::min(std::min(s, 256), cap));
+    // about two blocks per SM; each split covers at least 32 tokens
+    const long long blocks = (long long)dwg_col_blocks(c) * ceil_div(c.E, kWgE);
+    const int s = (int)std::min<long long>(256, ceil_div(2LL * num_sms(), blocks));
+    const int cap = std::max(1, ceil_div(c.T, 32));
+    return std::max(1, std::min(s, cap));
 }
 
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
@@ -238,25 +320,37 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
                                     const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
     const float inv_temp = 1.0f / c.temperature;
-    const int grid = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
+    const int V = c.dtype == MOE_BF16 ? 8 : 4;
+    dim3 g0(ceil_div(c.T, kDxTok), ceil_div(c.d, kDxThreads * V));
     if (c.dtype == MOE_BF16)
-        soft_dz_kernel<__nv_bfloat16><<<grid, kSoftThreads, 0, st>>>(
+        soft_dz_dx_kernel<__nv_bfloat16><<<g0, kDxThreads, 0, st>>>(
             logits, P, c.T, c.E, c.d, inv_temp, weight, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
     else
-        soft_dz_kernel<float><<<grid, kSoftThreads, 0, st>>>(logits, P, c.T, c.E, c.d, inv_temp, weight,
-                                                             (const float*)Wg, (float*)dx, s.dz);
+        soft_dz_dx_kernel<float><<<g0, kDxThreads, 0, st>>>(logits, P, c.T, c.E, c.d, inv_temp, weight,
+                                                            (const float*)Wg, (float*)dx, s.dz);
     count_launch();
+    return launch_dense_dwg(c, s.dz, x, dWg, dbg, true, s, st);
+}
+
+cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void* x, float* dWg, float* dbg,
+                             bool accumulate, const SoftScratch& s, cudaStream_t st) {
+    if (c.T == 0 && accumulate) return cudaSuccess;
     const int splits = soft_splits(c);
-    dim3 g1(ceil_div(c.d + 1, kSoftThreads), c.E, splits);
-    if (c.dtype == MOE_BF16)
-        soft_dwg_partial_kernel<__nv_bfloat16><<<g1, kSoftThreads, 0, st>>>(s.dz, (const __nv_bfloat16*)x, c.T,
-                                                                           c.E, c.d, splits, s.dwg_part);
-    else
-        soft_dwg_partial_kernel<float><<<g1, kSoftThreads, 0, st>>>(s.dz, (const float*)x, c.T, c.E, c.d,
-                                                                   splits, s.dwg_part);
-    count_launch();
-    dim3 g2(ceil_div(c.d + 1, kSoftThreads), c.E);
-    soft_dwg_reduce_kernel<<<g2, kSoftThreads, 0, st>>>(s.dwg_part, c.E, c.d, splits, dWg, dbg);
+    if (c.T > 0) {
+        dim3 g1(dwg_col_blocks(c), ceil_div(c.E, kWgE), splits);
+        if (c.dtype == MOE_BF16)
+            soft_dwg_partial_kernel<__nv_bfloat16><<<g1, kWgThreads, 0, st>>>(dz, (const __nv_bfloat16*)x, c.T,
+                                                                             c.E, c.d, splits, s.dwg_part);
+        else
+            soft_dwg_partial_kernel<float><<<g1, kWgThreads, 0, st>>>(dz, (const float*)x, c.T, c.E, c.d,
+                                                                     splits, s.dwg_part);
+        count_launch();
+    } else {
+        cudaError_t e = cudaMemsetAsync(s.dwg_part, 0, sizeof(float) * (size_t)splits * c.E * (c.d + 1), st);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 g2(ceil_div(c.d + 1, 32), c.E);
+    soft_dwg_reduce_kernel<<<g2, kSoftThreads, 0, st>>>(s.dwg_part, c.E, c.d, splits, accumulate, dWg, dbg);
     count_launch();
     return cudaGetLastError();
 }
