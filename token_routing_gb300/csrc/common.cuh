@@ -98,20 +98,31 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.26:
 //   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),  t = 1 / (1 + p x),
 // absolute error <= 1.5e-7; with x = |a| / sqrt(2), exp(-x^2) = exp(-a^2 / 2) = sqrt(2 pi) phi(a).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ void gelu_and_grad_f(float a, float& g, float& gp) {
-    const float x = fabsf(a) * 0.70710678118654752f;
-    // hardware reciprocal and exponential (about 1 ulp): far below the formula's 1.5e-7
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, x, 1.0f));
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    poly *= t;
-    const float e = __expf(-0.5f * a * a);                   // exp(-a^2/2) = exp(-x^2)
-    const float erf_abs = 1.0f - poly * e;                   // erf(|a|/sqrt 2)
-    const float Phi = 0.5f + copysignf(0.5f * erf_abs, a);   // standard normal CDF
+    // hardware reciprocal and base-2 exponential (relative error ~2^-22): far below the
+    // formula's 1.5e-7. The 1/2 of Phi = (1 + erf) / 2 is folded into the coefficients:
+    // h = 0.5 (a1 t + ... + a5 t^5) exp(-a^2/2) = 0.5 erfc(|a| / sqrt 2).
+    const float t = rcp_approx(fmaf(0.3275911f * 0.70710678118654752f, fabsf(a), 1.0f));
+    float q = fmaf(0.5f * 1.061405429f, t, 0.5f * -1.453152027f);
+    q = fmaf(q, t, 0.5f * 1.421413741f);
+    q = fmaf(q, t, 0.5f * -0.284496736f);
+    q = fmaf(q, t, 0.5f * 0.254829592f);
+    const float e = ex2_approx(a * a * -0.72134752044448170f);   // exp(-a^2/2) = 2^(-a^2 log2(e) / 2)
+    const float h = (q * t) * e;
+    const float Phi = a >= 0.f ? 1.0f - h : h;                     // standard normal CDF
     g = a * Phi;
-    gp = fmaf(a * 0.39894228040143268f, e, Phi);            // Phi + a phi(a)
+    gp = fmaf(a * 0.39894228040143268f, e, Phi);                  // Phi + a phi(a)
 }
 
 __device__ __forceinline__ float gelu_f(float a) {

@@ -169,8 +169,8 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
             // side input of the first chunk, fetched while the accumulator is being produced:
-            // the bias row (same for every lane) or, for dH, the forward pre-activation A read
-            // coalesced (lane l: row (l>>2)+8i of the warp's 32 rows, 16-byte segment l&3)
+            // the bias row (same for every lane) or, for dH, the saved GELU'(A) read coalesced
+            // (lane l: row (l>>2)+8i of the warp's 32 rows, 16-byte segment l&3)
             const size_t aux_row0 = (size_t)(t.m0 + quarter * 32 + (lane >> 2));
             Raw32 next;
             if (t.n0 + c_lo < p.N) {
@@ -183,6 +183,9 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
+            // the TMEM load of chunk c + 32 is in flight while chunk c is processed
+            uint32_t acc[32];
+            if (t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
             for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
                 if (t.n0 + c >= p.N) break;
                 const int n = t.n0 + c;
@@ -193,12 +196,11 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
-                uint32_t acc[32];
-                tmem_ld32(taddr + c, acc);
-                tmem_ld_wait();
+                tmem_ld_wait_regs(acc);
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                if (more) tmem_ld32(taddr + c + 32, acc);
                 const int y = t.m0 + quarter * 32;
                 if (KIND == kGemmWgrad) {
                     const uint32_t b = st.acquire(lane);

@@ -24,10 +24,14 @@ namespace {
 
 constexpr int P_BM = 256;                           // pair tile rows (128 per CTA)
 constexpr int P_HALF = 128;
-constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = P_HALF * BK * 2;          // 16 KB per CTA
 constexpr int P_B_BYTES = P_HALF * BK * 2;          // 16 KB per CTA: half of B's 256 columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+
+// Six 32 KB stages, except for Ffn1: its epilogue writes two outputs per chunk (H and GELU'),
+// so each epilogue warp keeps two pairs of staging buffers and the ring has five stages.
+template <int KIND> constexpr int pair_stages() { return KIND == kGemmFfn1 ? 5 : 6; }
+template <int KIND> constexpr int pair_epi_bytes() { return EPI_WARPS * (KIND == kGemmFfn1 ? 4 : 2) * STG_BYTES; }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -104,10 +108,11 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1) {
     constexpr bool WGRAD = (KIND == kGemmWgrad);
+    constexpr int P_STAGES = pair_stages<KIND>();
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stg_smem = smem + P_STAGES * P_STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(stg_smem + EPI_SMEM);
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg_smem + pair_epi_bytes<KIND>());
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -229,6 +234,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         const int quarter = warp & 3;
         const int c_lo = ((warp - 2) >> 2) * (BN / 2);
         Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
+        Stager2 st2{smem_u32(stg_smem + (warp - 2) * 4 * STG_BYTES), 0};   // Ffn1 only
         const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(tempty), 0), map_to_rank(smem_u32(tempty + 1), 0)};
         uint32_t tl = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += nclusters) {
@@ -256,6 +262,9 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
+            // the TMEM load of chunk c + 32 is in flight while chunk c is processed
+            uint32_t acc[32];
+            if (t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
             for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
                 if (t.n0 + c >= p.N) break;
                 const int n = t.n0 + c;
@@ -266,12 +275,11 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
-                uint32_t acc[32];
-                tmem_ld32(taddr + c, acc);
-                tmem_ld_wait();
+                tmem_ld_wait_regs(acc);
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                if (more) tmem_ld32(taddr + c + 32, acc);
                 const int y = t.m0 + quarter * 32;
                 if (KIND == kGemmWgrad) {
                     const uint32_t b = st.acquire(lane);
@@ -286,10 +294,8 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                         float gp[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) gelu_and_grad_f(v[i], v[i], gp[i]);
-                        uint32_t b = st.acquire(lane);
-                        st.store(lane, b, gp, &tmO0, n, y);
-                        b = st.acquire(lane);
-                        st.store(lane, b, v, &tmO1, n, y);
+                        const uint32_t b = st2.acquire(lane);
+                        st2.store(lane, b, gp, v, &tmO0, &tmO1, n, y);
                     } else {
                         const uint32_t b = st.acquire(lane);
                         st.store(lane, b, v, &tmO0, n, y);
@@ -335,12 +341,18 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     }
 }
 
-constexpr size_t kPairSmemBytes = 1024 + P_STAGES * P_STAGE_BYTES + EPI_SMEM + 16 * sizeof(uint64_t) + 16 +
-                                  kMaxOffsets * sizeof(int);
+template <int KIND>
+constexpr size_t pair_smem_bytes() {
+    return 1024 + (size_t)pair_stages<KIND>() * P_STAGE_BYTES + pair_epi_bytes<KIND>() + 16 * sizeof(uint64_t) +
+           16 + kMaxOffsets * sizeof(int);
+}
+static_assert(pair_smem_bytes<kGemmFfn1>() <= 227 * 1024 && pair_smem_bytes<kGemmFfn2>() <= 227 * 1024,
+              "shared memory per CTA");
 
 template <int KIND, bool A_MN, bool B_MN>
 cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
                         const CUtensorMap& o1, int clusters, cudaStream_t s) {
+    constexpr size_t kPairSmemBytes = pair_smem_bytes<KIND>();
     auto kern = tc_gemm_pair_kernel<KIND, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
     if (e != cudaSuccess) return e;

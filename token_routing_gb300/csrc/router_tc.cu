@@ -128,31 +128,63 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
         const int tok = tok0 + row;
         if constexpr (K == 0) {
             // dense soft routing: w[t, e] = softmax(z_t / temp)_e over all E, slot e = expert e.
-            // Three passes over the row in TMEM (max, sum, write); the noise is recomputed.
+            // Three passes over the row (max, sum, write). Without noise every pass reads the
+            // logits from TMEM; with noise the first pass leaves the noisy logits in the
+            // token's own w row (each normal is drawn once) and the later passes read them back.
             if (mbar_wait(tfull, 0, p.err)) {
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
-                float m = -INFINITY, ssum = 0.f;
-                for (int pass = 0; pass < 3; ++pass) {
-                    const float inv = pass == 2 ? 1.f / ssum : 0.f;
-                    for (int c = 0; c < p.E_pad; c += 32) {
+                const bool live = tok < p.T;
+                if (p.noise_std > 0.f) {
+                    float* wr = p.w + (size_t)(live ? tok : 0) * p.E;
+                    float m = -INFINITY;
+                    for (int c = 0; c < p.E_pad; c += 32) {   // warp-uniform TMEM loads
                         uint32_t r[32];
                         tmem_ld32(taddr + c, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int e = c + i;
-                            if (e < p.E) {
-                                float v = __uint_as_float(r[i]) + s_bias[e];
-                                if (p.noise_std > 0.f) v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed), v);
-                                if (pass == 0) {
-                                    if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
-                                    m = fmaxf(m, v);
-                                } else if (pass == 1) {
-                                    ssum += expf((v - m) * p.inv_temp);
-                                } else if (tok < p.T) {
-                                    p.idx[(size_t)tok * p.E + e] = e;
-                                    p.w[(size_t)tok * p.E + e] = expf((v - m) * p.inv_temp) * inv;
+                            if (e < p.E && live) {
+                                const float v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed),
+                                                     __uint_as_float(r[i]) + s_bias[e]);
+                                if (p.logits) p.logits[(size_t)tok * p.E + e] = v;
+                                wr[e] = v;
+                                m = fmaxf(m, v);
+                            }
+                        }
+                    }
+                    if (live) {
+                        float ssum = 0.f;
+                        for (int e = 0; e < p.E; ++e) ssum += expf((wr[e] - m) * p.inv_temp);
+                        const float inv = 1.f / ssum;
+                        for (int e = 0; e < p.E; ++e) {
+                            p.idx[(size_t)tok * p.E + e] = e;
+                            wr[e] = expf((wr[e] - m) * p.inv_temp) * inv;
+                        }
+                    }
+                } else {
+                    float m = -INFINITY, ssum = 0.f;
+                    for (int pass = 0; pass < 3; ++pass) {
+                        const float inv = pass == 2 ? 1.f / ssum : 0.f;
+                        for (int c = 0; c < p.E_pad; c += 32) {
+                            uint32_t r[32];
+                            tmem_ld32(taddr + c, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int e = c + i;
+                                if (e < p.E) {
+                                    const float v = __uint_as_float(r[i]) + s_bias[e];
+                                    if (pass == 0) {
+                                        if (p.logits && live) p.logits[(size_t)tok * p.E + e] = v;
+                                        m = fmaxf(m, v);
+                                    } else if (pass == 1) {
+                                        ssum += expf((v - m) * p.inv_temp);
+                                    } else if (live) {
+                                        p.idx[(size_t)tok * p.E + e] = e;
+                                        p.w[(size_t)tok * p.E + e] = expf((v - m) * p.inv_temp) * inv;
+                                    }
                                 }
                             }
                         }

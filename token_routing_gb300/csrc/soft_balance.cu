@@ -178,7 +178,22 @@ soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P,
             for (int v = 0; v < V; ++v) acc[i][v] = 0.f;
         }
     }
-    for (int e = 0; e < E; ++e) {
+    // four experts' Wg loads in flight, then their FMAs in ascending expert order
+    int e = 0;
+    for (; e + 4 <= E; e += 4) {
+        float wv[4][V];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load_cols(Wg + (size_t)(e + u) * d, c, d, wv[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < kDxTok; ++i) {
+                const float z = s_dz[i][e + u];
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[i][v] = fmaf(z, wv[u][v], acc[i][v]);
+            }
+    }
+    for (; e < E; ++e) {
         float wv[V];
         load_cols(Wg + (size_t)e * d, c, d, wv);
 #pragma unroll
@@ -223,7 +238,22 @@ soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, i
         }
         __syncthreads();
         if (col_ok) {
-            for (int i = 0; i < n; ++i) {
+            // four token rows in flight, then their FMAs in token order
+            int i = 0;
+            for (; i + 4 <= n; i += 4) {
+                float xv[4][V];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) load_cols(x + (size_t)(tc + i + q) * d, c, d, xv[q]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int u = 0; u < kWgE; ++u) {
+                        const float z = s_dz[i + q][u];
+#pragma unroll
+                        for (int v = 0; v < V; ++v) acc[u][v] = fmaf(z, xv[q][v], acc[u][v]);
+                    }
+            }
+            for (; i < n; ++i) {
                 float xv[V];
                 load_cols(x + (size_t)(tc + i) * d, c, d, xv);
 #pragma unroll

@@ -193,6 +193,33 @@ struct Stager {
     }
 };
 
+// Two outputs per 32-column chunk (Ffn1: GELU'(A) and H): buffer pair (count & 1) of one
+// epilogue warp, one proxy fence and one bulk group per chunk.
+struct Stager2 {
+    uint32_t base;
+    int count;
+    __device__ __forceinline__ uint32_t acquire(int lane) {
+        if (lane == 0 && count >= 2) bulk_wait_read1();
+        __syncwarp();
+        return base + (count & 1) * 2 * STG_BYTES;
+    }
+    __device__ __forceinline__ void store(int lane, uint32_t buf, const float* v0, const float* v1,
+                                          const CUtensorMap* tm0, const CUtensorMap* tm1, int x, int y) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf, lane, j), pack8(v0 + 8 * j));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf + STG_BYTES, lane, j), pack8(v1 + 8 * j));
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm0, buf, x, y);
+            tma_store_2d(tm1, buf + STG_BYTES, x, y);
+            bulk_commit();
+        }
+        ++count;
+    }
+};
+
 template <int KIND>
 __device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
     // an expert with no rows: its weight-gradient tile is zero
