@@ -28,10 +28,14 @@ constexpr int P_A_BYTES = P_HALF * BK * 2;          // 16 KB per CTA
 constexpr int P_B_BYTES = P_HALF * BK * 2;          // 16 KB per CTA: half of B's 256 columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 
-// Six 32 KB stages, except for Ffn1: its epilogue writes two outputs per chunk (H and GELU'),
-// so each epilogue warp keeps two pairs of staging buffers and the ring has five stages.
+// 8 epilogue warps (two per TMEM lane quarter, 128 columns each) that fetch the next chunk's
+// accumulator columns and side input ahead of use. Ffn1 writes two outputs per chunk (GELU'
+// and H): each of its warps keeps two staging buffer pairs, and its ring has five 32 KB stages
+// instead of six. (Sixteen epilogue warps without the fetch-ahead measured slower.)
+template <int KIND> constexpr int pair_epi_warps() { return 8; }
+template <int KIND> constexpr int pair_threads() { return 64 + 32 * pair_epi_warps<KIND>(); }
 template <int KIND> constexpr int pair_stages() { return KIND == kGemmFfn1 ? 5 : 6; }
-template <int KIND> constexpr int pair_epi_bytes() { return EPI_WARPS * (KIND == kGemmFfn1 ? 4 : 2) * STG_BYTES; }
+template <int KIND> constexpr int pair_epi_bytes() { return pair_epi_warps<KIND>() * (KIND == kGemmFfn1 ? 4 : 2) * STG_BYTES; }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -103,12 +107,15 @@ __device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const in
 }
 
 template <int KIND, bool A_MN, bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<KIND>(), 1)
 tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1) {
     constexpr bool WGRAD = (KIND == kGemmWgrad);
     constexpr int P_STAGES = pair_stages<KIND>();
+    constexpr int PE_THREADS = 32 * pair_epi_warps<KIND>();
+    constexpr int COLS = BN / (pair_epi_warps<KIND>() / 4);   // accumulator columns per epilogue warp
+    constexpr bool PREFETCH = pair_epi_warps<KIND>() == 8;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stg_smem = smem + P_STAGES * P_STAGE_BYTES;
@@ -130,7 +137,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, 2 * EPI_THREADS); }
+        for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, 2 * PE_THREADS); }
         mbar_init(drain, 1);
         *s_fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -232,9 +239,9 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     } else {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
         const int quarter = warp & 3;
-        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        const int c_lo = ((warp - 2) >> 2) * COLS;
         Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
-        Stager2 st2{smem_u32(stg_smem + (warp - 2) * 4 * STG_BYTES), 0};   // Ffn1 only
+        Stager2<2> st2{smem_u32(stg_smem + (warp - 2) * 4 * STG_BYTES), 0};   // Ffn1 only
         const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(tempty), 0), map_to_rank(smem_u32(tempty + 1), 0)};
         uint32_t tl = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += nclusters) {
@@ -251,8 +258,10 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
             const size_t aux_row0 = (size_t)(t.m0 + quarter * 32 + (lane >> 2));
+            // side input (bias row, or dH's saved GELU'(A)) of the first chunk, fetched while the
+            // accumulator is produced; each later chunk's is fetched one chunk ahead
             Raw32 next;
-            if (t.n0 + c_lo < p.N) {
+            if (PREFETCH && t.n0 + c_lo < p.N) {
                 if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
                 if (KIND == kGemmDH)
 #pragma unroll
@@ -262,24 +271,27 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
-            // the TMEM load of chunk c + 32 is in flight while chunk c is processed
+            // with PREFETCH the TMEM load of chunk c + 32 is in flight while chunk c is processed
             uint32_t acc[32];
-            if (t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
-            for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
+            if (PREFETCH && t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
+            for (int c = c_lo; c < c_lo + COLS; c += 32) {
                 if (t.n0 + c >= p.N) break;
                 const int n = t.n0 + c;
-                const Raw32 cur = next;
-                const bool more = c + 32 < c_lo + BN / 2 && n + 32 < p.N;
-                if (more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
-                if (more && KIND == kGemmDH)
+                Raw32 cur;
+                if (PREFETCH) cur = next;
+                else if (has_bias<KIND>()) load_raw32(cur, p.bias + (size_t)t.e * p.N + n);
+                const bool more = c + 32 < c_lo + COLS && n + 32 < p.N;
+                if (PREFETCH && more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
+                if (PREFETCH && more && KIND == kGemmDH)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
+                if (!PREFETCH) tmem_ld32(taddr + c, acc);
                 tmem_ld_wait_regs(acc);
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-                if (more) tmem_ld32(taddr + c + 32, acc);
+                if (PREFETCH && more) tmem_ld32(taddr + c + 32, acc);
                 const int y = t.m0 + quarter * 32;
                 if (KIND == kGemmWgrad) {
                     const uint32_t b = st.acquire(lane);
@@ -291,11 +303,8 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 32; ++i) v[i] += bv[i];
                     if (KIND == kGemmFfn1) {
                         // H = GELU(A) for the second GEMM, GELU'(A) saved for the backward
-                        float gp[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) gelu_and_grad_f(v[i], v[i], gp[i]);
                         const uint32_t b = st2.acquire(lane);
-                        st2.store(lane, b, gp, v, &tmO0, &tmO1, n, y);
+                        st2.store_gelu(lane, b, v, &tmO0, &tmO1, n, y);
                     } else {
                         const uint32_t b = st.acquire(lane);
                         st.store(lane, b, v, &tmO0, n, y);
@@ -356,7 +365,7 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorM
     auto kern = tc_gemm_pair_kernel<KIND, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<2 * clusters, THREADS, kPairSmemBytes, s>>>(p, a, b, o0, o1);
+    kern<<<2 * clusters, pair_threads<KIND>(), kPairSmemBytes, s>>>(p, a, b, o0, o1);
     count_launch();
     return cudaGetLastError();
 }

@@ -28,6 +28,7 @@ constexpr int RTHREADS = 192;
 
 struct RouteTcParams {
     int T, d, E, E_pad, stages;
+    int rows;          // tokens per CTA: 128, or 64 when 128-token tiles would leave SMs idle
     float inv_temp;
     float noise_std;
     uint32_t noise_seed;
@@ -59,9 +60,19 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
     __shared__ int s_fail;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok0 = blockIdx.x * RBM;
+    const int tok0 = blockIdx.x * p.rows;
     const int kblocks = (p.d + RBK - 1) / RBK;
     const uint32_t ncols = p.E_pad <= 32 ? 32 : p.E_pad <= 64 ? 64 : p.E_pad <= 128 ? 128 : 256;
+
+    // With 64-token tiles the MMA still runs M = 128: rows 64..127 of every stage's A tile are
+    // zeroed once (TMA fills only the first 64) and their accumulator rows are ignored.
+    if (p.rows < RBM) {
+        for (int s = 0; s < RSTAGES; ++s) {
+            uint4* a = reinterpret_cast<uint4*>(smem + s * stage_bytes + p.rows * RBK * 2);
+            for (int i = threadIdx.x; i < (RBM - p.rows) * RBK * 2 / 16; i += blockDim.x) a[i] = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
 
     for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) {
         s_cnt[e] = 0;
@@ -90,7 +101,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                 const uint32_t ph = (kb / RSTAGES) & 1;
                 if (!mbar_wait(empty + s, ph ^ 1, p.err)) { ok = false; break; }
                 const uint32_t sa = smem_u32(smem + s * stage_bytes);
-                mbar_expect_tx(full + s, stage_bytes);
+                mbar_expect_tx(full + s, p.rows * RBK * 2 + p.E_pad * RBK * 2);
                 tma_load_2d(sa, &tmX, kb * RBK, tok0, full + s);
                 tma_load_2d(sa + RBM * RBK * 2, &tmW, kb * RBK, 0, full + s);
             }
@@ -125,7 +136,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
     } else {
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int tok = tok0 + row;
+        const int tok = row < p.rows ? tok0 + row : p.T;   // rows beyond the tile: no token
         if constexpr (K == 0) {
             // dense soft routing: w[t, e] = softmax(z_t / temp)_e over all E, slot e = expert e.
             // Three passes over the row (max, sum, write). Without noise every pass reads the
@@ -255,7 +266,7 @@ cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtens
     auto kern = route_tc_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<ceil_div(p.T, RBM), RTHREADS, smem, s>>>(p, tx, tw);
+    kern<<<ceil_div(p.T, p.rows), RTHREADS, smem, s>>>(p, tx, tw);
     count_launch();
     return cudaGetLastError();
 }
@@ -275,10 +286,13 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.bg = c.has_gate_bias ? bg : nullptr;
     p.idx = idx; p.w = w; p.counts = counts; p.logits = logits;
     p.err = device_error_word();
+    p.rows = (long long)c.T >= (long long)RBM * num_sms() ? RBM : 64;
     CUtensorMap tx, tw;
-    if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, RBM)) return cudaErrorInvalidValue;
+    if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, (uint32_t)p.rows)) return cudaErrorInvalidValue;
     if (!make_map(&tw, Wg, (uint64_t)c.d, (uint64_t)c.E, (uint32_t)p.E_pad)) return cudaErrorInvalidValue;
-    p.stages = std::max(2, std::min(RMAX_STAGES, RSMEM_BUDGET / route_stage_bytes(p.E_pad)));
+    // 64-token tiles fit two CTAs per SM (half the shared memory each)
+    const int budget = p.rows < RBM ? RSMEM_BUDGET / 2 : RSMEM_BUDGET;
+    p.stages = std::max(2, std::min(RMAX_STAGES, budget / route_stage_bytes(p.E_pad)));
     const size_t smem = 1024 + (size_t)p.stages * route_stage_bytes(p.E_pad) +
                         (2 * RMAX_STAGES + 4) * sizeof(uint64_t) + 16 + 2 * MOE_MAX_EXPERTS * sizeof(int);
     if (dense_routing(c)) return launch_k<0>(p, tx, tw, smem, s);

@@ -107,17 +107,31 @@ soft_load_kernel(const float* __restrict__ logits, int T, int E, float inv_temp,
     }
 }
 
-// P[e] = sum over the blocks' partials (in order); loss = weight * mean_e (P_e - T/E)^2 in double.
-__global__ void __launch_bounds__(kSoftThreads)
+// P[e] = sum of the blocks' partials; loss = weight * mean_e (P_e - T/E)^2 in double. One
+// block of 32 warps: warp w owns experts w, w + 32, ...; its lanes add chunks lane, lane + 32,
+// ... (eight experts' loads in flight), then a butterfly sums the lanes (fixed order).
+constexpr int kFinalThreads = 1024;
+__global__ void __launch_bounds__(kFinalThreads)
 soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, float weight,
                   float* __restrict__ P, float* __restrict__ loss) {
     __shared__ float s_P[MOE_MAX_EXPERTS];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < nchunk; ++c) acc += part[(size_t)c * E + e];
-        s_P[e] = acc;
-        P[e] = acc;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int J = MOE_MAX_EXPERTS / (kFinalThreads / 32);
+    float acc[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] = 0.f;
+    for (int c = lane; c < nchunk; c += 32) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = warp + j * (kFinalThreads / 32);
+            if (e < E) acc[j] += part[(size_t)c * E + e];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = warp + j * (kFinalThreads / 32);
+        const float v = warp_sum(acc[j]);
+        if (lane == 0 && e < E) { s_P[e] = v; P[e] = v; }
     }
     __syncthreads();
     if (threadIdx.x == 0 && loss) {
@@ -340,7 +354,7 @@ cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, floa
         cudaError_t e = cudaMemsetAsync(s.part, 0, sizeof(float) * c.E, st);
         if (e != cudaSuccess) return e;
     }
-    soft_final_kernel<<<1, kSoftThreads, 0, st>>>(s.part, nchunk, c.T, c.E, weight, P, loss);
+    soft_final_kernel<<<1, kFinalThreads, 0, st>>>(s.part, nchunk, c.T, c.E, weight, P, loss);
     count_launch();
     return cudaGetLastError();
 }

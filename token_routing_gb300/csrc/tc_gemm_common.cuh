@@ -167,6 +167,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // One epilogue warp's staging buffers and store count (buffer = count & 1).
@@ -193,22 +194,33 @@ struct Stager {
     }
 };
 
-// Two outputs per 32-column chunk (Ffn1: GELU'(A) and H): buffer pair (count & 1) of one
-// epilogue warp, one proxy fence and one bulk group per chunk.
+// Two outputs per 32-column chunk (Ffn1: GELU'(A) and H): NB buffer pairs of one epilogue
+// warp (pair count % NB), one proxy fence and one bulk group per chunk.
+template <int NB>
 struct Stager2 {
     uint32_t base;
     int count;
+    // Returns the next buffer pair once the TMA stores that last read it have finished.
     __device__ __forceinline__ uint32_t acquire(int lane) {
-        if (lane == 0 && count >= 2) bulk_wait_read1();
+        if (lane == 0 && count >= NB) {
+            if (NB == 1) bulk_wait_read0();
+            else bulk_wait_read1();
+        }
         __syncwarp();
-        return base + (count & 1) * 2 * STG_BYTES;
+        return base + (count % NB) * 2 * STG_BYTES;
     }
-    __device__ __forceinline__ void store(int lane, uint32_t buf, const float* v0, const float* v1,
-                                          const CUtensorMap* tm0, const CUtensorMap* tm1, int x, int y) {
+    // a: the lane's 32 biased pre-activations. Eight at a time: GELU'(a) into the first
+    // buffer (tm0), GELU(a) into the second (tm1); then one fence and the two TMA stores.
+    __device__ __forceinline__ void store_gelu(int lane, uint32_t buf, const float* a,
+                                               const CUtensorMap* tm0, const CUtensorMap* tm1, int x, int y) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf, lane, j), pack8(v0 + 8 * j));
+        for (int j = 0; j < 4; ++j) {
+            float g[8], gp[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sts128(sw64_addr(buf + STG_BYTES, lane, j), pack8(v1 + 8 * j));
+            for (int i = 0; i < 8; ++i) gelu_and_grad_f(a[8 * j + i], g[i], gp[i]);
+            sts128(sw64_addr(buf, lane, j), pack8(gp));
+            sts128(sw64_addr(buf + STG_BYTES, lane, j), pack8(g));
+        }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
