@@ -183,9 +183,11 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
-            // the TMEM load of chunk c + 32 is in flight while chunk c is processed
+            // the heavy epilogues (Ffn1's GELU, dH's product with GELU') load the next
+            // accumulator chunk from TMEM while processing the current one
+            constexpr bool PREFETCH = KIND == kGemmFfn1 || KIND == kGemmDH;
             uint32_t acc[32];
-            if (t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
+            if (PREFETCH && t.n0 + c_lo < p.N) tmem_ld32(taddr + c_lo, acc);
             for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
                 if (t.n0 + c >= p.N) break;
                 const int n = t.n0 + c;
@@ -196,11 +198,12 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
+                if (!PREFETCH) tmem_ld32(taddr + c, acc);
                 tmem_ld_wait_regs(acc);
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-                if (more) tmem_ld32(taddr + c + 32, acc);
+                if (PREFETCH && more) tmem_ld32(taddr + c + 32, acc);
                 const int y = t.m0 + quarter * 32;
                 if (KIND == kGemmWgrad) {
                     const uint32_t b = st.acquire(lane);

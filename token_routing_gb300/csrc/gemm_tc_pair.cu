@@ -115,7 +115,9 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     constexpr int P_STAGES = pair_stages<KIND>();
     constexpr int PE_THREADS = 32 * pair_epi_warps<KIND>();
     constexpr int COLS = BN / (pair_epi_warps<KIND>() / 4);   // accumulator columns per epilogue warp
-    constexpr bool PREFETCH = pair_epi_warps<KIND>() == 8;
+    // the heavy epilogues (Ffn1's GELU, dH's product with GELU') load the next accumulator
+    // chunk from TMEM while processing the current one
+    constexpr bool PREFETCH = KIND == kGemmFfn1 || KIND == kGemmDH;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stg_smem = smem + P_STAGES * P_STAGE_BYTES;
@@ -261,7 +263,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             // side input (bias row, or dH's saved GELU'(A)) of the first chunk, fetched while the
             // accumulator is produced; each later chunk's is fetched one chunk ahead
             Raw32 next;
-            if (PREFETCH && t.n0 + c_lo < p.N) {
+            if (t.n0 + c_lo < p.N) {
                 if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
                 if (KIND == kGemmDH)
 #pragma unroll
@@ -277,12 +279,10 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             for (int c = c_lo; c < c_lo + COLS; c += 32) {
                 if (t.n0 + c >= p.N) break;
                 const int n = t.n0 + c;
-                Raw32 cur;
-                if (PREFETCH) cur = next;
-                else if (has_bias<KIND>()) load_raw32(cur, p.bias + (size_t)t.e * p.N + n);
+                const Raw32 cur = next;
                 const bool more = c + 32 < c_lo + COLS && n + 32 < p.N;
-                if (PREFETCH && more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
-                if (PREFETCH && more && KIND == kGemmDH)
+                if (more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
+                if (more && KIND == kGemmDH)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));

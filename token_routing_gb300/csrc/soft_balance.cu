@@ -145,9 +145,10 @@ soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, floa
     }
 }
 
-// 8 tokens per block (x), V columns per thread (y). dz_te = p_te (g_e - sum_j p_tj g_j) / temp for the block's tokens
-// (written to dz by the first column block), then dx[t, c..c+V) += sum_e dz_te Wg[e, c..c+V),
-// experts in ascending order, read-modify-write in the activation type.
+// For rows that are no multiple of 16 bytes. 8 tokens per block (x), V columns per thread (y).
+// dz_te = p_te (g_e - sum_j p_tj g_j) / temp for the block's tokens (written to dz by the first
+// column block), then dx[t, c..c+V) += sum_e dz_te Wg[e, c..c+V), experts in ascending order,
+// read-modify-write in the activation type.
 template <typename T>
 __global__ void __launch_bounds__(kDxThreads)
 soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, int d,
@@ -222,13 +223,14 @@ soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P,
         if (i < nt) store_cols(dx + (size_t)(t0 + i) * d, c, d, acc[i]);
 }
 
-// Split-K partials of dz^T x: part[split, e, c] = sum over the split's tokens (in order) of
-// dz[t, e] x[t, c], for 8 experts per block and V columns per thread; part[split, e, d] =
-// sum over the split's tokens of dz[t, e] (for dbg), from the first column block.
+// Split-K partials of dz^T x for rows that are no multiple of 16 bytes: part[split, e, c] =
+// sum over the split's tokens (in order) of dz[t, e] x[t, c], for 8 experts per block and V
+// columns per thread; part[split, e, d] = sum over the split's tokens of dz[t, e] (for dbg),
+// from the first column block.
 template <typename T>
 __global__ void __launch_bounds__(kWgThreads)
 soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Tn, int E, int d,
-                        int splits, float* __restrict__ part) {
+                        int splits, int pitch_, float* __restrict__ part) {
     constexpr int V = Vec16<T>::N;
     __shared__ float s_dz[kWgChunk][kWgE];
     const int e0 = blockIdx.y * kWgE, sp = blockIdx.z;
@@ -281,7 +283,7 @@ soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, i
         if (sums)
             for (int i = 0; i < n; ++i) colsum += s_dz[i][threadIdx.x];
     }
-    const size_t pitch = (size_t)d + 1;
+    const size_t pitch = (size_t)pitch_;
 #pragma unroll
     for (int u = 0; u < kWgE; ++u) {
         if (e0 + u >= E) break;
@@ -293,17 +295,238 @@ soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, i
     if (sums && e0 + threadIdx.x < E) part[((size_t)sp * E + e0 + threadIdx.x) * pitch + d] = colsum;
 }
 
+// ---------------------------------------------------------------- tiled kernels (16-byte rows)
+// The two contractions of the backward, dx += dz Wg ([T,E] x [E,d]) and dWg += dz^T x
+// ([E,T] x [T,d]), on CUDA cores with operand tiles staged in shared memory by cp.async, so
+// that many row loads are in flight per SM without holding registers. Each thread owns 8
+// consecutive columns and 4 tokens (dx) or 4 experts (dWg).
+constexpr int kTileThreads = 256;
+constexpr int kTileCols = 512;       // 64 column groups of 8
+constexpr int kTileStages = 3;       // dz^T x token pipeline depth
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(pred ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 8 consecutive elements at p (16-byte aligned) as floats.
+template <typename T>
+__device__ __forceinline__ void lds8(const T* p, float* out) {
+    if constexpr (sizeof(T) == 2) {
+        unpack16<T>(*reinterpret_cast<const uint4*>(p), out);
+    } else {
+        unpack16<T>(*reinterpret_cast<const uint4*>(p), out);
+        unpack16<T>(*reinterpret_cast<const uint4*>(p + 4), out + 4);
+    }
+}
+
+// dz_te = p_te (g_e - sum_j p_tj g_j) / temp, one warp per token.
+__global__ void __launch_bounds__(kSoftThreads)
+soft_dz_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, float inv_temp,
+               float weight, float* __restrict__ dz) {
+    __shared__ float s_g[MOE_MAX_EXPERTS];
+    const float mean = (float)Tn / (float)E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_g[e] = weight * 2.f * (P[e] - mean) / (float)E;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
+        float p[kQ], sdot = 0.f;
+        token_softmax(logits + (size_t)t * E, E, inv_temp, lane, p);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q)
+            if (lane + 32 * q < E) sdot += p[q] * s_g[lane + 32 * q];
+        sdot = warp_sum(sdot);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E) dz[(size_t)t * E + e] = p[q] * (s_g[e] - sdot) * inv_temp;
+        }
+    }
+}
+
+// dx[t, c] += sum_e dz[t, e] Wg[e, c] for 16 tokens (x) x 512 columns (y) per block, experts
+// in ascending order. dz of the block's tokens is staged once (transposed: 4 tokens per 16
+// bytes); Wg streams through (at most) two stages of ec experts. Shared memory is sized by E:
+// E * 64 B + stages * ec * 512 elements.
+template <typename T>
+__global__ void __launch_bounds__(kTileThreads)
+soft_dx_tiled_kernel(const float* __restrict__ dz, const T* __restrict__ Wg, int Tn, int E, int d, int ec,
+                     T* __restrict__ dx) {
+    constexpr int TB = 16;
+    extern __shared__ __align__(16) uint8_t sm[];
+    float* zt = reinterpret_cast<float*>(sm);                           // [E][TB]
+    T* ws = reinterpret_cast<T*>(sm + (size_t)E * TB * sizeof(float));   // [stages][ec][kTileCols]
+    const int tid = threadIdx.x, tc = tid & 63, tt = tid >> 6;
+    const int t0 = blockIdx.x * TB;
+    const int cb = blockIdx.y * kTileCols;
+    const int c = cb + tc * 8;
+    const int EC = ec;
+    const int nch = (E + EC - 1) / EC;
+
+    auto issue = [&](int ch) {
+        T* dst = ws + (size_t)(ch & 1) * EC * kTileCols;
+        constexpr int VR = kTileCols * (int)sizeof(T) / 16;   // 16-byte vectors per row
+        for (int i = tid; i < EC * VR; i += kTileThreads) {
+            const int r = i / VR, v = i % VR;
+            const int e = ch * EC + r, cc = cb + v * (16 / (int)sizeof(T));
+            const bool ok = e < E && cc < d;
+            cp_async16(smem_addr(dst + (size_t)r * kTileCols + v * (16 / (int)sizeof(T))),
+                       ok ? (const void*)(Wg + (size_t)e * d + cc) : (const void*)Wg, ok);
+        }
+    };
+    issue(0);
+    cp_async_commit();
+    for (int i = tid; i < E * TB; i += kTileThreads) {
+        const int e = i / TB, r = i % TB;
+        zt[i] = t0 + r < Tn ? dz[(size_t)(t0 + r) * E + e] : 0.f;
+    }
+    float acc[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) acc[u][v] = 0.f;
+        const int t = t0 + tt * 4 + u;
+        if (t < Tn && c < d) load_cols(dx + (size_t)t * d, c, d, acc[u]);
+        if (sizeof(T) == 4 && t < Tn && c + 4 < d) load_cols(dx + (size_t)t * d, c + 4, d, acc[u] + 4);
+    }
+    for (int ch = 0; ch < nch; ++ch) {
+        if (ch + 1 < nch) issue(ch + 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const T* wrow = ws + (size_t)(ch & 1) * EC * kTileCols + tc * 8;
+        const int ne = min(EC, E - ch * EC);
+        for (int j = 0; j < ne; ++j) {
+            float wv[8];
+            lds8(wrow + (size_t)j * kTileCols, wv);
+            const float4 z = *reinterpret_cast<const float4*>(zt + (size_t)(ch * EC + j) * TB + tt * 4);
+            const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc[u][v] = fmaf(zz[u], wv[v], acc[u][v]);
+        }
+        __syncthreads();   // the stage is refilled by the next iteration's issue
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = t0 + tt * 4 + u;
+        if (t >= Tn || c >= d) continue;
+        store_cols(dx + (size_t)t * d, c, d, acc[u]);
+        if (sizeof(T) == 4 && c + 4 < d) store_cols(dx + (size_t)t * d, c + 4, d, acc[u] + 4);
+    }
+}
+
+// Split-K partials of dz^T x for 16 experts (y) x 512 columns (x) per block over a token split
+// (z): part[split, e, c] = sum over the split's tokens, in order, of dz[t, e] x[t, c];
+// part[split, e, d] = the split's sum of dz[t, e] (for dbg), from the first column block.
+// Token chunks of x and dz go through a three-stage cp.async pipeline.
+template <typename T>
+__global__ void __launch_bounds__(kTileThreads)
+soft_dwg_tiled_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Tn, int E, int d, int splits,
+                      int pitch, float* __restrict__ part) {
+    constexpr int EB = 16;
+    constexpr int TS = sizeof(T) == 2 ? 32 : 16;      // 32 KB of x per stage
+    constexpr int VR = kTileCols * (int)sizeof(T) / 16;
+    extern __shared__ __align__(16) uint8_t sm[];
+    T* xs = reinterpret_cast<T*>(sm);                                                   // [S][TS][cols]
+    float* zs = reinterpret_cast<float*>(sm + (size_t)kTileStages * TS * kTileCols * sizeof(T));   // [S][TS][EB]
+    const int tid = threadIdx.x, tc = tid & 63, te = tid >> 6;
+    const int cb = blockIdx.x * kTileCols, e0 = blockIdx.y * EB, sp = blockIdx.z;
+    const int per = (Tn + splits - 1) / splits;
+    const int t0 = sp * per, t1 = min(Tn, t0 + per);
+    const int nch = t1 > t0 ? (t1 - t0 + TS - 1) / TS : 0;
+    const int c = cb + tc * 8;
+    const bool sums = blockIdx.x == 0 && tid < EB;
+
+    auto issue = [&](int ch) {
+        const int st = ch % kTileStages, tb = t0 + ch * TS;
+        T* xd = xs + (size_t)st * TS * kTileCols;
+        for (int i = tid; i < TS * VR; i += kTileThreads) {
+            const int r = i / VR, v = i % VR;
+            const int t = tb + r, cc = cb + v * (16 / (int)sizeof(T));
+            const bool ok = t < t1 && cc < d;
+            cp_async16(smem_addr(xd + (size_t)r * kTileCols + v * (16 / (int)sizeof(T))),
+                       ok ? (const void*)(x + (size_t)t * d + cc) : (const void*)x, ok);
+        }
+        float* zd = zs + (size_t)st * TS * EB;
+        for (int i = tid; i < TS * EB; i += kTileThreads) {
+            const int r = i / EB, u = i % EB;
+            const int t = tb + r, e = e0 + u;
+            const bool ok = t < t1 && e < E;
+            cp_async4(smem_addr(zd + i), ok ? (const void*)(dz + (size_t)t * E + e) : (const void*)dz, ok);
+        }
+    };
+
+    float acc[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) acc[u][v] = 0.f;
+    float colsum = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < kTileStages - 1; ++ch) {
+        if (ch < nch) issue(ch);
+        cp_async_commit();
+    }
+    for (int ch = 0; ch < nch; ++ch) {
+        cp_async_wait<kTileStages - 2>();
+        __syncthreads();   // chunk ch is in place everywhere; chunk ch - 1 is no longer read
+        if (ch + kTileStages - 1 < nch) issue(ch + kTileStages - 1);
+        cp_async_commit();
+        const int st = ch % kTileStages;
+        const int n = min(TS, t1 - (t0 + ch * TS));
+        const T* xr = xs + (size_t)st * TS * kTileCols + tc * 8;
+        const float* zr = zs + (size_t)st * TS * EB + te * 4;
+        for (int r = 0; r < n; ++r) {
+            float xv[8];
+            lds8(xr + (size_t)r * kTileCols, xv);
+            const float4 z = *reinterpret_cast<const float4*>(zr + (size_t)r * EB);
+            const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc[u][v] = fmaf(zz[u], xv[v], acc[u][v]);
+        }
+        if (sums)
+            for (int r = 0; r < n; ++r) colsum += zs[((size_t)st * TS + r) * EB + tid];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = e0 + te * 4 + u;
+        if (e >= E) continue;
+        float* row = part + ((size_t)sp * E + e) * pitch;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (c + 4 * h < d)
+                *reinterpret_cast<float4*>(row + c + 4 * h) =
+                    make_float4(acc[u][4 * h], acc[u][4 * h + 1], acc[u][4 * h + 2], acc[u][4 * h + 3]);
+    }
+    if (sums && e0 + tid < E) part[((size_t)sp * E + e0 + tid) * pitch + d] = colsum;
+}
+
 // dWg[e, c] (+)= sum over splits; dbg[e] (+)= the dz column sums. One block per (expert, 32
 // columns): warp w adds splits w, w + 8, ... in order, then the 8 warp sums are added in
 // warp order.
 __global__ void __launch_bounds__(kSoftThreads)
-soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits, bool accumulate,
+soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits, int pitch_, bool accumulate,
                        float* __restrict__ dWg, float* __restrict__ dbg) {
     __shared__ float s_acc[kSoftThreads / 32][32];
     const int e = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * 32 + lane;
-    const size_t pitch = (size_t)d + 1;
+    const size_t pitch = (size_t)pitch_;
     float acc = 0.f;
     if (c <= d) {
 #pragma unroll 4
@@ -329,18 +552,42 @@ static int dwg_col_blocks(const moe_config_t& c) {
     return std::max(1, ceil_div(c.d, kWgThreads * V));
 }
 
+// Row pitch of the dz^T x partials: d columns + the dz column sum, rounded up to 16 bytes.
+static int dwg_pitch(const moe_config_t& c) { return (c.d + 1 + 3) / 4 * 4; }
+
 int soft_splits(const moe_config_t& c) {
-    // about two blocks per SM; each split covers at least 32 tokens
-    const long long blocks = (long long)dwg_col_blocks(c) * ceil_div(c.E, kWgE);
+    // about two blocks of the tiled kernel per SM; each split covers at least 16 tokens
+    const long long blocks = (long long)ceil_div(c.d, kTileCols) * ceil_div(c.E, 16);
     const int s = (int)std::min<long long>(256, ceil_div(2LL * num_sms(), blocks));
-    const int cap = std::max(1, ceil_div(c.T, 32));
+    const int cap = std::max(1, ceil_div(c.T, 16));
     return std::max(1, std::min(s, cap));
+}
+
+// The tiled kernels need rows of whole 16-byte vectors and 16-byte aligned bases.
+static bool tiled_ok(const moe_config_t& c, const void* a, const void* b) {
+    const int V = c.dtype == MOE_BF16 ? 8 : 4;
+    return c.d % V == 0 && (((uintptr_t)a | (uintptr_t)b) & 15) == 0;
+}
+
+// experts per Wg stage of soft_dx_tiled_kernel (32 KB per stage at most) and its shared memory
+template <typename T>
+static int dx_tiled_ec(int E) { return std::min(E, sizeof(T) == 2 ? 32 : 16); }
+template <typename T>
+static size_t dx_tiled_smem(int E) {
+    const int ec = dx_tiled_ec<T>(E);
+    const int stages = E > ec ? 2 : 1;
+    return (size_t)E * 16 * sizeof(float) + (size_t)stages * ec * kTileCols * sizeof(T);
+}
+template <typename T>
+static size_t dwg_tiled_smem() {
+    constexpr int TS = sizeof(T) == 2 ? 32 : 16;
+    return (size_t)kTileStages * TS * (kTileCols * sizeof(T) + 16 * sizeof(float));
 }
 
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
     s->part = ws.take<float>((size_t)soft_chunks(c) * c.E);
     s->dz = ws.take<float>((size_t)c.T * c.E + 1);
-    s->dwg_part = ws.take<float>((size_t)soft_splits(c) * c.E * (c.d + 1));
+    s->dwg_part = ws.take<float>((size_t)soft_splits(c) * c.E * dwg_pitch(c));
 }
 
 cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, float weight, float* P,
@@ -364,15 +611,40 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
                                     const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
     const float inv_temp = 1.0f / c.temperature;
-    const int V = c.dtype == MOE_BF16 ? 8 : 4;
-    dim3 g0(ceil_div(c.T, kDxTok), ceil_div(c.d, kDxThreads * V));
-    if (c.dtype == MOE_BF16)
-        soft_dz_dx_kernel<__nv_bfloat16><<<g0, kDxThreads, 0, st>>>(
-            logits, P, c.T, c.E, c.d, inv_temp, weight, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
-    else
-        soft_dz_dx_kernel<float><<<g0, kDxThreads, 0, st>>>(logits, P, c.T, c.E, c.d, inv_temp, weight,
-                                                            (const float*)Wg, (float*)dx, s.dz);
-    count_launch();
+    if (tiled_ok(c, Wg, dx)) {
+        const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
+        soft_dz_kernel<<<g0, kSoftThreads, 0, st>>>(logits, P, c.T, c.E, inv_temp, weight, s.dz);
+        count_launch();
+        dim3 g(ceil_div(c.T, 16), ceil_div(c.d, kTileCols));
+        if (c.dtype == MOE_BF16) {
+            auto k = soft_dx_tiled_kernel<__nv_bfloat16>;
+            const size_t sm = dx_tiled_smem<__nv_bfloat16>(c.E);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            if (e != cudaSuccess) return e;
+            k<<<g, kTileThreads, sm, st>>>(s.dz, (const __nv_bfloat16*)Wg, c.T, c.E, c.d,
+                                           dx_tiled_ec<__nv_bfloat16>(c.E), (__nv_bfloat16*)dx);
+        } else {
+            auto k = soft_dx_tiled_kernel<float>;
+            const size_t sm = dx_tiled_smem<float>(c.E);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            if (e != cudaSuccess) return e;
+            k<<<g, kTileThreads, sm, st>>>(s.dz, (const float*)Wg, c.T, c.E, c.d, dx_tiled_ec<float>(c.E),
+                                           (float*)dx);
+        }
+        count_launch();
+    } else {
+        const int V = c.dtype == MOE_BF16 ? 8 : 4;
+        dim3 g0(ceil_div(c.T, kDxTok), ceil_div(c.d, kDxThreads * V));
+        if (c.dtype == MOE_BF16)
+            soft_dz_dx_kernel<__nv_bfloat16><<<g0, kDxThreads, 0, st>>>(
+                logits, P, c.T, c.E, c.d, inv_temp, weight, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
+        else
+            soft_dz_dx_kernel<float><<<g0, kDxThreads, 0, st>>>(logits, P, c.T, c.E, c.d, inv_temp, weight,
+                                                                (const float*)Wg, (float*)dx, s.dz);
+        count_launch();
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     return launch_dense_dwg(c, s.dz, x, dWg, dbg, true, s, st);
 }
 
@@ -380,21 +652,38 @@ cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void*
                              bool accumulate, const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0 && accumulate) return cudaSuccess;
     const int splits = soft_splits(c);
-    if (c.T > 0) {
+    const int pitch = dwg_pitch(c);
+    if (c.T > 0 && tiled_ok(c, x, s.dwg_part)) {
+        dim3 g1(ceil_div(c.d, kTileCols), ceil_div(c.E, 16), splits);
+        if (c.dtype == MOE_BF16) {
+            auto k = soft_dwg_tiled_kernel<__nv_bfloat16>;
+            const size_t sm = dwg_tiled_smem<__nv_bfloat16>();
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            if (e != cudaSuccess) return e;
+            k<<<g1, kTileThreads, sm, st>>>(dz, (const __nv_bfloat16*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
+        } else {
+            auto k = soft_dwg_tiled_kernel<float>;
+            const size_t sm = dwg_tiled_smem<float>();
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            if (e != cudaSuccess) return e;
+            k<<<g1, kTileThreads, sm, st>>>(dz, (const float*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
+        }
+        count_launch();
+    } else if (c.T > 0) {
         dim3 g1(dwg_col_blocks(c), ceil_div(c.E, kWgE), splits);
         if (c.dtype == MOE_BF16)
             soft_dwg_partial_kernel<__nv_bfloat16><<<g1, kWgThreads, 0, st>>>(dz, (const __nv_bfloat16*)x, c.T,
-                                                                             c.E, c.d, splits, s.dwg_part);
+                                                                             c.E, c.d, splits, pitch, s.dwg_part);
         else
             soft_dwg_partial_kernel<float><<<g1, kWgThreads, 0, st>>>(dz, (const float*)x, c.T, c.E, c.d,
-                                                                     splits, s.dwg_part);
+                                                                     splits, pitch, s.dwg_part);
         count_launch();
     } else {
-        cudaError_t e = cudaMemsetAsync(s.dwg_part, 0, sizeof(float) * (size_t)splits * c.E * (c.d + 1), st);
+        cudaError_t e = cudaMemsetAsync(s.dwg_part, 0, sizeof(float) * (size_t)splits * c.E * pitch, st);
         if (e != cudaSuccess) return e;
     }
     dim3 g2(ceil_div(c.d + 1, 32), c.E);
-    soft_dwg_reduce_kernel<<<g2, kSoftThreads, 0, st>>>(s.dwg_part, c.E, c.d, splits, accumulate, dWg, dbg);
+    soft_dwg_reduce_kernel<<<g2, kSoftThreads, 0, st>>>(s.dwg_part, c.E, c.d, splits, pitch, accumulate, dWg, dbg);
     count_launch();
     return cudaGetLastError();
 }
