@@ -21,6 +21,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
                const float* __restrict__ w, int Tn, int d, int k, T* __restrict__ y) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
@@ -106,6 +107,7 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
                    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
                    const int32_t* __restrict__ slot_row, int d, int k, int rows_cap, bool dense,
                    T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossblk) {
+    pdl_wait();
     __shared__ float s_warp[8];
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -173,6 +175,7 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                   const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
                   int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
@@ -242,6 +245,7 @@ router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw
                        const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                        const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
                        int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+    pdl_wait();
     __shared__ float s_dz[8][MOE_MAX_EXPERTS];
     __shared__ int s_row[8][MOE_MAX_EXPERTS];
     __shared__ int s_ex[8][MOE_MAX_EXPERTS];
@@ -325,6 +329,7 @@ __global__ void __launch_bounds__(256)
 dwg_partial_kernel(const T* __restrict__ x, const float* __restrict__ dz,
                    const int32_t* __restrict__ assign_off, const int32_t* __restrict__ assign_tok,
                    int d, int k, int nchunk, float* __restrict__ part) {
+    pdl_wait();
     constexpr int V = Vec16<T>::N;
     constexpr int PIECE = 256;
     __shared__ int s_tok[PIECE];
@@ -390,6 +395,7 @@ dwg_partial_kernel(const T* __restrict__ x, const float* __restrict__ dz,
 // assignments (one block per expert, fixed reduction tree).
 __global__ void __launch_bounds__(256)
 dwg_reduce_kernel(const float* __restrict__ part, int d, int nchunk, float* __restrict__ dWg) {
+    pdl_wait();
     const int e = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= d) return;
@@ -401,6 +407,7 @@ dwg_reduce_kernel(const float* __restrict__ part, int d, int nchunk, float* __re
 __global__ void __launch_bounds__(256)
 dbg_kernel(const float* __restrict__ dz, const int32_t* __restrict__ assign_off,
            const int32_t* __restrict__ assign_tok, float* __restrict__ dbg) {
+    pdl_wait();
     __shared__ float red[256];
     const int e = blockIdx.x;
     float acc = 0.f;
@@ -421,6 +428,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 colsum_quarter_kernel(const T* __restrict__ M, int width, const int32_t* __restrict__ offsets, int E,
                       float* __restrict__ part) {
+    pdl_wait();
     constexpr int V = Vec16<T>::N;
     constexpr int QROWS = MOE_ROW_ALIGN / kColsumParts;
     const int pq = blockIdx.x;  // tile * 4 + quarter (x: up to 2^31 - 1 quarters)
@@ -455,6 +463,7 @@ colsum_quarter_kernel(const T* __restrict__ M, int width, const int32_t* __restr
 __global__ void __launch_bounds__(256)
 bias_reduce_kernel(const float* __restrict__ part, int width, const int32_t* __restrict__ offsets,
                    float* __restrict__ db) {
+    pdl_wait();
     const int e = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= width) return;
@@ -468,6 +477,7 @@ bias_reduce_kernel(const float* __restrict__ part, int width, const int32_t* __r
 __global__ void __launch_bounds__(256)
 loss_kernel(const float* __restrict__ lossblk, int nblk, const float* __restrict__ balance, float aux,
             float* __restrict__ loss) {
+    pdl_wait();
     __shared__ float red[8];
     float acc = 0.f;
     for (int i = threadIdx.x; i < nblk; i += blockDim.x) acc += lossblk[i];
@@ -493,10 +503,10 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t*
     if (c.T == 0) return cudaSuccess;
     const int grid = warp_grid(c.T);
     if (c.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)Yp, slot_row, w, c.T,
+        launch_pdl(combine_kernel<__nv_bfloat16>, grid, 256, 0, s, (const __nv_bfloat16*)Yp, slot_row, w, c.T,
                                                            c.d, c.k, (__nv_bfloat16*)y);
     else
-        combine_kernel<float><<<grid, 256, 0, s>>>((const float*)Yp, slot_row, w, c.T, c.d, c.k, (float*)y);
+        launch_pdl(combine_kernel<float>, grid, 256, 0, s, (const float*)Yp, slot_row, w, c.T, c.d, c.k, (float*)y);
     count_launch();
     return cudaGetLastError();
 }
@@ -508,16 +518,16 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
                                const int32_t* slot_row, void* dYp, float* dw, float* lossblk,
                                cudaStream_t s) {
     if (c.T > 0) {
-        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)c.T * c.k, s);
+        cudaError_t e = launch_fill(dw, (long long)c.T * c.k, 0.f, s);
         if (e != cudaSuccess) return e;
     }
     const int grid = combine_bwd_blocks(c);
     if (c.dtype == MOE_BF16)
-        combine_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        launch_pdl(combine_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
             (const __nv_bfloat16*)dy, (const __nv_bfloat16*)Yp, w, offsets, c.E, row_token, slot_row,
             c.d, c.k, c.rows_capacity, dense_routing(c), (__nv_bfloat16*)dYp, dw, lossblk);
     else
-        combine_bwd_kernel<float><<<grid, 256, 0, s>>>((const float*)dy, (const float*)Yp, w, offsets,
+        launch_pdl(combine_bwd_kernel<float>, grid, 256, 0, s, (const float*)dy, (const float*)Yp, w, offsets,
                                                        c.E, row_token, slot_row, c.d, c.k,
                                                        c.rows_capacity, dense_routing(c), (float*)dYp, dw,
                                                        lossblk);
@@ -533,19 +543,19 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
     const float inv_temp = 1.0f / c.temperature;
     if (c.k > MOE_MAX_K) {
         if (c.dtype == MOE_BF16)
-            router_bwd_wide_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            launch_pdl(router_bwd_wide_kernel<__nv_bfloat16>, grid, 256, 0, s, 
                 w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
                 c.E, inv_temp, dz, (__nv_bfloat16*)dx);
         else
-            router_bwd_wide_kernel<float><<<grid, 256, 0, s>>>(w, dw, idx, slot_row, (const float*)Wg,
+            launch_pdl(router_bwd_wide_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
                                                                (const float*)dXp, c.T, c.d, c.k, c.E,
                                                                inv_temp, dz, (float*)dx);
     } else if (c.dtype == MOE_BF16)
-        router_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        launch_pdl(router_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
             w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
             c.E, inv_temp, dz, (__nv_bfloat16*)dx);
     else
-        router_bwd_kernel<float><<<grid, 256, 0, s>>>(w, dw, idx, slot_row, (const float*)Wg,
+        launch_pdl(router_bwd_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
                                                       (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp,
                                                       dz, (float*)dx);
     count_launch();
@@ -565,17 +575,17 @@ cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
     const int V = c.dtype == MOE_BF16 ? 8 : 4;
     const int threads = std::max(32, std::min(256, (ceil_div(c.d, V) + 31) / 32 * 32));
     if (c.dtype == MOE_BF16)
-        dwg_partial_kernel<__nv_bfloat16><<<g1, threads, 0, s>>>((const __nv_bfloat16*)x, dz, srt.assign_off,
+        launch_pdl(dwg_partial_kernel<__nv_bfloat16>, g1, threads, 0, s, (const __nv_bfloat16*)x, dz, srt.assign_off,
                                                                  srt.assign_tok, c.d, c.k, nchunk, part);
     else
-        dwg_partial_kernel<float><<<g1, threads, 0, s>>>((const float*)x, dz, srt.assign_off,
+        launch_pdl(dwg_partial_kernel<float>, g1, threads, 0, s, (const float*)x, dz, srt.assign_off,
                                                          srt.assign_tok, c.d, c.k, nchunk, part);
     count_launch();
     dim3 g2(ceil_div(c.d, 256), c.E);
-    dwg_reduce_kernel<<<g2, 256, 0, s>>>(part, c.d, nchunk, dWg);
+    launch_pdl(dwg_reduce_kernel, g2, 256, 0, s, part, c.d, nchunk, dWg);
     count_launch();
     if (dbg) {
-        dbg_kernel<<<c.E, 256, 0, s>>>(dz, srt.assign_off, srt.assign_tok, dbg);
+        launch_pdl(dbg_kernel, c.E, 256, 0, s, dz, srt.assign_off, srt.assign_tok, dbg);
         count_launch();
     }
     return cudaGetLastError();
@@ -589,9 +599,9 @@ cudaError_t launch_colsum(const moe_config_t& c, const void* M, int width, const
     const int threads = std::max(32, std::min(256, (ceil_div(width, V) + 31) / 32 * 32));
     dim3 g(quarters, ceil_div(width, threads * V));
     if (c.dtype == MOE_BF16)
-        colsum_quarter_kernel<__nv_bfloat16><<<g, threads, 0, s>>>((const __nv_bfloat16*)M, width, offsets, c.E, part);
+        launch_pdl(colsum_quarter_kernel<__nv_bfloat16>, g, threads, 0, s, (const __nv_bfloat16*)M, width, offsets, c.E, part);
     else
-        colsum_quarter_kernel<float><<<g, threads, 0, s>>>((const float*)M, width, offsets, c.E, part);
+        launch_pdl(colsum_quarter_kernel<float>, g, threads, 0, s, (const float*)M, width, offsets, c.E, part);
     count_launch();
     return cudaGetLastError();
 }
@@ -599,14 +609,14 @@ cudaError_t launch_colsum(const moe_config_t& c, const void* M, int width, const
 cudaError_t launch_bias_reduce(const moe_config_t& c, const float* part, int width,
                                const int32_t* offsets, float* db, cudaStream_t s) {
     dim3 g(ceil_div(width, 256), c.E);
-    bias_reduce_kernel<<<g, 256, 0, s>>>(part, width, offsets, db);
+    launch_pdl(bias_reduce_kernel, g, 256, 0, s, part, width, offsets, db);
     count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_loss(const moe_config_t& c, const float* lossblk, const float* balance_loss,
                         float* loss, cudaStream_t s) {
-    loss_kernel<<<1, 256, 0, s>>>(lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss);
+    launch_pdl(loss_kernel, 1, 256, 0, s, lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss);
     count_launch();
     return cudaGetLastError();
 }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <algorithm>
 #include <atomic>
 
 #include "../../include/moe.h"
@@ -21,6 +22,42 @@ __device__ __forceinline__ void raise_error(int* err, int code) {
 // Cycle budget of every spin-wait (~2 s at 2 GHz): a wait that runs out records
 // kErrTimeout and returns false so the kernel can unwind instead of hanging.
 constexpr long long kSpinBudgetCycles = 4000000000LL;
+
+// ---------------------------------------------------------------- dependent launches
+// Kernels are launched with programmatic stream serialization: a kernel may start (and run
+// its prologue) while the previous kernel of its stream finishes. Every kernel therefore
+// calls pdl_wait() before its first access to global memory that another kernel writes or
+// reads; the wait returns once the previous kernel has completed and its writes are visible
+// (immediately when there is none). It then lets the next kernel of the stream launch.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// p[0..n) = v as a kernel, so that it orders with the dependent launches around it like any
+// other kernel of the stream.
+template <typename V>
+__global__ void __launch_bounds__(256) fill_kernel(V* __restrict__ p, long long n, V v) {
+    pdl_wait();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        p[i] = v;
+}
 
 // ---------------------------------------------------------------- element types
 template <typename T> struct Elem;
@@ -179,5 +216,14 @@ struct Workspace {
 };
 
 int num_sms();
+
+template <typename V>
+inline cudaError_t launch_fill(V* p, long long n, V v, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const long long blocks = std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
+    cudaError_t e = launch_pdl(fill_kernel<V>, dim3((unsigned)blocks), dim3(256), 0, s, p, n, v);
+    count_launch();
+    return e;
+}
 
 }  // namespace moe

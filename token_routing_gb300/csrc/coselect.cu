@@ -18,6 +18,7 @@ constexpr int kCoselSmemE = 64;   // up to this many experts the block histogram
 template <bool SMEM>
 __global__ void __launch_bounds__(kCoselThreads)
 coselect_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ H, int* err) {
+    pdl_wait();
     __shared__ int s_h[SMEM ? kCoselSmemE * kCoselSmemE : 1];
     if (SMEM) {
         for (int i = threadIdx.x; i < E * E; i += blockDim.x) s_h[i] = 0;
@@ -53,6 +54,7 @@ coselect_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int32_t* _
 // into H[0][0]; coselect_dense_fill_kernel then copies the count to every cell i <= j.
 __global__ void __launch_bounds__(kCoselThreads)
 coselect_dense_count_kernel(const int32_t* __restrict__ idx, int T, int E, int32_t* __restrict__ H, int* err) {
+    pdl_wait();
     __shared__ int s_n;
     if (threadIdx.x == 0) s_n = 0;
     __syncthreads();
@@ -70,6 +72,7 @@ coselect_dense_count_kernel(const int32_t* __restrict__ idx, int T, int E, int32
 
 __global__ void __launch_bounds__(kCoselThreads)
 coselect_dense_fill_kernel(int E, int32_t* __restrict__ H) {
+    pdl_wait();
     const int32_t n = H[0];
     __syncthreads();
     for (int c = threadIdx.x; c < E * E; c += blockDim.x) {
@@ -81,20 +84,20 @@ coselect_dense_fill_kernel(int E, int32_t* __restrict__ H) {
 }  // namespace
 
 cudaError_t launch_coselect(const moe_config_t& c, const int32_t* idx, int32_t* H, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(H, 0, sizeof(int32_t) * (size_t)c.E * c.E, s);
+    cudaError_t e = launch_fill(H, (long long)c.E * c.E, (int32_t)0, s);
     if (e != cudaSuccess || c.T == 0) return e;
     const int grid = std::max(1, std::min(ceil_div(c.T, kCoselThreads), 2 * num_sms()));
     if (dense_routing(c) && c.k > MOE_MAX_K) {
-        coselect_dense_count_kernel<<<grid, kCoselThreads, 0, s>>>(idx, c.T, c.E, H, device_error_word());
+        launch_pdl(coselect_dense_count_kernel, grid, kCoselThreads, 0, s, idx, c.T, c.E, H, device_error_word());
         count_launch();
-        coselect_dense_fill_kernel<<<1, kCoselThreads, 0, s>>>(c.E, H);
+        launch_pdl(coselect_dense_fill_kernel, 1, kCoselThreads, 0, s, c.E, H);
         count_launch();
         return cudaGetLastError();
     }
     if (c.E <= kCoselSmemE)
-        coselect_kernel<true><<<grid, kCoselThreads, 0, s>>>(idx, c.T, c.k, c.E, H, device_error_word());
+        launch_pdl(coselect_kernel<true>, grid, kCoselThreads, 0, s, idx, c.T, c.k, c.E, H, device_error_word());
     else
-        coselect_kernel<false><<<grid, kCoselThreads, 0, s>>>(idx, c.T, c.k, c.E, H, device_error_word());
+        launch_pdl(coselect_kernel<false>, grid, kCoselThreads, 0, s, idx, c.T, c.k, c.E, H, device_error_word());
     count_launch();
     return cudaGetLastError();
 }

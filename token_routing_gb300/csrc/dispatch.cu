@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(256)
 dense_layout_kernel(const int32_t* __restrict__ idx, int T, int E, int C, int align, int32_t* __restrict__ kept,
                     int32_t* __restrict__ offsets, int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row,
                     int32_t* __restrict__ n_dropped, int* err) {
+    pdl_wait();
     const int kp = min(T, C);
     const long long B = ((long long)kp + align - 1) / align * align;
     const long long n_slot = (long long)T * E;
@@ -266,6 +267,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 gather_kernel(const T* __restrict__ x, const int32_t* __restrict__ offsets, int E,
               const int32_t* __restrict__ row_token, int d, int rows_cap, T* __restrict__ Xp) {
+    pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int nrows = min(offsets[E], rows_cap);
@@ -351,7 +353,7 @@ cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32
                                 int32_t* row_token, int32_t* slot_row, int32_t* n_dropped, cudaStream_t st) {
     const long long items = (long long)c.T * c.E + (long long)c.rows_capacity;
     const int grid = (int)std::max(1LL, std::min((items + 255) / 256, (long long)num_sms() * 8));
-    dense_layout_kernel<<<grid, 256, 0, st>>>(idx, c.T, c.E, c.capacity, c.row_align, kept, offsets, row_token,
+    launch_pdl(dense_layout_kernel, grid, 256, 0, st, idx, c.T, c.E, c.capacity, c.row_align, kept, offsets, row_token,
                                               slot_row, n_dropped, device_error_word());
     count_launch();
     return cudaGetLastError();
@@ -363,11 +365,11 @@ cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* o
     const int rows_per_block = 8;
     const int grid = ceil_div(c.rows_capacity, rows_per_block);
     if (c.dtype == MOE_BF16)
-        gather_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)x, offsets, c.E,
+        launch_pdl(gather_kernel<__nv_bfloat16>, grid, 256, 0, st, (const __nv_bfloat16*)x, offsets, c.E,
                                                            row_token, c.d, c.rows_capacity,
                                                            (__nv_bfloat16*)Xp);
     else
-        gather_kernel<float><<<grid, 256, 0, st>>>((const float*)x, offsets, c.E, row_token, c.d,
+        launch_pdl(gather_kernel<float>, grid, 256, 0, st, (const float*)x, offsets, c.E, row_token, c.d,
                                                    c.rows_capacity, (float*)Xp);
     count_launch();
     return cudaGetLastError();

@@ -27,6 +27,7 @@ __device__ __forceinline__ int expert_of_row(const int32_t* offsets, int E, int 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 row_gemm_simt_kernel(RowGemmArgs a) {
+    pdl_wait();
     __shared__ float As[kBK][kBM + 4];
     __shared__ float Bs[kBK][kBN + 4];
     const int m0 = blockIdx.y * kBM;
@@ -105,6 +106,7 @@ row_gemm_simt_kernel(RowGemmArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 wgrad_simt_kernel(WgradArgs a) {
+    pdl_wait();
     __shared__ float Ps[kBK][kBM + 4];
     __shared__ float Qs[kBK][kBN + 4];
     const int e = blockIdx.z;
@@ -159,16 +161,16 @@ wgrad_simt_kernel(WgradArgs a) {
 cudaError_t launch_row_gemm_simt(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
     if (a.rows_capacity == 0) return cudaSuccess;
     dim3 grid(ceil_div(a.N, kBN), ceil_div(a.rows_capacity, kBM));
-    if (c.dtype == MOE_BF16) row_gemm_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
-    else row_gemm_simt_kernel<float><<<grid, kThreads, 0, s>>>(a);
+    if (c.dtype == MOE_BF16) launch_pdl(row_gemm_simt_kernel<__nv_bfloat16>, grid, kThreads, 0, s, a);
+    else launch_pdl(row_gemm_simt_kernel<float>, grid, kThreads, 0, s, a);
     count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_wgrad_simt(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
     dim3 grid(ceil_div(a.N, kBN), ceil_div(a.M, kBM), a.E);
-    if (c.dtype == MOE_BF16) wgrad_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
-    else wgrad_simt_kernel<float><<<grid, kThreads, 0, s>>>(a);
+    if (c.dtype == MOE_BF16) launch_pdl(wgrad_simt_kernel<__nv_bfloat16>, grid, kThreads, 0, s, a);
+    else launch_pdl(wgrad_simt_kernel<float>, grid, kThreads, 0, s, a);
     count_launch();
     return cudaGetLastError();
 }

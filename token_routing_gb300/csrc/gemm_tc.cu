@@ -47,7 +47,6 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, EPI_THREADS); }
@@ -62,6 +61,10 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                      ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // everything above touches only this CTA's shared memory and TMEM, and overlaps the
+    // previous kernel's tail; global memory is read from here on
+    pdl_wait();
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -278,7 +281,7 @@ cudaError_t launch_kernel(const TcParams& p, const CUtensorMap& a, const CUtenso
     auto kern = tc_gemm_kernel<KIND, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, kSmemBytes, s>>>(p, a, b, o0, o1);
+    launch_pdl(kern, grid, THREADS, kSmemBytes, s, p, a, b, o0, o1);
     count_launch();
     return cudaGetLastError();
 }

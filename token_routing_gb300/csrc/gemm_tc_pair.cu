@@ -136,7 +136,6 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     const int cluster_id = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
 
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(tfull + b, 1); mbar_init(tempty + b, 2 * PE_THREADS); }
@@ -151,6 +150,10 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                      ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
+    // everything above touches only this CTA's shared memory and TMEM, and overlaps the
+    // previous kernel's tail; global memory is read from here on
+    pdl_wait();
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -365,7 +368,7 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorM
     auto kern = tc_gemm_pair_kernel<KIND, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<2 * clusters, pair_threads<KIND>(), kPairSmemBytes, s>>>(p, a, b, o0, o1);
+    launch_pdl(kern, 2 * clusters, pair_threads<KIND>(), kPairSmemBytes, s, p, a, b, o0, o1);
     count_launch();
     return cudaGetLastError();
 }

@@ -33,6 +33,7 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
              int Tn, int d, int E, int k, float inv_temp, float noise_std, uint32_t noise_seed,
              int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
              float* __restrict__ logits) {
+    pdl_wait();
     extern __shared__ float smem[];
     float* xs = smem;                                    // [kRouteTok][kRouteKc+1]
     float* wsm = xs + kRouteTok * (kRouteKc + 1);        // [E][kRouteKc+1]
@@ -166,6 +167,7 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
 // (dense_T >= 0) every expert's count is first set to dense_T, the number of tokens.
 __global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double mean, int dense_T,
                                     float* __restrict__ out) {
+    pdl_wait();
     if (threadIdx.x == 0 && blockIdx.x == 0) {
         if (dense_T >= 0)
             for (int e = 0; e < E; ++e) counts[e] = dense_T;
@@ -183,7 +185,7 @@ __global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double 
 cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
                          int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
                          cudaStream_t s) {
-    cudaError_t st = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
+    cudaError_t st = launch_fill(counts, (long long)c.E, (int32_t)0, s);
     if (st != cudaSuccess) return st;
     if (c.T > 0 && tc_route_supported(c)) {
         st = launch_route_tc(c, x, Wg, bg, idx, w, counts, logits, s);
@@ -197,13 +199,13 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         if (c.dtype == MOE_BF16) {
             auto kern = route_kernel<__nv_bfloat16>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            kern<<<grid, kRouteThreads, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
+            launch_pdl(kern, grid, kRouteThreads, smem, s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
                                                    bias, c.T, c.d, c.E, c.k, inv_temp, c.noise_std, c.noise_seed,
                                                    idx, w, counts, logits);
         } else {
             auto kern = route_kernel<float>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            kern<<<grid, kRouteThreads, smem, s>>>((const float*)x, (const float*)Wg, bias, c.T, c.d,
+            launch_pdl(kern, grid, kRouteThreads, smem, s, (const float*)x, (const float*)Wg, bias, c.T, c.d,
                                                    c.E, c.k, inv_temp, c.noise_std, c.noise_seed, idx, w,
                                                    counts, logits);
         }
@@ -212,7 +214,7 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         if (st != cudaSuccess) return st;
     }
     const double mean = (double)c.T * (double)c.k / (double)c.E;
-    balance_loss_kernel<<<1, 32, 0, s>>>(counts, c.E, mean, dense_routing(c) ? c.T : -1, balance_loss);
+    launch_pdl(balance_loss_kernel, 1, 32, 0, s, counts, c.E, mean, dense_routing(c) ? c.T : -1, balance_loss);
     count_launch();
     return cudaGetLastError();
 }

@@ -74,10 +74,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
 
-    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) {
-        s_cnt[e] = 0;
-        s_bias[e] = (p.bg && e < p.E) ? p.bg[e] : 0.f;
-    }
+    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_cnt[e] = 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < RSTAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         mbar_init(tfull, 1);
@@ -87,6 +84,10 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) tmem_alloc(tmem_slot, ncols);
+    // everything above touches only this CTA's shared memory and TMEM, and overlaps the
+    // previous kernel's tail; global memory is read from here on
+    pdl_wait();
+    for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_bias[e] = (p.bg && e < p.E) ? p.bg[e] : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -266,7 +267,7 @@ cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtens
     auto kern = route_tc_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<ceil_div(p.T, p.rows), RTHREADS, smem, s>>>(p, tx, tw);
+    launch_pdl(kern, dim3(ceil_div(p.T, p.rows)), dim3(RTHREADS), smem, s, p, tx, tw);
     count_launch();
     return cudaGetLastError();
 }

@@ -81,6 +81,7 @@ __device__ __forceinline__ void store_cols(T* row, int c, int d, const float* in
 // its 8 tokens in order, then the 8 warp sums are added in warp order.
 __global__ void __launch_bounds__(kSoftThreads)
 soft_load_kernel(const float* __restrict__ logits, int T, int E, float inv_temp, float* __restrict__ part) {
+    pdl_wait();
     __shared__ float s_part[kSoftThreads / 32][MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kSoftTok + warp * (kSoftTok / (kSoftThreads / 32));
@@ -114,6 +115,7 @@ constexpr int kFinalThreads = 1024;
 __global__ void __launch_bounds__(kFinalThreads)
 soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, float weight,
                   float* __restrict__ P, float* __restrict__ loss) {
+    pdl_wait();
     __shared__ float s_P[MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int J = MOE_MAX_EXPERTS / (kFinalThreads / 32);
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kDxThreads)
 soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, int d,
                   float inv_temp, float weight, const T* __restrict__ Wg, T* __restrict__ dx,
                   float* __restrict__ dz) {
+    pdl_wait();
     constexpr int V = Vec16<T>::N;
     __shared__ float s_g[MOE_MAX_EXPERTS];
     __shared__ float s_dz[kDxTok][MOE_MAX_EXPERTS];
@@ -231,6 +234,7 @@ template <typename T>
 __global__ void __launch_bounds__(kWgThreads)
 soft_dwg_partial_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Tn, int E, int d,
                         int splits, int pitch_, float* __restrict__ part) {
+    pdl_wait();
     constexpr int V = Vec16<T>::N;
     __shared__ float s_dz[kWgChunk][kWgE];
     const int e0 = blockIdx.y * kWgE, sp = blockIdx.z;
@@ -334,6 +338,7 @@ __device__ __forceinline__ void lds8(const T* p, float* out) {
 __global__ void __launch_bounds__(kSoftThreads)
 soft_dz_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, float inv_temp,
                float weight, float* __restrict__ dz) {
+    pdl_wait();
     __shared__ float s_g[MOE_MAX_EXPERTS];
     const float mean = (float)Tn / (float)E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_g[e] = weight * 2.f * (P[e] - mean) / (float)E;
@@ -363,6 +368,7 @@ template <typename T>
 __global__ void __launch_bounds__(kTileThreads)
 soft_dx_tiled_kernel(const float* __restrict__ dz, const T* __restrict__ Wg, int Tn, int E, int d, int ec,
                      T* __restrict__ dx) {
+    pdl_wait();
     constexpr int TB = 16;
     extern __shared__ __align__(16) uint8_t sm[];
     float* zt = reinterpret_cast<float*>(sm);                           // [E][TB]
@@ -436,6 +442,7 @@ template <typename T>
 __global__ void __launch_bounds__(kTileThreads)
 soft_dwg_tiled_kernel(const float* __restrict__ dz, const T* __restrict__ x, int Tn, int E, int d, int splits,
                       int pitch, float* __restrict__ part) {
+    pdl_wait();
     constexpr int EB = 16;
     constexpr int TS = sizeof(T) == 2 ? 32 : 16;      // 32 KB of x per stage
     constexpr int VR = kTileCols * (int)sizeof(T) / 16;
@@ -522,6 +529,7 @@ soft_dwg_tiled_kernel(const float* __restrict__ dz, const T* __restrict__ x, int
 __global__ void __launch_bounds__(kSoftThreads)
 soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits, int pitch_, bool accumulate,
                        float* __restrict__ dWg, float* __restrict__ dbg) {
+    pdl_wait();
     __shared__ float s_acc[kSoftThreads / 32][32];
     const int e = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -595,13 +603,13 @@ cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, floa
     const float inv_temp = 1.0f / c.temperature;
     const int nchunk = soft_chunks(c);
     if (c.T > 0) {
-        soft_load_kernel<<<nchunk, kSoftThreads, 0, st>>>(logits, c.T, c.E, inv_temp, s.part);
+        launch_pdl(soft_load_kernel, nchunk, kSoftThreads, 0, st, logits, c.T, c.E, inv_temp, s.part);
         count_launch();
     } else {
-        cudaError_t e = cudaMemsetAsync(s.part, 0, sizeof(float) * c.E, st);
+        cudaError_t e = launch_fill(s.part, (long long)c.E, 0.f, st);
         if (e != cudaSuccess) return e;
     }
-    soft_final_kernel<<<1, kFinalThreads, 0, st>>>(s.part, nchunk, c.T, c.E, weight, P, loss);
+    launch_pdl(soft_final_kernel, 1, kFinalThreads, 0, st, s.part, nchunk, c.T, c.E, weight, P, loss);
     count_launch();
     return cudaGetLastError();
 }
@@ -613,7 +621,7 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
     const float inv_temp = 1.0f / c.temperature;
     if (tiled_ok(c, Wg, dx)) {
         const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
-        soft_dz_kernel<<<g0, kSoftThreads, 0, st>>>(logits, P, c.T, c.E, inv_temp, weight, s.dz);
+        launch_pdl(soft_dz_kernel, g0, kSoftThreads, 0, st, logits, P, c.T, c.E, inv_temp, weight, s.dz);
         count_launch();
         dim3 g(ceil_div(c.T, 16), ceil_div(c.d, kTileCols));
         if (c.dtype == MOE_BF16) {
@@ -621,14 +629,14 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
             const size_t sm = dx_tiled_smem<__nv_bfloat16>(c.E);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
             if (e != cudaSuccess) return e;
-            k<<<g, kTileThreads, sm, st>>>(s.dz, (const __nv_bfloat16*)Wg, c.T, c.E, c.d,
+            launch_pdl(k, g, kTileThreads, sm, st, s.dz, (const __nv_bfloat16*)Wg, c.T, c.E, c.d,
                                            dx_tiled_ec<__nv_bfloat16>(c.E), (__nv_bfloat16*)dx);
         } else {
             auto k = soft_dx_tiled_kernel<float>;
             const size_t sm = dx_tiled_smem<float>(c.E);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
             if (e != cudaSuccess) return e;
-            k<<<g, kTileThreads, sm, st>>>(s.dz, (const float*)Wg, c.T, c.E, c.d, dx_tiled_ec<float>(c.E),
+            launch_pdl(k, g, kTileThreads, sm, st, s.dz, (const float*)Wg, c.T, c.E, c.d, dx_tiled_ec<float>(c.E),
                                            (float*)dx);
         }
         count_launch();
@@ -636,10 +644,10 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
         const int V = c.dtype == MOE_BF16 ? 8 : 4;
         dim3 g0(ceil_div(c.T, kDxTok), ceil_div(c.d, kDxThreads * V));
         if (c.dtype == MOE_BF16)
-            soft_dz_dx_kernel<__nv_bfloat16><<<g0, kDxThreads, 0, st>>>(
+            launch_pdl(soft_dz_dx_kernel<__nv_bfloat16>, g0, kDxThreads, 0, st, 
                 logits, P, c.T, c.E, c.d, inv_temp, weight, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
         else
-            soft_dz_dx_kernel<float><<<g0, kDxThreads, 0, st>>>(logits, P, c.T, c.E, c.d, inv_temp, weight,
+            launch_pdl(soft_dz_dx_kernel<float>, g0, kDxThreads, 0, st, logits, P, c.T, c.E, c.d, inv_temp, weight,
                                                                 (const float*)Wg, (float*)dx, s.dz);
         count_launch();
     }
@@ -660,30 +668,30 @@ cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void*
             const size_t sm = dwg_tiled_smem<__nv_bfloat16>();
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
             if (e != cudaSuccess) return e;
-            k<<<g1, kTileThreads, sm, st>>>(dz, (const __nv_bfloat16*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
+            launch_pdl(k, g1, kTileThreads, sm, st, dz, (const __nv_bfloat16*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
         } else {
             auto k = soft_dwg_tiled_kernel<float>;
             const size_t sm = dwg_tiled_smem<float>();
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
             if (e != cudaSuccess) return e;
-            k<<<g1, kTileThreads, sm, st>>>(dz, (const float*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
+            launch_pdl(k, g1, kTileThreads, sm, st, dz, (const float*)x, c.T, c.E, c.d, splits, pitch, s.dwg_part);
         }
         count_launch();
     } else if (c.T > 0) {
         dim3 g1(dwg_col_blocks(c), ceil_div(c.E, kWgE), splits);
         if (c.dtype == MOE_BF16)
-            soft_dwg_partial_kernel<__nv_bfloat16><<<g1, kWgThreads, 0, st>>>(dz, (const __nv_bfloat16*)x, c.T,
+            launch_pdl(soft_dwg_partial_kernel<__nv_bfloat16>, g1, kWgThreads, 0, st, dz, (const __nv_bfloat16*)x, c.T,
                                                                              c.E, c.d, splits, pitch, s.dwg_part);
         else
-            soft_dwg_partial_kernel<float><<<g1, kWgThreads, 0, st>>>(dz, (const float*)x, c.T, c.E, c.d,
+            launch_pdl(soft_dwg_partial_kernel<float>, g1, kWgThreads, 0, st, dz, (const float*)x, c.T, c.E, c.d,
                                                                      splits, pitch, s.dwg_part);
         count_launch();
     } else {
-        cudaError_t e = cudaMemsetAsync(s.dwg_part, 0, sizeof(float) * (size_t)splits * c.E * pitch, st);
+        cudaError_t e = launch_fill(s.dwg_part, (long long)splits * c.E * pitch, 0.f, st);
         if (e != cudaSuccess) return e;
     }
     dim3 g2(ceil_div(c.d + 1, 32), c.E);
-    soft_dwg_reduce_kernel<<<g2, kSoftThreads, 0, st>>>(s.dwg_part, c.E, c.d, splits, pitch, accumulate, dWg, dbg);
+    launch_pdl(soft_dwg_reduce_kernel, g2, kSoftThreads, 0, st, s.dwg_part, c.E, c.d, splits, pitch, accumulate, dWg, dbg);
     count_launch();
     return cudaGetLastError();
 }
