@@ -33,6 +33,10 @@
  * - Pointers named as device pointers must point to device memory of the current device;
  *   host pointers are only the moe_config_t. The caller owns every buffer; the library
  *   allocates no device memory and keeps no per-call state. Outputs are overwritten.
+ * - Activation, weight and scratch arrays (x, Wg, W1, b1, W2, b2, Xp, Gp, H, Yp, y, dy, dx,
+ *   dW1, dW2 and ws) are read and written in 16-byte vectors and by TMA: their base
+ *   addresses must be 16-byte aligned (cudaMalloc and PyTorch allocations are), else the
+ *   call returns MOE_ERR_INVALID_ARG.
  * - All layouts are row-major, dense, following nn.Linear: x [T,d], Wg [E,d], bg [E] fp32,
  *   W1 [E,d_ff,d], b1 [E,d_ff], W2 [E,d,d_ff], b2 [E,d]. "act" below means the element
  *   type selected by cfg->dtype: fp32 (MOE_F32) or bf16 (MOE_BF16) for x, weights,
@@ -127,7 +131,9 @@ MOE_API size_t moe_workspace_bytes(const moe_config_t* cfg);
  *      T each with k = E), balance_loss [1] fp32,
  *      logits [T,E] fp32 (nullable: the routing logits z = x Wg^T + bg + noise; needed by
  *      moe_soft_balance).
- * Logits are accumulated in fp32. All pointers are device pointers. */
+ * Logits are accumulated in fp32. All pointers are device pointers. `ws` (moe_workspace_bytes)
+ * holds the routing noise when cfg->noise_std > 0 (drawn once per call, then added to the
+ * logits); it may be NULL when there is no noise. */
 MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
                        int32_t* idx, float* w, int32_t* counts, float* balance_loss,
                        float* logits, void* ws, moe_stream_t stream);

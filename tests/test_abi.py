@@ -129,6 +129,31 @@ def test_entry_points_reject_null_pointers(moe_lib):
     assert lib.moe_route(ctypes.byref(c2), p, p, None, p, p, p, p, None, p, None) == inval  # bg required
 
 
+def test_entry_points_reject_misaligned_arrays(moe_lib):
+    """Activation, weight and scratch arrays must start on a 16-byte boundary: a pointer one
+    element into a buffer is refused before anything is launched."""
+    lib = moe_lib.load()
+    c = _cfg(moe_lib)
+    assert lib.moe_config_init(ctypes.byref(c)) == 0
+    cfg = ctypes.byref(c)
+    p = ctypes.c_void_p(256)
+    q = ctypes.c_void_p(256 + 2)   # one bf16 element past an aligned base
+    inval = moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(cfg, q, p, None, p, p, p, p, None, p, None) == inval        # x
+    assert lib.moe_dispatch(cfg, p, p, p, p, p, p, p, q, p, None) == inval           # Xp
+    assert lib.moe_expert_ffn(cfg, p, p, p, q, p, p, p, p, p, p, None) == inval      # b1
+    assert lib.moe_combine(cfg, p, p, p, q, None) == inval                           # y
+    args = [p] * 26
+    args[0] = q                                                                       # dy
+    assert lib.moe_backward(cfg, *args) == inval
+    assert lib.moe_dispatch_noalloc(cfg, p, q, p, p, p, p, p, p, None) == inval       # x
+    # routing noise needs the workspace
+    cn = _cfg(moe_lib)
+    cn.noise_std = 0.1
+    assert lib.moe_config_init(ctypes.byref(cn)) == 0
+    assert lib.moe_route(ctypes.byref(cn), p, p, None, p, p, p, p, None, None, None) == inval
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_compute_call_without_gpu_reports_cuda_error(moe_lib):
     lib = moe_lib.load()

@@ -3,6 +3,7 @@
 // gemm_tc.cu / gemm_simt.cu and combine.cu.
 #include <climits>
 #include <cmath>
+#include <initializer_list>
 #include <mutex>
 
 #include "internal.cuh"
@@ -79,6 +80,14 @@ moe_status_t check_config(const moe_config_t* c) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Activation, weight and scratch arrays are read and written in 16-byte vectors and by TMA:
+// their base addresses must be 16-byte aligned (null pointers pass; they are checked apart).
+bool aligned16(std::initializer_list<const void*> ps) {
+    for (const void* p : ps)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return false;
+    return true;
+}
+
 #define MOE_TRY(expr)                                   \
     do {                                                \
         cudaError_t _e = (expr);                        \
@@ -97,6 +106,7 @@ struct BackwardScratch {
     float* colsum_d;    // column-sum partials of dYp (db2)
     float* colsum_f;    // column-sum partials of dA (db1)
     SoftScratch soft;   // soft balance loss
+    float* noise;       // routing noise [E, T] (expert-major), when cfg.noise_std > 0
 };
 
 size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
@@ -113,6 +123,7 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     b->dwg_part = ws.take<float>((size_t)c.E * dwg_chunks(c) * c.d);
     b->colsum_d = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d + 1);
     b->colsum_f = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d_ff + 1);
+    b->noise = ws.take<float>(c.noise_std > 0.f ? (size_t)c.T * c.E + 1 : 1);
     soft_scratch_take(ws, c, &b->soft);
     return align_up(ws.used, 256);
 }
@@ -206,12 +217,20 @@ size_t moe_workspace_bytes(const moe_config_t* cfg) {
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* bg,
                        int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
                        void* ws, moe_stream_t stream) {
-    (void)ws;
     moe_status_t st = check_config(cfg);
     if (st != MOE_OK) return st;
     if (!Wg || !counts || !balance_loss || (cfg->has_gate_bias && !bg)) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!x || !idx || !w)) return MOE_ERR_INVALID_ARG;
-    return cuda_status(launch_route(*cfg, x, Wg, bg, idx, w, counts, balance_loss, logits, (cudaStream_t)stream));
+    if (cfg->noise_std > 0.f && cfg->T > 0 && !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({x, Wg, ws})) return MOE_ERR_INVALID_ARG;
+    float* noise = nullptr;
+    if (ws) {
+        BackwardScratch b;
+        carve_backward(*cfg, ws, &b);
+        noise = b.noise;
+    }
+    return cuda_status(launch_route(*cfg, x, Wg, bg, idx, w, counts, balance_loss, logits, noise,
+                                    (cudaStream_t)stream));
 }
 
 moe_status_t moe_soft_balance(const moe_config_t* cfg, const float* logits, float weight, float* P,
@@ -219,6 +238,7 @@ moe_status_t moe_soft_balance(const moe_config_t* cfg, const float* logits, floa
     moe_status_t st = check_config(cfg);
     if (st != MOE_OK) return st;
     if (!P || !ws || (cfg->T > 0 && !logits) || !std::isfinite(weight)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({ws})) return MOE_ERR_INVALID_ARG;
     BackwardScratch b;
     carve_backward(*cfg, ws, &b);
     return cuda_status(launch_soft_balance(*cfg, logits, weight, P, loss, b.soft, (cudaStream_t)stream));
@@ -231,6 +251,7 @@ moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const float* log
     if (st != MOE_OK) return st;
     if (!P || !Wg || !dWg || !ws || !std::isfinite(weight)) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!logits || !x || !dx)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({x, Wg, dx, ws})) return MOE_ERR_INVALID_ARG;
     BackwardScratch b;
     carve_backward(*cfg, ws, &b);
     return cuda_status(launch_soft_balance_bwd(*cfg, logits, P, weight, x, Wg, dx, dWg, dbg, b.soft,
@@ -245,6 +266,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const voi
     if (!kept || !offsets || !n_dropped || !ws) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({x, Xp, ws})) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (dense_routing(*cfg)) {
         MOE_TRY(launch_dense_layout(*cfg, idx, kept, offsets, row_token, slot_row, n_dropped, s));
@@ -266,6 +288,7 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* Xp, const int32
     if (st != MOE_OK) return st;
     if (!offsets || !W1 || !b1 || !W2 || !b2) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!Xp || !Gp || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({Xp, W1, b1, W2, b2, Gp, H, Yp})) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity == 0) return MOE_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const moe_config_t& c = *cfg;
@@ -287,6 +310,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* Yp, const int32_t*
     moe_status_t st = check_config(cfg);
     if (st != MOE_OK) return st;
     if (cfg->T > 0 && (!Yp || !slot_row || !w || !y)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({Yp, y})) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_combine(*cfg, Yp, slot_row, w, y, (cudaStream_t)stream));
 }
 
@@ -303,6 +327,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
         return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!dy || !x || !idx || !w || !slot_row || !dx)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp || !Gp || !H || !Yp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({dy, x, Wg, Xp, Gp, H, Yp, W1, W2, dx, dW1, dW2, ws})) return MOE_ERR_INVALID_ARG;
     const moe_config_t& c = *cfg;
     cudaStream_t s = (cudaStream_t)stream;
     BackwardScratch b;

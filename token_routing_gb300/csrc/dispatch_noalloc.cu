@@ -55,6 +55,7 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
     if (!kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(Xp)) & 15u) != 0) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (dense_routing(*cfg)) {
         // closed-form layout: no scratch, no size limit

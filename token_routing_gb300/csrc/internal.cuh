@@ -43,14 +43,17 @@ struct WgradArgs {
 };
 
 // router.cu
+// noise: scratch [E, T] for the routing noise (needed when c.noise_std > 0 on the tensor-core
+// path; drawn there once per call by a full-occupancy kernel)
 cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
                          int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
-                         cudaStream_t s);
+                         float* noise, cudaStream_t s);
 
 // router_tc.cu: gate GEMM on tcgen05 + top-k + softmax + counts (bf16, d % 64 == 0)
 bool tc_route_supported(const moe_config_t& c);
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                            int32_t* idx, float* w, int32_t* counts, float* logits, cudaStream_t s);
+                            int32_t* idx, float* w, int32_t* counts, float* logits, const float* noise,
+                            cudaStream_t s);
 
 // dispatch.cu: stable counting sort of the assignments by expert
 struct SortScratch {

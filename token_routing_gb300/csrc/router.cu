@@ -163,6 +163,16 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
     }
 }
 
+// noise[e, t] = N(0,1) normal of (token t, expert e), expert-major so that the router's
+// lanes (consecutive tokens) read consecutive addresses.
+__global__ void __launch_bounds__(256)
+noise_kernel(int Tn, int E, uint32_t seed, float* __restrict__ noise) {
+    pdl_wait();
+    const long long n = (long long)Tn * E;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        noise[i] = routing_noise((int)(i % Tn), (int)(i / Tn), seed);
+}
+
 // balance_loss = mean over experts of (counts[e] - T*k/E)^2, in double. With dense routing
 // (dense_T >= 0) every expert's count is first set to dense_T, the number of tokens.
 __global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double mean, int dense_T,
@@ -184,11 +194,20 @@ __global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double 
 
 cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
                          int32_t* idx, float* w, int32_t* counts, float* balance_loss, float* logits,
-                         cudaStream_t s) {
+                         float* noise, cudaStream_t s) {
     cudaError_t st = launch_fill(counts, (long long)c.E, (int32_t)0, s);
     if (st != cudaSuccess) return st;
     if (c.T > 0 && tc_route_supported(c)) {
-        st = launch_route_tc(c, x, Wg, bg, idx, w, counts, logits, s);
+        const bool noisy = c.noise_std > 0.f;
+        if (noisy) {
+            if (!noise) return cudaErrorInvalidValue;
+            const long long n = (long long)c.T * c.E;
+            const int grid = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 16);
+            st = launch_pdl(noise_kernel, dim3(grid), dim3(256), 0, s, c.T, c.E, c.noise_seed, noise);
+            count_launch();
+            if (st != cudaSuccess) return st;
+        }
+        st = launch_route_tc(c, x, Wg, bg, idx, w, counts, logits, noisy ? noise : nullptr, s);
         if (st != cudaSuccess) return st;
     } else if (c.T > 0) {
         const size_t smem = sizeof(float) * ((size_t)kRouteTok * (kRouteKc + 1) +

@@ -37,6 +37,7 @@ struct RouteTcParams {
     float* w;
     int32_t* counts;
     float* logits;   // [T, E] or null
+    const float* noise;   // [E, T] N(0,1) draws, or null (no noise)
     int* err;
 };
 
@@ -147,7 +148,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
                 const bool live = tok < p.T;
-                if (p.noise_std > 0.f) {
+                if (p.noise) {
                     float* wr = p.w + (size_t)(live ? tok : 0) * p.E;
                     float m = -INFINITY;
                     for (int c = 0; c < p.E_pad; c += 32) {   // warp-uniform TMEM loads
@@ -158,7 +159,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                         for (int i = 0; i < 32; ++i) {
                             const int e = c + i;
                             if (e < p.E && live) {
-                                const float v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed),
+                                const float v = fmaf(p.noise_std, p.noise[(size_t)e * p.T + tok],
                                                      __uint_as_float(r[i]) + s_bias[e]);
                                 if (p.logits) p.logits[(size_t)tok * p.E + e] = v;
                                 wr[e] = v;
@@ -219,7 +220,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     int e = c + i;
                     if (e < p.E) {
                         float v = __uint_as_float(r[i]) + s_bias[e];
-                        if (p.noise_std > 0.f) v = fmaf(p.noise_std, routing_noise(tok, e, p.noise_seed), v);
+                        if (p.noise && tok < p.T) v = fmaf(p.noise_std, p.noise[(size_t)e * p.T + tok], v);
                         if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
                         // insert into the list sorted by (logit desc, id asc); experts arrive in
                         // ascending id, so an equal logit never displaces an earlier one
@@ -277,7 +278,8 @@ cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtens
 bool tc_route_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && c.d % 64 == 0; }
 
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg, const float* bg,
-                            int32_t* idx, float* w, int32_t* counts, float* logits, cudaStream_t s) {
+                            int32_t* idx, float* w, int32_t* counts, float* logits, const float* noise,
+                            cudaStream_t s) {
     RouteTcParams p{};
     p.T = c.T; p.d = c.d; p.E = c.E;
     p.E_pad = (c.E + 31) / 32 * 32;
@@ -286,6 +288,7 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.noise_seed = c.noise_seed;
     p.bg = c.has_gate_bias ? bg : nullptr;
     p.idx = idx; p.w = w; p.counts = counts; p.logits = logits;
+    p.noise = noise;
     p.err = device_error_word();
     p.rows = (long long)c.T >= (long long)RBM * num_sms() ? RBM : 64;
     CUtensorMap tx, tw;
