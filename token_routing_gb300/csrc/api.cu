@@ -369,17 +369,25 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;
     gx.sBe = (long long)c.d_ff * c.d; gx.sBn = 1; gx.sBk = c.d;
     MOE_TRY(row_gemm(c, gx, s));
-    // router backward: softmax Jacobian, dx, then dWg and dbg (sparse dz: from an assignment
-    // sort by expert; dense routing: dz is [T, E] and dWg = dz^T x directly)
+    // router backward: softmax Jacobian, dx and (block 0) the reported loss, then dWg and dbg.
+    // dz^T x: dense routing has dz as [T, E] already; with few experts (E <= 32) the router
+    // backward also writes dz as dense rows and the tiled dz^T x kernels take them; otherwise
+    // the assignments are sorted by expert and each expert's segment is summed.
+    float* dbg_out = c.has_gate_bias ? dbg : nullptr;
     if (dense_routing(c)) {
-        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
-        MOE_TRY(launch_dense_dwg(c, b.dz, x, dWg, c.has_gate_bias ? dbg : nullptr, false, b.soft, s));
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, nullptr, b.lossblk,
+                                  balance_loss, loss, s));
+        MOE_TRY(launch_dense_dwg(c, b.dz, x, dWg, dbg_out, false, b.soft, s));
+    } else if (c.E <= 32) {
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, b.soft.dz, b.lossblk,
+                                  balance_loss, loss, s));
+        MOE_TRY(launch_dense_dwg(c, b.soft.dz, x, dWg, dbg_out, false, b.soft, s));
     } else {
         MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
-        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, s));
-        MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, c.has_gate_bias ? dbg : nullptr, s));
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, nullptr, b.lossblk,
+                                  balance_loss, loss, s));
+        MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, dbg_out, s));
     }
-    if (loss) MOE_TRY(launch_loss(c, b.lossblk, balance_loss, loss, s));
     // join
     MOE_TRY(cudaEventRecord(ev.c, side));
     MOE_TRY(cudaStreamWaitEvent(s, ev.c, 0));

@@ -166,6 +166,29 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
     }
 }
 
+// loss = sum of the combine-backward block partials (fixed order) + aux * balance_loss, by
+// the 256 threads of one block (every thread of the block must call it).
+struct LossArgs {
+    const float* lossblk;
+    int nblk;
+    const float* balance;
+    float aux;
+    float* loss;     // null: no loss
+};
+__device__ __forceinline__ void block_loss(const LossArgs& la) {
+    __shared__ float red[8];
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < la.nblk; i += blockDim.x) acc += la.lossblk[i];
+    acc = warp_sum(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int i = 0; i < 8; ++i) t += (double)red[i];
+        *la.loss = (float)(t + (la.balance ? (double)la.aux * (double)*la.balance : 0.0));
+    }
+}
+
 // Router backward + un-permute, one warp per token:
 //   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature          (softmax Jacobian)
 //   dx[t] = sum_{kept j} dXp[slot_row[t,j]] + sum_j dz_j Wg[idx[t,j]]
@@ -174,7 +197,8 @@ __global__ void __launch_bounds__(256)
 router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                   const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
-                  int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+                  int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx,
+                  float* __restrict__ dz_dense, LossArgs la) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -200,6 +224,14 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
             for (int j = 0; j < MOE_MAX_K; ++j)
                 if (j == lane) mine = dzj[j];
             dz[(size_t)t * k + lane] = mine;
+        }
+        if (dz_dense && lane < E) {
+            // E <= 32: lane e writes expert e's entry of the dense [T, E] row (0 if unselected)
+            float v = 0.f;
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_K; ++j)
+                if (j < k && ex[j] == lane) v = dzj[j];
+            dz_dense[(size_t)t * E + lane] = v;
         }
         if ((d % V) == 0) {
             for (int c = lane * V; c < d; c += 32 * V) {
@@ -233,6 +265,7 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
             }
         }
     }
+    if (blockIdx.x == 0 && la.loss) block_loss(la);   // whole block 0, after its tokens
 }
 
 // Router backward + un-permute for k > MOE_MAX_K (dense routing, k = E): one warp per token,
@@ -244,7 +277,7 @@ __global__ void __launch_bounds__(256)
 router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                        const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                        const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
-                       int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx) {
+                       int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx, LossArgs la) {
     pdl_wait();
     __shared__ float s_dz[8][MOE_MAX_EXPERTS];
     __shared__ int s_row[8][MOE_MAX_EXPERTS];
@@ -319,6 +352,7 @@ router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw
         }
         __syncwarp();
     }
+    if (blockIdx.x == 0 && la.loss) block_loss(la);   // whole block 0, after its tokens
 }
 
 // dWg partials: block (e, chunk) sums dz[a] * x[token(a)] over a contiguous piece of expert
@@ -537,27 +571,31 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
 
 cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg,
-                              const void* dXp, float* dz, void* dx, cudaStream_t s) {
-    if (c.T == 0) return cudaSuccess;
+                              const void* dXp, float* dz, void* dx, float* dz_dense,
+                              const float* lossblk, const float* balance_loss, float* loss, cudaStream_t s) {
+    LossArgs la{lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss};
+    if (c.T == 0) {
+        if (loss) return launch_loss(c, lossblk, balance_loss, loss, s);
+        return cudaSuccess;
+    }
     const int grid = warp_grid(c.T);
     const float inv_temp = 1.0f / c.temperature;
     if (c.k > MOE_MAX_K) {
         if (c.dtype == MOE_BF16)
-            launch_pdl(router_bwd_wide_kernel<__nv_bfloat16>, grid, 256, 0, s, 
-                w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
-                c.E, inv_temp, dz, (__nv_bfloat16*)dx);
+            launch_pdl(router_bwd_wide_kernel<__nv_bfloat16>, grid, 256, 0, s, w, dw, idx, slot_row,
+                       (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz,
+                       (__nv_bfloat16*)dx, la);
         else
             launch_pdl(router_bwd_wide_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
-                                                               (const float*)dXp, c.T, c.d, c.k, c.E,
-                                                               inv_temp, dz, (float*)dx);
-    } else if (c.dtype == MOE_BF16)
-        launch_pdl(router_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
-            w, dw, idx, slot_row, (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k,
-            c.E, inv_temp, dz, (__nv_bfloat16*)dx);
-    else
+                       (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, la);
+    } else if (c.dtype == MOE_BF16) {
+        launch_pdl(router_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, w, dw, idx, slot_row,
+                   (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz,
+                   (__nv_bfloat16*)dx, dz_dense, la);
+    } else {
         launch_pdl(router_bwd_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
-                                                      (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp,
-                                                      dz, (float*)dx);
+                   (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, dz_dense, la);
+    }
     count_launch();
     return cudaGetLastError();
 }
