@@ -111,7 +111,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<KIND>()
 tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1) {
-    constexpr bool WGRAD = (KIND == kGemmWgrad);
+    constexpr bool WGRAD = (KIND == kGemmWgrad || KIND == kGemmWgradF32);
+    constexpr bool AUX = (KIND == kGemmDH || KIND == kGemmAccum);   // side input read per chunk
     constexpr int P_STAGES = pair_stages<KIND>();
     constexpr int PE_THREADS = 32 * pair_epi_warps<KIND>();
     constexpr int COLS = BN / (pair_epi_warps<KIND>() / 4);   // accumulator columns per epilogue warp
@@ -256,7 +257,15 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             t.m0 = pt.m0 + (int)rank * P_HALF;  // this CTA's rows
             const int row_in_tile = quarter * 32 + lane;
             if (t.kblocks == 0) {
-                if (WGRAD) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
+                if (KIND == kGemmWgrad) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
+                if (KIND == kGemmWgradF32) {
+                    const int m = t.m0 + row_in_tile;
+                    for (int c = c_lo; c < c_lo + COLS && m < p.M; c += 32)
+                        for (int i = 0; i < 32; i += 4)
+                            if (t.n0 + c + i < p.N)
+                                *reinterpret_cast<float4*>(p.outf + ((size_t)t.e * p.M + m) * p.N + t.n0 + c + i) =
+                                    make_float4(0.f, 0.f, 0.f, 0.f);
+                }
                 continue;
             }
             const int buf = tl & 1;
@@ -268,10 +277,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             Raw32 next;
             if (t.n0 + c_lo < p.N) {
                 if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
-                if (KIND == kGemmDH)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + t.n0 + c_lo + (lane & 3) * 8));
+                if (AUX) load_aux32<KIND>(next, p, aux_row0, t.n0 + c_lo, lane);
             }
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
@@ -285,10 +291,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                 const Raw32 cur = next;
                 const bool more = c + 32 < c_lo + COLS && n + 32 < p.N;
                 if (more && has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + n + 32);
-                if (more && KIND == kGemmDH)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        next.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + (aux_row0 + 8 * i) * p.N + n + 32 + (lane & 3) * 8));
+                if (more && AUX) load_aux32<KIND>(next, p, aux_row0, n + 32, lane);
                 if (!PREFETCH) tmem_ld32(taddr + c, acc);
                 tmem_ld_wait_regs(acc);
                 float v[32];
@@ -296,7 +299,17 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
                 if (PREFETCH && more) tmem_ld32(taddr + c + 32, acc);
                 const int y = t.m0 + quarter * 32;
-                if (KIND == kGemmWgrad) {
+                if (KIND == kGemmWgradF32) {
+                    // each lane writes its row's 32 fp32 values (128 contiguous bytes)
+                    const int m = y + lane;
+                    if (m < p.M) {
+                        float* dst = p.outf + ((size_t)t.e * p.M + m) * p.N + n;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            if (n + i < p.N)
+                                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    }
+                } else if (KIND == kGemmWgrad) {
                     const uint32_t b = st.acquire(lane);
                     if (y < p.M) st.store(lane, b, v, &tmO0, n, t.e * p.M + y);
                 } else if (KIND == kGemmFfn1 || KIND == kGemmFfn2) {
@@ -312,7 +325,9 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                         const uint32_t b = st.acquire(lane);
                         st.store(lane, b, v, &tmO0, n, y);
                     }
-                } else if (KIND == kGemmDH) {
+                } else if (AUX) {
+                    // the side input arrived coalesced (lane l: rows (l>>2)+8i, 16-byte segment
+                    // l&3); the staging buffer turns it into this lane's row
                     const uint32_t b = st.acquire(lane);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) sts128(sw64_addr(b, (lane >> 2) + 8 * i, lane & 3), cur.q[i]);
@@ -321,10 +336,15 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                     for (int j = 0; j < 4; ++j) unpack8(lds128(sw64_addr(b, lane, j)), a + 8 * j);
                     __syncwarp();
+                    if (KIND == kGemmDH) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= a[i];  // a = GELU'(A) saved by the forward
+                        for (int i = 0; i < 32; ++i) v[i] *= a[i];  // a = GELU'(A) saved by the forward
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += a[i];  // accumulate into aux (= out0)
+                    }
                     st.store(lane, b, v, &tmO0, n, y);
-                    if (p.colsum) {
+                    if (KIND == kGemmDH && p.colsum) {
                         const float sum = warp_colsum32(v, lane);
                         p.colsum[((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n + lane] = sum;
                     }
@@ -377,11 +397,12 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorM
 
 cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
     if (a.rows_capacity == 0) return cudaSuccess;
-    if (c.row_align % P_BM != 0) return cudaErrorInvalidValue;  // 256-row tiles need 256-row buckets
+    if (a.rows_capacity % P_BM != 0) return cudaErrorInvalidValue;  // 256-row tiles need 256-row buckets
     TcParams p{};
     p.kind = a.kind;
     p.offsets = a.offsets;
-    p.E = a.E; p.N = a.N; p.K = a.K; p.M = 0;
+    const int rows_valid = a.rows_valid > 0 ? a.rows_valid : a.rows_capacity;
+    p.E = a.E; p.N = a.N; p.K = a.K; p.M = rows_valid;
     p.n_tiles = ceil_div(a.N, BN);
     p.m_tiles = a.rows_capacity / P_BM;
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
@@ -400,7 +421,8 @@ cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a,
         // B(n, k) = W[e*K + k][n], N-major: boxes of 64 n x 64 k
         if (!make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.E * a.K, BK)) return cudaErrorInvalidValue;
     }
-    if (!make_map_ex(&to0, a.out0, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    // stores to rows that do not exist (rows_valid < rows_capacity) fall outside the map
+    if (!make_map_ex(&to0, a.out0, (uint64_t)a.N, (uint64_t)rows_valid, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (a.kind == kGemmFfn1) {
         if (!make_map_ex(&to1, a.out1, (uint64_t)a.N, (uint64_t)a.rows_capacity, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -415,27 +437,34 @@ cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a,
         case kGemmFfn2: return launch_pair<kGemmFfn2, false, false>(p, ta, tb, to0, to1, clusters, s);
         case kGemmDH: return launch_pair<kGemmDH, false, true>(p, ta, tb, to0, to1, clusters, s);
         case kGemmDX: return launch_pair<kGemmDX, false, true>(p, ta, tb, to0, to1, clusters, s);
+        case kGemmAccum: return launch_pair<kGemmAccum, false, true>(p, ta, tb, to0, to1, clusters, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
     TcParams p{};
-    p.kind = kGemmWgrad;
+    p.kind = a.f32 ? kGemmWgradF32 : kGemmWgrad;
     p.offsets = a.offsets;
     p.E = a.E; p.N = a.N; p.M = a.M; p.K = 0;
     p.n_tiles = ceil_div(a.N, BN);
     p.m_tiles = ceil_div(a.M, P_BM);
-    p.out0 = static_cast<__nv_bfloat16*>(a.C);
+    p.out0 = a.f32 ? nullptr : static_cast<__nv_bfloat16*>(a.C);
+    p.outf = a.f32 ? static_cast<float*>(a.C) : nullptr;
     p.err = device_error_word();
     CUtensorMap ta, tb, to0;
-    const uint64_t rows = (uint64_t)std::max(c.rows_capacity, 1);
-    if (!make_map(&ta, a.P, (uint64_t)a.M, rows, BK)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, a.Q, (uint64_t)a.N, rows, BK)) return cudaErrorInvalidValue;
-    if (!make_map_ex(&to0, a.C, (uint64_t)a.N, (uint64_t)a.E * a.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint64_t rows_p = (uint64_t)std::max(a.rows_p > 0 ? a.rows_p : c.rows_capacity, 1);
+    const uint64_t rows_q = (uint64_t)std::max(a.rows_q > 0 ? a.rows_q : c.rows_capacity, 1);
+    if (!make_map(&ta, a.P, (uint64_t)a.M, rows_p, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, a.Q, (uint64_t)a.N, rows_q, BK)) return cudaErrorInvalidValue;
+    if (a.f32) {
+        to0 = ta;   // unused: the fp32 epilogue writes from registers
+    } else if (!make_map_ex(&to0, a.C, (uint64_t)a.N, (uint64_t)a.E * a.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) {
         return cudaErrorInvalidValue;
+    }
     const long long tiles = (long long)a.E * p.m_tiles * p.n_tiles;
     const int clusters = (int)std::max(1LL, std::min<long long>(tiles, num_sms() / 2));
+    if (a.f32) return launch_pair<kGemmWgradF32, true, true>(p, ta, tb, to0, to0, clusters, s);
     return launch_pair<kGemmWgrad, true, true>(p, ta, tb, to0, to0, clusters, s);
 }
 

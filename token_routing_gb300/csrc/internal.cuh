@@ -17,6 +17,8 @@ enum GemmKind : int {
     kGemmDH = 2,     // dA = (dYp W2_e) * Gp
     kGemmDX = 3,     // dXp = dA W1_e
     kGemmWgrad = 4,  // dW_e = P_e^T Q_e over the rows of bucket e (dW2: P=dYp,Q=H; dW1: P=dA,Q=Xp)
+    kGemmAccum = 5,  // out = aux + A B (in place on aux: dx += dz Wg of the soft balance loss)
+    kGemmWgradF32 = 6,  // as kGemmWgrad with an fp32 output written from registers (split-K partials)
 };
 
 struct RowGemmArgs {
@@ -32,6 +34,7 @@ struct RowGemmArgs {
     int E, N, K;
     int rows_capacity;
     long long sBe, sBn, sBk; // element strides of B: expert, output column, reduction index
+    int rows_valid = 0;      // rows of out0/aux that exist (0: rows_capacity); kGemmAccum
 };
 
 struct WgradArgs {
@@ -40,6 +43,8 @@ struct WgradArgs {
     void* C;                // [E, M, N]
     const int32_t* offsets;
     int E, M, N;
+    int rows_p = 0, rows_q = 0;   // rows of P and Q (0: cfg.rows_capacity)
+    bool f32 = false;             // C is fp32 [E, M, N] (kGemmWgradF32)
 };
 
 // router.cu
@@ -94,12 +99,21 @@ struct SoftScratch {
     float* part;     // [chunks, E] per-chunk soft loads
     float* dz;       // [T, E] gradient of the logits
     float* dwg_part; // [splits, E, d]
+    // tensor-core contractions (bf16, d % 64 == 0): dz split into bf16 hi and lo parts
+    void* dzs;       // [T_pad, K2] bf16: columns [0,E) hi, [E8, E8+E) lo, zero elsewhere
+    void* wge;       // [K2, d] bf16: Wg in rows [0,E) and [E8, E8+E), zero elsewhere
+    int32_t* offs;   // [splits + 1] token buckets of the dz^T x split-K, then [0, T_pad]
+    float* wpart;    // [splits, K2, d] fp32 split-K partials of dzs^T x
+    float* dbg_part; // [blocks, E] partial column sums of dz
 };
 int soft_chunks(const moe_config_t& c);
 int soft_splits(const moe_config_t& c);
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s);
 cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, float weight, float* P,
                                 float* loss, const SoftScratch& s, cudaStream_t st);
+// dz^T x and dz Wg on tcgen05 (bf16 layers with d % 64 == 0 and E >= 32).
+bool soft_tc_ok(const moe_config_t& c);
+
 // dWg (+)= dz^T x and dbg (+)= column sums of dz for a dense dz [T, E] (split-K partials in
 // s.dwg_part, fixed-order reductions); accumulate = false overwrites dWg and dbg.
 cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void* x, float* dWg, float* dbg,

@@ -551,6 +551,106 @@ soft_dwg_reduce_kernel(const float* __restrict__ part, int E, int d, int splits,
     }
 }
 
+// ---------------------------------------------------------------- tensor-core contractions
+// dz is fp32; the tcgen05 GEMMs take bf16. Each value is split into hi = bf16(dz) and
+// lo = bf16(dz - hi), so hi + lo carries about 16 significant bits, and
+//   dz Wg  = [hi | lo] [Wg ; Wg]        (K = 2 E, padded)
+//   dz^T x = hi^T x + lo^T x            (rows E8 + e of the product hold lo^T x)
+// with every product of bf16 values exact in the fp32 accumulators.
+constexpr int kSplitThreads = 256;
+
+__host__ __device__ inline int e8_of(int E) { return (E + 7) / 8 * 8; }
+__host__ __device__ inline int k2_of(int E) { return (2 * e8_of(E) + 63) / 64 * 64; }
+
+// dzs[t, :] = hi / lo layout of dz[t, :] for t < T, zero rows for T <= t < T_pad (one warp per
+// row, grid-stride). Column sums of dz over the block's rows go to dbg_part[block, :] (warps
+// in order, rows in grid-stride order). Block 0 also writes the bucket offsets.
+__global__ void __launch_bounds__(kSplitThreads)
+soft_split_kernel(const float* __restrict__ dz, int Tn, int Tpad, int E, __nv_bfloat16* __restrict__ dzs,
+                  float* __restrict__ dbg_part, int32_t* __restrict__ offs, int splits, int bucket) {
+    pdl_wait();
+    __shared__ float s_sum[kSplitThreads / 32][MOE_MAX_EXPERTS];
+    const int e8 = e8_of(E), k2 = k2_of(E);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= splits; i += blockDim.x) offs[i] = min(i * bucket, Tpad);
+        if (threadIdx.x == 0) { offs[splits + 1] = 0; offs[splits + 2] = Tpad; }
+    }
+    float acc[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tpad; t += nwarps) {
+        __nv_bfloat16* row = dzs + (size_t)t * k2;
+        for (int c = lane; c < k2; c += 32) {
+            float v = 0.f;
+            if (t < Tn) {
+                if (c < E) {
+                    v = __bfloat162float(__float2bfloat16_rn(dz[(size_t)t * E + c]));
+                } else if (c >= e8 && c < e8 + E) {
+                    const float z = dz[(size_t)t * E + c - e8];
+                    v = z - __bfloat162float(__float2bfloat16_rn(z));
+                }
+            }
+            row[c] = __float2bfloat16_rn(v);
+        }
+        if (t < Tn) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q)
+                if (lane + 32 * q < E) acc[q] += dz[(size_t)t * E + lane + 32 * q];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+        if (lane + 32 * q < E) s_sum[warp][lane + 32 * q] = acc[q];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSplitThreads / 32; ++w) v += s_sum[w][e];
+        dbg_part[(size_t)blockIdx.x * E + e] = v;
+    }
+}
+
+// wge[r, c] = Wg[r, c] for r < E, Wg[r - E8, c] for E8 <= r < E8 + E, 0 otherwise.
+__global__ void __launch_bounds__(256)
+soft_wge_kernel(const __nv_bfloat16* __restrict__ Wg, int E, int d, __nv_bfloat16* __restrict__ wge) {
+    pdl_wait();
+    const int e8 = e8_of(E), k2 = k2_of(E);
+    const long long n = (long long)k2 * d;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / d), c = (int)(i % d);
+        const int src = r < E ? r : (r >= e8 && r < e8 + E ? r - e8 : -1);
+        wge[i] = src >= 0 ? Wg[(size_t)src * d + c] : __float2bfloat16_rn(0.f);
+    }
+}
+
+// dWg[e, c] (+)= sum over splits (in order) of wpart[s, e, c] + wpart[s, E8 + e, c];
+// dbg[e] (+)= sum over blocks (in order) of dbg_part[b, e] (block x = 0, one warp per expert).
+__global__ void __launch_bounds__(256)
+soft_dwg_tc_reduce_kernel(const float* __restrict__ wpart, int splits, int E, int d, const float* __restrict__ dbg_part,
+                          int nblk, bool accumulate, float* __restrict__ dWg, float* __restrict__ dbg) {
+    pdl_wait();
+    const int e = blockIdx.y;
+    const int e8 = e8_of(E), k2 = k2_of(E);
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c < d) {
+        float v = 0.f;
+        for (int sp = 0; sp < splits; ++sp) {
+            const float* base = wpart + (size_t)sp * k2 * d;
+            v += base[(size_t)e * d + c] + base[(size_t)(e8 + e) * d + c];
+        }
+        dWg[(size_t)e * d + c] = accumulate ? dWg[(size_t)e * d + c] + v : v;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 32 && dbg) {
+        const int lane = threadIdx.x;
+        float a = 0.f;
+        for (int b = lane; b < nblk; b += 32) a += dbg_part[(size_t)b * E + e];
+        a = warp_sum(a);
+        if (lane == 0) dbg[e] = accumulate ? dbg[e] + a : a;
+    }
+}
+
 }  // namespace
 
 int soft_chunks(const moe_config_t& c) { return std::max(1, ceil_div(c.T, kSoftTok)); }
@@ -592,10 +692,92 @@ static size_t dwg_tiled_smem() {
     return (size_t)kTileStages * TS * (kTileCols * sizeof(T) + 16 * sizeof(float));
 }
 
+// Tensor cores from 32 experts up; below that the contractions are a few FMAs per loaded
+// element and the tiled CUDA-core kernels take as long with fewer launches (measured equal at
+// 8192 x 16).
+bool soft_tc_ok(const moe_config_t& c) { return c.dtype == MOE_BF16 && c.d % 64 == 0 && c.E >= 32; }
+
+// Geometry of the tensor-core contractions: tokens padded to the 256-row tiles, and the
+// token buckets (split-K) of dz^T x, sized so that about one round of CTA pairs is busy.
+struct SoftTc {
+    int tpad, k2, splits, bucket, nblk;
+};
+static SoftTc soft_tc_geom(const moe_config_t& c) {
+    SoftTc g;
+    g.tpad = std::max(256, (c.T + 255) / 256 * 256);
+    g.k2 = k2_of(c.E);
+    const long long tiles_per_split = (long long)ceil_div(g.k2, 256) * ceil_div(c.d, 256);
+    const int want = (int)std::max<long long>(1, (num_sms() / 2 + tiles_per_split - 1) / tiles_per_split);
+    const int max_splits = std::max(1, g.tpad / 256);   // buckets of at least 256 rows
+    g.splits = std::min(want, max_splits);
+    g.bucket = (ceil_div(g.tpad, g.splits) + 63) / 64 * 64;
+    g.splits = ceil_div(g.tpad, g.bucket);
+    g.nblk = std::max(1, std::min(ceil_div(g.tpad, kSplitThreads / 32), 2 * num_sms()));
+    return g;
+}
+
 void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
     s->part = ws.take<float>((size_t)soft_chunks(c) * c.E);
     s->dz = ws.take<float>((size_t)c.T * c.E + 1);
     s->dwg_part = ws.take<float>((size_t)soft_splits(c) * c.E * dwg_pitch(c));
+    if (soft_tc_ok(c)) {
+        const SoftTc g = soft_tc_geom(c);
+        s->dzs = ws.take<__nv_bfloat16>((size_t)g.tpad * g.k2);
+        s->wge = ws.take<__nv_bfloat16>((size_t)g.k2 * c.d);
+        s->offs = ws.take<int32_t>((size_t)g.splits + 3);
+        s->wpart = ws.take<float>((size_t)g.splits * g.k2 * c.d);
+        s->dbg_part = ws.take<float>((size_t)g.nblk * c.E);
+    } else {
+        s->dzs = s->wge = nullptr;
+        s->offs = nullptr;
+        s->wpart = s->dbg_part = nullptr;
+    }
+}
+
+// dz (fp32 [T, E]) -> hi/lo bf16 layout, dbg partials and bucket offsets.
+static cudaError_t launch_soft_split(const moe_config_t& c, const float* dz, const SoftScratch& s, cudaStream_t st) {
+    const SoftTc g = soft_tc_geom(c);
+    cudaError_t e = launch_pdl(soft_split_kernel, dim3(g.nblk), dim3(kSplitThreads), 0, st, dz, c.T, g.tpad, c.E,
+                               (__nv_bfloat16*)s.dzs, s.dbg_part, s.offs, g.splits, g.bucket);
+    count_launch();
+    return e;
+}
+
+// dWg (+)= dz^T x, dbg (+)= column sums of dz, from the split layout already in s.dzs.
+static cudaError_t launch_dzx_tc(const moe_config_t& c, const void* x, float* dWg, float* dbg, bool accumulate,
+                                 const SoftScratch& s, cudaStream_t st) {
+    const SoftTc g = soft_tc_geom(c);
+    WgradArgs wa{s.dzs, x, s.wpart, s.offs, g.splits, g.k2, c.d};
+    wa.rows_p = g.tpad;
+    wa.rows_q = std::max(c.T, 1);
+    wa.f32 = true;
+    cudaError_t e = launch_wgrad_tc_pair(c, wa, st);
+    if (e != cudaSuccess) return e;
+    dim3 gr(ceil_div(c.d, 256), c.E);
+    e = launch_pdl(soft_dwg_tc_reduce_kernel, gr, dim3(256), 0, st, (const float*)s.wpart, g.splits, c.E, c.d,
+                   (const float*)s.dbg_part, g.nblk, accumulate, dWg, dbg);
+    count_launch();
+    return e;
+}
+
+// dx += dz Wg from the split layout already in s.dzs.
+static cudaError_t launch_dzwg_tc(const moe_config_t& c, const void* Wg, void* dx, const SoftScratch& s,
+                                  cudaStream_t st) {
+    const SoftTc g = soft_tc_geom(c);
+    const long long n = (long long)g.k2 * c.d;
+    const int grid = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
+    cudaError_t e = launch_pdl(soft_wge_kernel, dim3(grid), dim3(256), 0, st, (const __nv_bfloat16*)Wg, c.E, c.d,
+                               (__nv_bfloat16*)s.wge);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    RowGemmArgs ra{};
+    ra.kind = kGemmAccum;
+    ra.A = s.dzs; ra.B = s.wge; ra.aux = dx; ra.out0 = dx;
+    ra.offsets = s.offs + g.splits + 1;   // one bucket [0, T_pad]
+    ra.E = 1; ra.N = c.d; ra.K = g.k2; ra.rows_capacity = g.tpad;
+    ra.sBe = 0; ra.sBn = 1; ra.sBk = c.d;
+    ra.rows_valid = c.T;
+    return launch_row_gemm_tc_pair(c, ra, st);
 }
 
 cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, float weight, float* P,
@@ -619,6 +801,17 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
                                     const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
     const float inv_temp = 1.0f / c.temperature;
+    if (soft_tc_ok(c)) {
+        // dz on CUDA cores, both contractions on the tensor cores
+        const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
+        cudaError_t e = launch_pdl(soft_dz_kernel, dim3(g0), dim3(kSoftThreads), 0, st, logits, P, c.T, c.E,
+                                   inv_temp, weight, s.dz);
+        count_launch();
+        if (e != cudaSuccess) return e;
+        if ((e = launch_soft_split(c, s.dz, s, st)) != cudaSuccess) return e;
+        if ((e = launch_dzwg_tc(c, Wg, dx, s, st)) != cudaSuccess) return e;
+        return launch_dzx_tc(c, x, dWg, dbg, true, s, st);
+    }
     if (tiled_ok(c, Wg, dx)) {
         const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
         launch_pdl(soft_dz_kernel, g0, kSoftThreads, 0, st, logits, P, c.T, c.E, inv_temp, weight, s.dz);
@@ -659,6 +852,11 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
 cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void* x, float* dWg, float* dbg,
                              bool accumulate, const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0 && accumulate) return cudaSuccess;
+    if (c.T > 0 && soft_tc_ok(c)) {
+        cudaError_t e = launch_soft_split(c, dz, s, st);
+        if (e != cudaSuccess) return e;
+        return launch_dzx_tc(c, x, dWg, dbg, accumulate, s, st);
+    }
     const int splits = soft_splits(c);
     const int pitch = dwg_pitch(c);
     if (c.T > 0 && tiled_ok(c, x, s.dwg_part)) {

@@ -30,12 +30,14 @@ constexpr int EPI_SMEM = EPI_WARPS * 2 * STG_BYTES;
 struct TcParams {
     int kind;                 // GemmKind
     const int32_t* offsets;   // [E+1] bucket starts
-    int E, N, K, M;           // row GEMMs: out [rows, N], K reduction; wgrad: C_e [M, N]
+    int E, N, K, M;           // row GEMMs: out [rows, N], K reduction (kGemmAccum: M = rows that
+                              // exist in aux/out); wgrad: C_e [M, N]
     int n_tiles, m_tiles;
     const __nv_bfloat16* bias;   // [E, N]
     const __nv_bfloat16* aux;    // [rows, N] (A of the forward, for dH)
     __nv_bfloat16* out0;
     __nv_bfloat16* out1;
+    float* outf;                 // kGemmWgradF32: fp32 [E, M, N]
     float* colsum;               // dH: per-(tile, lane quarter) column sums of dA, or null
     int* err;
 };
@@ -130,6 +132,19 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 
 template <int KIND>
 constexpr bool has_bias() { return KIND == kGemmFfn1 || KIND == kGemmFfn2; }
+
+// The side input (aux [rows, N] bf16) of one 32-row x 32-column chunk, read coalesced: lane l
+// loads the 16-byte segment l & 3 of rows aux_row0 + 8 i (aux_row0 = the warp's first row +
+// (l >> 2)). kGemmAccum reads zeros for rows at or beyond p.M (rows that do not exist).
+template <int KIND>
+__device__ __forceinline__ void load_aux32(Raw32& r, const TcParams& p, size_t aux_row0, int n, int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const size_t row = aux_row0 + 8 * i;
+        if (KIND == kGemmAccum && row >= (size_t)p.M) r.q[i] = make_uint4(0u, 0u, 0u, 0u);
+        else r.q[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + row * p.N + n + (lane & 3) * 8));
+    }
+}
 
 __device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int j) {
     return base + row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
