@@ -149,7 +149,7 @@ def kernel_launches():
 class StepGraph:
     """One training step of the layer (route, dispatch, expert_ffn, combine, backward)
     captured once into a CUDA graph and replayed; removes the per-launch host cost of the
-    step's ~26 kernels. The buffers in `b` and the tensors in `p`, `x`, `dy` are bound at
+    step's ~20 kernels. The buffers in `b` and the tensors in `p`, `x`, `dy` are bound at
     capture time: refill them in place between replays. Warm the step up eagerly before
     capturing (the first calls on a device resolve driver entry points)."""
 
