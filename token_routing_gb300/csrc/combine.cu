@@ -16,8 +16,9 @@ namespace moe {
 namespace {
 
 // y[t] = sum over kept slots of w[t,j] * Yp[slot_row[t,j]]; one warp per token. Slots are
-// taken in groups of MOE_MAX_K (one group unless k = E > MOE_MAX_K), in slot order.
-template <typename T>
+// taken in groups of G (one group unless k > G, i.e. dense routing), in slot order; G is the
+// smallest of 1, 2, 4, 8 that holds k, so that the registers (and occupancy) follow k.
+template <typename T, int G>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
                const float* __restrict__ w, int Tn, int d, int k, T* __restrict__ y) {
@@ -25,7 +26,6 @@ combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
-    constexpr int G = MOE_MAX_K;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
         int rows[G];
         float ws[G];
@@ -189,10 +189,10 @@ __device__ __forceinline__ void block_loss(const LossArgs& la) {
     }
 }
 
-// Router backward + un-permute, one warp per token:
+// Router backward + un-permute, one warp per token (KC >= k slots held in registers):
 //   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature          (softmax Jacobian)
 //   dx[t] = sum_{kept j} dXp[slot_row[t,j]] + sum_j dz_j Wg[idx[t,j]]
-template <typename T>
+template <typename T, int KC>
 __global__ void __launch_bounds__(256)
 router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
@@ -204,11 +204,11 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
-        float wj[MOE_MAX_K], dzj[MOE_MAX_K];
-        int rows[MOE_MAX_K], ex[MOE_MAX_K];
+        float wj[KC], dzj[KC];
+        int rows[KC], ex[KC];
         float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) {
+        for (int j = 0; j < KC; ++j) {
             wj[j] = (j < k) ? w[(size_t)t * k + j] : 0.f;
             dzj[j] = (j < k) ? dw[(size_t)t * k + j] : 0.f;
             rows[j] = (j < k) ? slot_row[(size_t)t * k + j] : -1;
@@ -217,11 +217,11 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
             s = fmaf(wj[j], dzj[j], s);
         }
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) dzj[j] = wj[j] * (dzj[j] - s) * inv_temp;
+        for (int j = 0; j < KC; ++j) dzj[j] = wj[j] * (dzj[j] - s) * inv_temp;
         if (lane < k) {
             float mine = 0.f;
 #pragma unroll
-            for (int j = 0; j < MOE_MAX_K; ++j)
+            for (int j = 0; j < KC; ++j)
                 if (j == lane) mine = dzj[j];
             dz[(size_t)t * k + lane] = mine;
         }
@@ -229,7 +229,7 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
             // E <= 32: lane e writes expert e's entry of the dense [T, E] row (0 if unselected)
             float v = 0.f;
 #pragma unroll
-            for (int j = 0; j < MOE_MAX_K; ++j)
+            for (int j = 0; j < KC; ++j)
                 if (j < k && ex[j] == lane) v = dzj[j];
             dz_dense[(size_t)t * E + lane] = v;
         }
@@ -239,7 +239,7 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
 #pragma unroll
                 for (int i = 0; i < V; ++i) acc[i] = 0.f;
 #pragma unroll
-                for (int j = 0; j < MOE_MAX_K; ++j) {
+                for (int j = 0; j < KC; ++j) {
                     if (j < k) {
                         float v[V];
                         if (rows[j] >= 0) {
@@ -532,16 +532,28 @@ int warp_grid(long long items, int warps_per_block = 8) {
 
 }  // namespace
 
+template <typename T, int G>
+static cudaError_t combine_g(const moe_config_t& c, const void* Yp, const int32_t* slot_row, const float* w,
+                             void* y, cudaStream_t s) {
+    const int grid = warp_grid(c.T);
+    return launch_pdl(combine_kernel<T, G>, grid, 256, 0, s, (const T*)Yp, slot_row, w, c.T, c.d, c.k, (T*)y);
+}
+template <typename T>
+static cudaError_t combine_t(const moe_config_t& c, const void* Yp, const int32_t* slot_row, const float* w,
+                             void* y, cudaStream_t s) {
+    if (c.k <= 1) return combine_g<T, 1>(c, Yp, slot_row, w, y, s);
+    if (c.k <= 2) return combine_g<T, 2>(c, Yp, slot_row, w, y, s);
+    if (c.k <= 4) return combine_g<T, 4>(c, Yp, slot_row, w, y, s);
+    return combine_g<T, 8>(c, Yp, slot_row, w, y, s);
+}
+
 cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t* slot_row,
                            const float* w, void* y, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    const int grid = warp_grid(c.T);
-    if (c.dtype == MOE_BF16)
-        launch_pdl(combine_kernel<__nv_bfloat16>, grid, 256, 0, s, (const __nv_bfloat16*)Yp, slot_row, w, c.T,
-                                                           c.d, c.k, (__nv_bfloat16*)y);
-    else
-        launch_pdl(combine_kernel<float>, grid, 256, 0, s, (const float*)Yp, slot_row, w, c.T, c.d, c.k, (float*)y);
+    cudaError_t e = c.dtype == MOE_BF16 ? combine_t<__nv_bfloat16>(c, Yp, slot_row, w, y, s)
+                                        : combine_t<float>(c, Yp, slot_row, w, y, s);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -569,6 +581,23 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
     return cudaGetLastError();
 }
 
+template <typename T, int KC>
+static void router_bwd_kc(const moe_config_t& c, int grid, float inv_temp, const float* w, const float* dw,
+                          const int32_t* idx, const int32_t* slot_row, const void* Wg, const void* dXp, float* dz,
+                          void* dx, float* dz_dense, const LossArgs& la, cudaStream_t s) {
+    launch_pdl(router_bwd_kernel<T, KC>, grid, 256, 0, s, w, dw, idx, slot_row, (const T*)Wg, (const T*)dXp, c.T, c.d,
+               c.k, c.E, inv_temp, dz, (T*)dx, dz_dense, la);
+}
+template <typename T>
+static void router_bwd_narrow(const moe_config_t& c, int grid, float inv_temp, const float* w, const float* dw,
+                              const int32_t* idx, const int32_t* slot_row, const void* Wg, const void* dXp, float* dz,
+                              void* dx, float* dz_dense, const LossArgs& la, cudaStream_t s) {
+    if (c.k <= 1) router_bwd_kc<T, 1>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+    else if (c.k <= 2) router_bwd_kc<T, 2>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+    else if (c.k <= 4) router_bwd_kc<T, 4>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+    else router_bwd_kc<T, 8>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+}
+
 cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg,
                               const void* dXp, float* dz, void* dx, float* dz_dense,
@@ -589,12 +618,9 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
             launch_pdl(router_bwd_wide_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
                        (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, la);
     } else if (c.dtype == MOE_BF16) {
-        launch_pdl(router_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, w, dw, idx, slot_row,
-                   (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz,
-                   (__nv_bfloat16*)dx, dz_dense, la);
+        router_bwd_narrow<__nv_bfloat16>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
     } else {
-        launch_pdl(router_bwd_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
-                   (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, dz_dense, la);
+        router_bwd_narrow<float>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
     }
     count_launch();
     return cudaGetLastError();
