@@ -143,18 +143,20 @@ cudaStream_t side_stream() {
 }
 
 // Fork/join events of one call; destroyed when the call returns (pending waits still hold).
-struct EventPair {
-    cudaEvent_t a = nullptr, b = nullptr, c = nullptr;
+struct EventSet {
+    cudaEvent_t a = nullptr, b = nullptr, c = nullptr, d = nullptr;
     bool ok = false;
-    EventPair() {
+    EventSet() {
         ok = cudaEventCreateWithFlags(&a, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&b, cudaEventDisableTiming) == cudaSuccess &&
-             cudaEventCreateWithFlags(&c, cudaEventDisableTiming) == cudaSuccess;
+             cudaEventCreateWithFlags(&c, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&d, cudaEventDisableTiming) == cudaSuccess;
     }
-    ~EventPair() {
+    ~EventSet() {
         if (a) cudaEventDestroy(a);
         if (b) cudaEventDestroy(b);
         if (c) cudaEventDestroy(c);
+        if (d) cudaEventDestroy(d);
     }
 };
 
@@ -334,19 +336,35 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     carve_backward(c, ws, &b);
     float* dwp = dw ? dw : b.dw;
 
-    // The backward is a small DAG. Main stream: combine backward -> dH -> dX -> router
-    // backward -> dWg -> loss. Side stream: dW2 and db2 (need dYp), then dW1 and db1 (need
-    // dA). The side branch forks and joins through events, which also works under stream
-    // capture; the branches write disjoint outputs, so results do not depend on the overlap.
+    // The backward is a small DAG.
+    //   main: combine backward -> dH -> dX -> un-permute (dx)
+    //   side: dz (softmax Jacobian) + loss -> dWg, dbg -> dW2, db2 -> [after dH] dW1, db1
+    // dz needs only the combine backward's dw, so where dz^T x runs on the tensor cores
+    // (bf16, more than 32 experts, or dense routing) dz and the gate-weight gradient run
+    // beside the expert GEMMs and only the un-permute follows dX. With 32 experts or fewer the
+    // CUDA-core dz^T x kernels would take SMs from dH (measured 2% slower that way): the
+    // router backward and dz^T x follow dX on the main stream, from dense dz rows. Otherwise
+    // (no tensor cores, more than 32 experts) the assignments are sorted by expert after dX.
+    // The branches fork and join through events, which also works under stream capture; they
+    // write disjoint outputs, so results do not depend on the overlap.
     cudaStream_t side = side_stream();
     if (!side) return MOE_ERR_CUDA;
-    EventPair ev;
+    EventSet ev;
     if (!ev.ok) return MOE_ERR_CUDA;
+    float* dbg_out = c.has_gate_bias ? dbg : nullptr;
+    const bool early_dz = dense_routing(c) || (c.dtype == MOE_BF16 && c.d % 64 == 0 && c.E > 32);
+    float* dz_dense = dense_routing(c) ? b.dz : b.soft.dz;
 
     // combine backward: dYp, dw, loss partials (padding rows of dYp zeroed)
     MOE_TRY(launch_combine_bwd(c, dy, Yp, w, offsets, row_token, slot_row, b.dYp, dwp, b.lossblk, s));
     MOE_TRY(cudaEventRecord(ev.a, s));
     MOE_TRY(cudaStreamWaitEvent(side, ev.a, 0));
+    if (early_dz) {
+        MOE_TRY(launch_router_dz(c, w, dwp, idx, b.dz, dense_routing(c) ? nullptr : dz_dense, b.lossblk,
+                                 balance_loss, loss, side));
+        MOE_TRY(cudaEventRecord(ev.d, side));
+        MOE_TRY(launch_dense_dwg(c, dz_dense, x, dWg, dbg_out, false, b.soft, side));
+    }
     WgradArgs w2{b.dYp, H, dW2, offsets, c.E, c.d, c.d_ff};
     MOE_TRY(wgrad(c, w2, side));
     MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, side));
@@ -369,23 +387,19 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;
     gx.sBe = (long long)c.d_ff * c.d; gx.sBn = 1; gx.sBk = c.d;
     MOE_TRY(row_gemm(c, gx, s));
-    // router backward: softmax Jacobian, dx and (block 0) the reported loss, then dWg and dbg.
-    // dz^T x: dense routing has dz as [T, E] already; with few experts (E <= 32) the router
-    // backward also writes dz as dense rows and the tiled dz^T x kernels take them; otherwise
-    // the assignments are sorted by expert and each expert's segment is summed.
-    float* dbg_out = c.has_gate_bias ? dbg : nullptr;
-    if (dense_routing(c)) {
-        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, nullptr, b.lossblk,
-                                  balance_loss, loss, s));
-        MOE_TRY(launch_dense_dwg(c, b.dz, x, dWg, dbg_out, false, b.soft, s));
+    if (early_dz) {
+        // un-permute: dx = sum over kept slots of dXp rows + dz Wg, with dz from the side branch
+        MOE_TRY(cudaStreamWaitEvent(s, ev.d, 0));
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, nullptr, nullptr, nullptr,
+                                  nullptr, true, s));
     } else if (c.E <= 32) {
-        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, b.soft.dz, b.lossblk,
-                                  balance_loss, loss, s));
-        MOE_TRY(launch_dense_dwg(c, b.soft.dz, x, dWg, dbg_out, false, b.soft, s));
+        MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, dz_dense, b.lossblk,
+                                  balance_loss, loss, false, s));
+        MOE_TRY(launch_dense_dwg(c, dz_dense, x, dWg, dbg_out, false, b.soft, s));
     } else {
         MOE_TRY(launch_sort(c, idx, b.sort, nullptr, nullptr, nullptr, nullptr, nullptr, s));
         MOE_TRY(launch_router_bwd(c, w, dwp, idx, slot_row, Wg, b.dXp, b.dz, dx, nullptr, b.lossblk,
-                                  balance_loss, loss, s));
+                                  balance_loss, loss, false, s));
         MOE_TRY(launch_dwg(c, x, b.dz, b.sort, b.dwg_part, dWg, dbg_out, s));
     }
     // join

@@ -189,6 +189,36 @@ __device__ __forceinline__ void block_loss(const LossArgs& la) {
     }
 }
 
+// The softmax Jacobian of the routing weights alone, one warp per token (any k):
+//   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature  -> dz [T, k]
+// and, when dz_dense is set (k <= MOE_MAX_K), dz as dense [T, E] rows (0 where unselected).
+// Block 0 then writes the reported loss. It needs only combine-backward outputs, so it runs
+// beside the expert GEMMs; the un-permute (dx) follows the dX GEMM.
+__global__ void __launch_bounds__(256)
+router_dz_kernel(const float* __restrict__ w, const float* __restrict__ dw, const int32_t* __restrict__ idx,
+                 int Tn, int k, int E, float inv_temp, float* __restrict__ dz, float* __restrict__ dz_dense,
+                 LossArgs la) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
+        const size_t base = (size_t)t * k;
+        float sp = 0.f;
+        for (int j = lane; j < k; j += 32) sp = fmaf(w[base + j], dw[base + j], sp);
+        const float s = warp_sum(sp);
+        for (int j = lane; j < k; j += 32) dz[base + j] = w[base + j] * (dw[base + j] - s) * inv_temp;
+        if (dz_dense) {
+            for (int e = lane; e < E; e += 32) {
+                float v = 0.f;
+                for (int j = 0; j < k; ++j)
+                    if (idx[base + j] == e) v = w[base + j] * (dw[base + j] - s) * inv_temp;
+                dz_dense[(size_t)t * E + e] = v;
+            }
+        }
+    }
+    if (blockIdx.x == 0 && la.loss) block_loss(la);   // whole block 0, after its tokens
+}
+
 // Router backward + un-permute, one warp per token (KC >= k slots held in registers):
 //   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature          (softmax Jacobian)
 //   dx[t] = sum_{kept j} dXp[slot_row[t,j]] + sum_j dz_j Wg[idx[t,j]]
@@ -198,7 +228,7 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                   const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
                   int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx,
-                  float* __restrict__ dz_dense, LossArgs la) {
+                  float* __restrict__ dz_dense, LossArgs la, bool dz_in) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -217,8 +247,9 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
             s = fmaf(wj[j], dzj[j], s);
         }
 #pragma unroll
-        for (int j = 0; j < KC; ++j) dzj[j] = wj[j] * (dzj[j] - s) * inv_temp;
-        if (lane < k) {
+        for (int j = 0; j < KC; ++j) dzj[j] = dz_in ? ((j < k) ? dz[(size_t)t * k + j] : 0.f)
+                                                   : wj[j] * (dzj[j] - s) * inv_temp;
+        if (lane < k && !dz_in) {
             float mine = 0.f;
 #pragma unroll
             for (int j = 0; j < KC; ++j)
@@ -277,7 +308,8 @@ __global__ void __launch_bounds__(256)
 router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                        const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                        const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
-                       int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx, LossArgs la) {
+                       int E, float inv_temp, float* __restrict__ dz, T* __restrict__ dx, LossArgs la,
+                       bool dz_in) {
     pdl_wait();
     __shared__ float s_dz[8][MOE_MAX_EXPERTS];
     __shared__ int s_row[8][MOE_MAX_EXPERTS];
@@ -291,9 +323,9 @@ router_bwd_wide_kernel(const float* __restrict__ w, const float* __restrict__ dw
         for (int j = lane; j < k; j += 32) s = fmaf(w[base + j], dw[base + j], s);
         s = warp_sum(s);
         for (int j = lane; j < k; j += 32) {
-            const float v = w[base + j] * (dw[base + j] - s) * inv_temp;
+            const float v = dz_in ? dz[base + j] : w[base + j] * (dw[base + j] - s) * inv_temp;
             s_dz[wid][j] = v;
-            dz[base + j] = v;
+            if (!dz_in) dz[base + j] = v;
             s_row[wid][j] = slot_row[base + j];
             s_ex[wid][j] = min(max(idx[base + j], 0), E - 1);
         }
@@ -584,24 +616,25 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
 template <typename T, int KC>
 static void router_bwd_kc(const moe_config_t& c, int grid, float inv_temp, const float* w, const float* dw,
                           const int32_t* idx, const int32_t* slot_row, const void* Wg, const void* dXp, float* dz,
-                          void* dx, float* dz_dense, const LossArgs& la, cudaStream_t s) {
+                          void* dx, float* dz_dense, const LossArgs& la, bool dz_in, cudaStream_t s) {
     launch_pdl(router_bwd_kernel<T, KC>, grid, 256, 0, s, w, dw, idx, slot_row, (const T*)Wg, (const T*)dXp, c.T, c.d,
-               c.k, c.E, inv_temp, dz, (T*)dx, dz_dense, la);
+               c.k, c.E, inv_temp, dz, (T*)dx, dz_dense, la, dz_in);
 }
 template <typename T>
 static void router_bwd_narrow(const moe_config_t& c, int grid, float inv_temp, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg, const void* dXp, float* dz,
-                              void* dx, float* dz_dense, const LossArgs& la, cudaStream_t s) {
-    if (c.k <= 1) router_bwd_kc<T, 1>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
-    else if (c.k <= 2) router_bwd_kc<T, 2>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
-    else if (c.k <= 4) router_bwd_kc<T, 4>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
-    else router_bwd_kc<T, 8>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+                              void* dx, float* dz_dense, const LossArgs& la, bool dz_in, cudaStream_t s) {
+    if (c.k <= 1) router_bwd_kc<T, 1>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, dz_in, s);
+    else if (c.k <= 2) router_bwd_kc<T, 2>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, dz_in, s);
+    else if (c.k <= 4) router_bwd_kc<T, 4>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, dz_in, s);
+    else router_bwd_kc<T, 8>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, dz_in, s);
 }
 
 cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg,
                               const void* dXp, float* dz, void* dx, float* dz_dense,
-                              const float* lossblk, const float* balance_loss, float* loss, cudaStream_t s) {
+                              const float* lossblk, const float* balance_loss, float* loss, bool dz_in,
+                              cudaStream_t s) {
     LossArgs la{lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss};
     if (c.T == 0) {
         if (loss) return launch_loss(c, lossblk, balance_loss, loss, s);
@@ -613,15 +646,30 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float
         if (c.dtype == MOE_BF16)
             launch_pdl(router_bwd_wide_kernel<__nv_bfloat16>, grid, 256, 0, s, w, dw, idx, slot_row,
                        (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz,
-                       (__nv_bfloat16*)dx, la);
+                       (__nv_bfloat16*)dx, la, dz_in);
         else
             launch_pdl(router_bwd_wide_kernel<float>, grid, 256, 0, s, w, dw, idx, slot_row, (const float*)Wg,
-                       (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, la);
+                       (const float*)dXp, c.T, c.d, c.k, c.E, inv_temp, dz, (float*)dx, la, dz_in);
     } else if (c.dtype == MOE_BF16) {
-        router_bwd_narrow<__nv_bfloat16>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+        router_bwd_narrow<__nv_bfloat16>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la,
+                                         dz_in, s);
     } else {
-        router_bwd_narrow<float>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, s);
+        router_bwd_narrow<float>(c, grid, inv_temp, w, dw, idx, slot_row, Wg, dXp, dz, dx, dz_dense, la, dz_in, s);
     }
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_dz(const moe_config_t& c, const float* w, const float* dw, const int32_t* idx,
+                             float* dz, float* dz_dense, const float* lossblk, const float* balance_loss,
+                             float* loss, cudaStream_t s) {
+    if (c.T == 0) {
+        if (loss) return launch_loss(c, lossblk, balance_loss, loss, s);
+        return cudaSuccess;
+    }
+    LossArgs la{lossblk, combine_bwd_blocks(c), balance_loss, c.aux_loss_weight, loss};
+    launch_pdl(router_dz_kernel, warp_grid(c.T), 256, 0, s, w, dw, idx, c.T, c.k, c.E, 1.0f / c.temperature, dz,
+               dz_dense, la);
     count_launch();
     return cudaGetLastError();
 }

@@ -135,10 +135,17 @@ cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void
 int combine_bwd_blocks(const moe_config_t& c);
 // Router backward + un-permute (dz, dx). dz_dense (nullable; k <= MOE_MAX_K and E <= 32): also
 // write dz as dense [T, E] rows. Block 0 also writes the reported loss when `loss` is set.
+// dz_in: take dz from `dz` (written by launch_router_dz) and compute dx only.
 cudaError_t launch_router_bwd(const moe_config_t& c, const float* w, const float* dw,
                               const int32_t* idx, const int32_t* slot_row, const void* Wg,
                               const void* dXp, float* dz, void* dx, float* dz_dense,
-                              const float* lossblk, const float* balance_loss, float* loss, cudaStream_t s);
+                              const float* lossblk, const float* balance_loss, float* loss, bool dz_in,
+                              cudaStream_t s);
+// The softmax Jacobian alone: dz [T, k], optionally dense [T, E] rows (k <= MOE_MAX_K), and
+// (block 0) the reported loss.
+cudaError_t launch_router_dz(const moe_config_t& c, const float* w, const float* dw, const int32_t* idx,
+                             float* dz, float* dz_dense, const float* lossblk, const float* balance_loss,
+                             float* loss, cudaStream_t s);
 int dwg_chunks(const moe_config_t& c);
 cudaError_t launch_dwg(const moe_config_t& c, const void* x, const float* dz,
                        const SortScratch& srt, float* part, float* dWg, float* dbg, cudaStream_t s);
