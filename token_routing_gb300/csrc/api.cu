@@ -278,7 +278,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const voi
         sort_scratch_take(w, *cfg, &srt);
         MOE_TRY(launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s));
     }
-    MOE_TRY(launch_gather(*cfg, x, offsets, row_token, Xp, s));
+    MOE_TRY(launch_gather(*cfg, x, offsets, row_token, slot_row, Xp, s));
     return MOE_OK;
 }
 

@@ -97,27 +97,22 @@ combine_kernel(const T* __restrict__ Yp, const int32_t* __restrict__ slot_row,
     }
 }
 
-// Row-parallel combine backward, one warp per bucket row r < offsets[E]:
-//   kept row of (t, j): dYp[r] = w[t,j] * dy[t], dw[t,j] = <dy[t], Yp[r]>, lossrow[r] = w*dw
-//   padding row:        dYp[r] = 0, lossrow[r] = 0
-// (dw of dropped slots is zeroed beforehand.) sum_r lossrow[r] = sum_t <y[t], dy[t]>.
+// Zero the padding rows (row_token = -1) of a bucket buffer M [rows, d], rows < offsets[E]:
+// each warp takes 32 rows at a time, finds the padding ones with a ballot and clears them
+// together (coalesced 16-byte stores).
 template <typename T>
-__global__ void __launch_bounds__(256)
-combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
-                   const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
-                   const int32_t* __restrict__ slot_row, int d, int k, int rows_cap, bool dense,
-                   T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossblk) {
-    pdl_wait();
-    __shared__ float s_warp[8];
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    const int nrows = min(offsets[E], rows_cap);
+__device__ __forceinline__ void zero_padding_rows(const int32_t* __restrict__ offsets, int E,
+                                                  const int32_t* __restrict__ row_token, int d, int rows_cap,
+                                                  T* __restrict__ M, int gw, int nwarps, int lane) {
     constexpr int V = Vec16<T>::N;
-    float wloss = 0.f;  // this warp's sum of w * dw over its rows, in row order
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += nwarps) {
-        const int t = row_token[r];
-        T* out = dYp + (size_t)r * d;
-        if (t < 0) {
+    const int nrows = min(offsets[E], rows_cap);
+    for (int r0 = gw * 32; r0 < nrows; r0 += nwarps * 32) {
+        const int r = r0 + lane;
+        unsigned pad = __ballot_sync(0xffffffffu, r < nrows && row_token[r] < 0);
+        while (pad) {
+            const int b = __ffs(pad) - 1;
+            pad &= pad - 1;
+            T* out = M + (size_t)(r0 + b) * d;
             if ((d % V) == 0) {
                 float z[V];
 #pragma unroll
@@ -126,37 +121,75 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
             } else {
                 for (int c = lane; c < d; c += 32) st_f(out + c, 0.f);
             }
-            continue;
         }
-        int jj = 0;
-        if (dense) {
-            jj = r / offsets[1];   // dense routing: slot j = expert j, equal-size buckets
-        } else {
-            for (int j = 0; j < k; ++j)
-                if (slot_row[(size_t)t * k + j] == r) jj = j;
-        }
-        const float wv = w[(size_t)t * k + jj];
-        float dot = 0.f;
-        if ((d % V) == 0) {
-            for (int c = lane * V; c < d; c += 32 * V) {
-                float g[V], yv[V], o[V];
-                load16(dy + (size_t)t * d + c, g);
-                load16(Yp + (size_t)r * d + c, yv);
-#pragma unroll
-                for (int i = 0; i < V; ++i) { dot = fmaf(g[i], yv[i], dot); o[i] = wv * g[i]; }
-                store16(out + c, o);
-            }
-        } else {
-            for (int c = lane; c < d; c += 32) {
-                const float g = ld_f(dy + (size_t)t * d + c);
-                dot = fmaf(g, ld_f(Yp + (size_t)r * d + c), dot);
-                st_f(out + c, wv * g);
-            }
-        }
-        dot = warp_sum(dot);
-        if (lane == 0) dw[(size_t)t * k + jj] = dot;
-        wloss = fmaf(wv, dot, wloss);
     }
+}
+
+// Combine backward, one warp per token, slots in groups of G (as in the combine):
+//   kept slot j (row r):  dYp[r] = w[t,j] dy[t],  dw[t,j] = <dy[t], Yp[r]>
+//   dropped slot j:       dw[t,j] = 0
+// then the padding rows of dYp are zeroed. lossblk[block] = the block's sum of w * dw over
+// kept slots (warps in order; a warp's tokens in order), so sum(lossblk) = sum_t <y[t], dy[t]>.
+template <typename T, int G>
+__global__ void __launch_bounds__(256)
+combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
+                   const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
+                   const int32_t* __restrict__ slot_row, int Tn, int d, int k, int rows_cap,
+                   T* __restrict__ dYp, float* __restrict__ dw, float* __restrict__ lossblk) {
+    pdl_wait();
+    __shared__ float s_warp[8];
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    constexpr int V = Vec16<T>::N;
+    float wloss = 0.f;
+    for (int t = gw; t < Tn; t += nwarps) {
+        for (int j0 = 0; j0 < k; j0 += G) {
+            int rows[G];
+            float ws[G], dot[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const bool in = j0 + j < k;
+                rows[j] = in ? slot_row[(size_t)t * k + j0 + j] : -1;
+                ws[j] = in ? w[(size_t)t * k + j0 + j] : 0.f;
+                dot[j] = 0.f;
+            }
+            if ((d % V) == 0) {
+                for (int c = lane * V; c < d; c += 32 * V) {
+                    float g[V];
+                    load16(dy + (size_t)t * d + c, g);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        if (rows[j] < 0) continue;
+                        float yv[V], o[V];
+                        load16(Yp + (size_t)rows[j] * d + c, yv);
+#pragma unroll
+                        for (int i = 0; i < V; ++i) { dot[j] = fmaf(g[i], yv[i], dot[j]); o[i] = ws[j] * g[i]; }
+                        store16(dYp + (size_t)rows[j] * d + c, o);
+                    }
+                }
+            } else {
+                for (int c = lane; c < d; c += 32) {
+                    const float g = ld_f(dy + (size_t)t * d + c);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        if (rows[j] < 0) continue;
+                        dot[j] = fmaf(g, ld_f(Yp + (size_t)rows[j] * d + c), dot[j]);
+                        st_f(dYp + (size_t)rows[j] * d + c, ws[j] * g);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float v = warp_sum(dot[j]);
+                if (j0 + j < k) {
+                    if (lane == 0) dw[(size_t)t * k + j0 + j] = rows[j] >= 0 ? v : 0.f;
+                    if (rows[j] >= 0) wloss = fmaf(ws[j], v, wloss);
+                }
+            }
+        }
+    }
+    zero_padding_rows(offsets, E, row_token, d, rows_cap, dYp, gw, nwarps, lane);
     if (lane == 0) s_warp[threadIdx.x >> 5] = wloss;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -589,27 +622,34 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Yp, const int32_t*
     return cudaGetLastError();
 }
 
-int combine_bwd_blocks(const moe_config_t& c) { return warp_grid(std::max(c.rows_capacity, 1)); }
+int combine_bwd_blocks(const moe_config_t& c) { return warp_grid(std::max(c.T, 1)); }
+
+template <typename T, int G>
+static cudaError_t combine_bwd_g(const moe_config_t& c, const void* dy, const void* Yp, const float* w,
+                                 const int32_t* offsets, const int32_t* row_token, const int32_t* slot_row,
+                                 void* dYp, float* dw, float* lossblk, cudaStream_t s) {
+    return launch_pdl(combine_bwd_kernel<T, G>, combine_bwd_blocks(c), 256, 0, s, (const T*)dy, (const T*)Yp, w,
+                      offsets, c.E, row_token, slot_row, c.T, c.d, c.k, c.rows_capacity, (T*)dYp, dw, lossblk);
+}
+template <typename T>
+static cudaError_t combine_bwd_t(const moe_config_t& c, const void* dy, const void* Yp, const float* w,
+                                 const int32_t* offsets, const int32_t* row_token, const int32_t* slot_row,
+                                 void* dYp, float* dw, float* lossblk, cudaStream_t s) {
+    if (c.k <= 1) return combine_bwd_g<T, 1>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s);
+    if (c.k <= 2) return combine_bwd_g<T, 2>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s);
+    if (c.k <= 4) return combine_bwd_g<T, 4>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s);
+    return combine_bwd_g<T, 8>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s);
+}
 
 cudaError_t launch_combine_bwd(const moe_config_t& c, const void* dy, const void* Yp,
                                const float* w, const int32_t* offsets, const int32_t* row_token,
                                const int32_t* slot_row, void* dYp, float* dw, float* lossblk,
                                cudaStream_t s) {
-    if (c.T > 0) {
-        cudaError_t e = launch_fill(dw, (long long)c.T * c.k, 0.f, s);
-        if (e != cudaSuccess) return e;
-    }
-    const int grid = combine_bwd_blocks(c);
-    if (c.dtype == MOE_BF16)
-        launch_pdl(combine_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
-            (const __nv_bfloat16*)dy, (const __nv_bfloat16*)Yp, w, offsets, c.E, row_token, slot_row,
-            c.d, c.k, c.rows_capacity, dense_routing(c), (__nv_bfloat16*)dYp, dw, lossblk);
-    else
-        launch_pdl(combine_bwd_kernel<float>, grid, 256, 0, s, (const float*)dy, (const float*)Yp, w, offsets,
-                                                       c.E, row_token, slot_row, c.d, c.k,
-                                                       c.rows_capacity, dense_routing(c), (float*)dYp, dw,
-                                                       lossblk);
+    cudaError_t e = c.dtype == MOE_BF16
+                        ? combine_bwd_t<__nv_bfloat16>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s)
+                        : combine_bwd_t<float>(c, dy, Yp, w, offsets, row_token, slot_row, dYp, dw, lossblk, s);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -261,32 +261,54 @@ dense_layout_kernel(const int32_t* __restrict__ idx, int T, int E, int C, int al
     }
 }
 
-// Xp[r] = x[row_token[r]] for r < offsets[E]; padding rows (row_token = -1) are zeroed.
-// One warp per row, 16-byte vectors when the row length allows.
-template <typename T>
+// Xp[slot_row[t, j]] = x[t] for every kept slot, one warp per token (x read once, stored to
+// each of its rows; slots in groups of G); then the padding rows (row_token = -1) below
+// offsets[E] are zeroed, 32 rows per warp at a time (ballot, then coalesced stores).
+template <typename T, int G>
 __global__ void __launch_bounds__(256)
 gather_kernel(const T* __restrict__ x, const int32_t* __restrict__ offsets, int E,
-              const int32_t* __restrict__ row_token, int d, int rows_cap, T* __restrict__ Xp) {
+              const int32_t* __restrict__ row_token, const int32_t* __restrict__ slot_row, int Tn, int k,
+              int d, int rows_cap, T* __restrict__ Xp) {
     pdl_wait();
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int nrows = min(offsets[E], rows_cap);
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
     constexpr int V = Vec16<T>::N;
-    for (int r = warp; r < nrows; r += (gridDim.x * blockDim.x) >> 5) {
-        const int t = row_token[r];
-        T* dst = Xp + (size_t)r * d;
-        if ((d % V) == 0) {
-            for (int c = lane * V; c < d; c += 32 * V) {
-                float v[V];
-                if (t >= 0) load16(x + (size_t)t * d + c, v);
-                else {
+    for (int t = gw; t < Tn; t += nwarps) {
+        for (int j0 = 0; j0 < k; j0 += G) {
+            int rows[G];
 #pragma unroll
-                    for (int i = 0; i < V; ++i) v[i] = 0.f;
+            for (int j = 0; j < G; ++j) rows[j] = j0 + j < k ? slot_row[(size_t)t * k + j0 + j] : -1;
+            if ((d % V) == 0) {
+                for (int c = lane * V; c < d; c += 32 * V) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d + c));
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        if (rows[j] >= 0) *reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * d + c) = v;
                 }
-                store16(dst + c, v);
+            } else {
+                for (int c = lane; c < d; c += 32) {
+                    const T v = x[(size_t)t * d + c];
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        if (rows[j] >= 0) Xp[(size_t)rows[j] * d + c] = v;
+                }
             }
-        } else {
-            for (int c = lane; c < d; c += 32) st_f(dst + c, t >= 0 ? ld_f(x + (size_t)t * d + c) : 0.f);
+        }
+    }
+    const int nrows = min(offsets[E], rows_cap);
+    for (int r0 = gw * 32; r0 < nrows; r0 += nwarps * 32) {
+        const int r = r0 + lane;
+        unsigned pad = __ballot_sync(0xffffffffu, r < nrows && row_token[r] < 0);
+        while (pad) {
+            const int b = __ffs(pad) - 1;
+            pad &= pad - 1;
+            T* out = Xp + (size_t)(r0 + b) * d;
+            if ((d % V) == 0) {
+                for (int c = lane * V; c < d; c += 32 * V) *reinterpret_cast<uint4*>(out + c) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                for (int c = lane; c < d; c += 32) out[c] = Elem<T>::from_f(0.f);
+            }
         }
     }
 }
@@ -359,19 +381,30 @@ cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32
     return cudaGetLastError();
 }
 
+template <typename T, int G>
+static cudaError_t gather_g(const moe_config_t& c, const void* x, const int32_t* offsets, const int32_t* row_token,
+                            const int32_t* slot_row, void* Xp, cudaStream_t st) {
+    const long long warps = std::max<long long>(c.T, 1);
+    const int grid = (int)std::max(1LL, std::min((warps + 7) / 8, (long long)num_sms() * 16));
+    return launch_pdl(gather_kernel<T, G>, grid, 256, 0, st, (const T*)x, offsets, c.E, row_token, slot_row, c.T,
+                      c.k, c.d, c.rows_capacity, (T*)Xp);
+}
+template <typename T>
+static cudaError_t gather_t(const moe_config_t& c, const void* x, const int32_t* offsets, const int32_t* row_token,
+                            const int32_t* slot_row, void* Xp, cudaStream_t st) {
+    if (c.k <= 1) return gather_g<T, 1>(c, x, offsets, row_token, slot_row, Xp, st);
+    if (c.k <= 2) return gather_g<T, 2>(c, x, offsets, row_token, slot_row, Xp, st);
+    if (c.k <= 4) return gather_g<T, 4>(c, x, offsets, row_token, slot_row, Xp, st);
+    return gather_g<T, 8>(c, x, offsets, row_token, slot_row, Xp, st);
+}
+
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* offsets,
-                          const int32_t* row_token, void* Xp, cudaStream_t st) {
+                          const int32_t* row_token, const int32_t* slot_row, void* Xp, cudaStream_t st) {
     if (c.rows_capacity == 0) return cudaSuccess;
-    const int rows_per_block = 8;
-    const int grid = ceil_div(c.rows_capacity, rows_per_block);
-    if (c.dtype == MOE_BF16)
-        launch_pdl(gather_kernel<__nv_bfloat16>, grid, 256, 0, st, (const __nv_bfloat16*)x, offsets, c.E,
-                                                           row_token, c.d, c.rows_capacity,
-                                                           (__nv_bfloat16*)Xp);
-    else
-        launch_pdl(gather_kernel<float>, grid, 256, 0, st, (const float*)x, offsets, c.E, row_token, c.d,
-                                                   c.rows_capacity, (float*)Xp);
+    cudaError_t e = c.dtype == MOE_BF16 ? gather_t<__nv_bfloat16>(c, x, offsets, row_token, slot_row, Xp, st)
+                                        : gather_t<float>(c, x, offsets, row_token, slot_row, Xp, st);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -61,7 +61,7 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
         // closed-form layout: no scratch, no size limit
         if (launch_dense_layout(*cfg, idx, kept, offsets, row_token, slot_row, n_dropped, s) != cudaSuccess)
             return MOE_ERR_CUDA;
-        if (launch_gather(*cfg, x, offsets, row_token, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (launch_gather(*cfg, x, offsets, row_token, slot_row, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
         return MOE_OK;
     }
     if (cfg->T > MOE_NOALLOC_MAX_TOKENS || (int64_t)cfg->T * cfg->k > MOE_NOALLOC_MAX_ASSIGNMENTS)
@@ -79,6 +79,6 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
     sort_scratch_take(ws, *cfg, &srt);
     if (launch_sort(*cfg, idx, srt, kept, offsets, row_token, slot_row, n_dropped, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_gather(*cfg, x, offsets, row_token, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gather(*cfg, x, offsets, row_token, slot_row, Xp, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

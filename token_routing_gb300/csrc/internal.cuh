@@ -78,7 +78,7 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
 cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32_t* kept, int32_t* offsets,
                                 int32_t* row_token, int32_t* slot_row, int32_t* n_dropped, cudaStream_t st);
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* offsets,
-                          const int32_t* row_token, void* Xp, cudaStream_t st);
+                          const int32_t* row_token, const int32_t* slot_row, void* Xp, cudaStream_t st);
 
 // gemm_simt.cu (fp32, and bf16 shapes the tensor-core kernel does not take)
 cudaError_t launch_row_gemm_simt(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
