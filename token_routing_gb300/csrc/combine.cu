@@ -216,9 +216,9 @@ __device__ __forceinline__ void block_loss(const LossArgs& la) {
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();
     if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < 8; ++i) t += (double)red[i];
-        *la.loss = (float)(t + (la.balance ? (double)la.aux * (double)*la.balance : 0.0));
+        float t = 0.f;
+        for (int i = 0; i < 8; ++i) t += red[i];
+        *la.loss = t + (la.balance ? la.aux * *la.balance : 0.f);
     }
 }
 
@@ -584,9 +584,9 @@ loss_kernel(const float* __restrict__ lossblk, int nblk, const float* __restrict
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();
     if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < 8; ++i) t += (double)red[i];
-        *loss = (float)(t + (balance ? (double)aux * (double)*balance : 0.0));
+        float t = 0.f;
+        for (int i = 0; i < 8; ++i) t += red[i];
+        *loss = t + (balance ? aux * *balance : 0.f);
     }
 }
 

@@ -173,21 +173,21 @@ noise_kernel(int Tn, int E, uint32_t seed, float* __restrict__ noise) {
         noise[i] = routing_noise((int)(i % Tn), (int)(i / Tn), seed);
 }
 
-// balance_loss = mean over experts of (counts[e] - T*k/E)^2, in double. With dense routing
-// (dense_T >= 0) every expert's count is first set to dense_T, the number of tokens.
-__global__ void balance_loss_kernel(int32_t* __restrict__ counts, int E, double mean, int dense_T,
-                                    float* __restrict__ out) {
+// balance_loss = mean over experts of (counts[e] - T*k/E)^2 (fp32: one warp, lanes over
+// experts, a fixed-order butterfly; GB300's FP64 rate is far too low for a serial loop). With
+// dense routing (dense_T >= 0) every expert's count is first set to dense_T, the token count.
+__global__ void __launch_bounds__(32)
+balance_loss_kernel(int32_t* __restrict__ counts, int E, float mean, int dense_T, float* __restrict__ out) {
     pdl_wait();
-    if (threadIdx.x == 0 && blockIdx.x == 0) {
-        if (dense_T >= 0)
-            for (int e = 0; e < E; ++e) counts[e] = dense_T;
-        double s = 0.0;
-        for (int e = 0; e < E; ++e) {
-            const double dv = (double)counts[e] - mean;
-            s += dv * dv;
-        }
-        *out = (float)(s / (double)E);
+    const int lane = threadIdx.x;
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) {
+        if (dense_T >= 0) counts[e] = dense_T;
+        const float dv = (float)(dense_T >= 0 ? dense_T : counts[e]) - mean;
+        s = fmaf(dv, dv, s);
     }
+    s = warp_sum(s);
+    if (lane == 0) *out = s / (float)E;
 }
 
 }  // namespace
@@ -232,7 +232,7 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         st = cudaGetLastError();
         if (st != cudaSuccess) return st;
     }
-    const double mean = (double)c.T * (double)c.k / (double)c.E;
+    const float mean = (float)((double)c.T * (double)c.k / (double)c.E);
     launch_pdl(balance_loss_kernel, 1, 32, 0, s, counts, c.E, mean, dense_routing(c) ? c.T : -1, balance_loss);
     count_launch();
     return cudaGetLastError();

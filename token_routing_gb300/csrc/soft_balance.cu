@@ -108,43 +108,41 @@ soft_load_kernel(const float* __restrict__ logits, int T, int E, float inv_temp,
     }
 }
 
-// P[e] = sum of the blocks' partials; loss = weight * mean_e (P_e - T/E)^2 in double. One
-// block of 32 warps: warp w owns experts w, w + 32, ...; its lanes add chunks lane, lane + 32,
-// ... (eight experts' loads in flight), then a butterfly sums the lanes (fixed order).
+// P[e] = sum of the soft-load partials over the chunks: block b takes experts 32 b + lane
+// (128-byte rows, coalesced); warp w adds chunks w, w + 32, ..., then the 32 warp sums are
+// added in warp order.
 constexpr int kFinalThreads = 1024;
 __global__ void __launch_bounds__(kFinalThreads)
-soft_final_kernel(const float* __restrict__ part, int nchunk, int T, int E, float weight,
-                  float* __restrict__ P, float* __restrict__ loss) {
+soft_final_kernel(const float* __restrict__ part, int nchunk, int E, float* __restrict__ P) {
     pdl_wait();
-    __shared__ float s_P[MOE_MAX_EXPERTS];
+    __shared__ float s_acc[kFinalThreads / 32][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int J = MOE_MAX_EXPERTS / (kFinalThreads / 32);
-    float acc[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) acc[j] = 0.f;
-    for (int c = lane; c < nchunk; c += 32) {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = warp + j * (kFinalThreads / 32);
-            if (e < E) acc[j] += part[(size_t)c * E + e];
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int e = warp + j * (kFinalThreads / 32);
-        const float v = warp_sum(acc[j]);
-        if (lane == 0 && e < E) { s_P[e] = v; P[e] = v; }
-    }
+    const int e = blockIdx.x * 32 + lane;
+    float acc = 0.f;
+    if (e < E)
+        for (int c = warp; c < nchunk; c += kFinalThreads / 32) acc += part[(size_t)c * E + e];
+    s_acc[warp][lane] = acc;
     __syncthreads();
-    if (threadIdx.x == 0 && loss) {
-        const double mean = (double)T / (double)E;
-        double s = 0.0;
-        for (int e = 0; e < E; ++e) {
-            const double dv = (double)s_P[e] - mean;
-            s += dv * dv;
-        }
-        *loss = (float)((double)weight * s / (double)E);
+    if (warp == 0 && e < E) {
+        float v = 0.f;
+        for (int w = 0; w < kFinalThreads / 32; ++w) v += s_acc[w][lane];
+        P[e] = v;
     }
+}
+
+// loss = weight * mean_e (P_e - T/E)^2: one warp, lanes over experts, fixed-order butterfly
+// (fp32: GB300's FP64 rate is far too low for a serial loop).
+__global__ void __launch_bounds__(32)
+soft_loss_kernel(const float* __restrict__ P, int T, int E, float weight, float* __restrict__ loss) {
+    pdl_wait();
+    const float mean = (float)T / (float)E;
+    float s = 0.f;
+    for (int e = threadIdx.x; e < E; e += 32) {
+        const float dv = P[e] - mean;
+        s = fmaf(dv, dv, s);
+    }
+    s = warp_sum(s);
+    if (threadIdx.x == 0) *loss = weight * s / (float)E;
 }
 
 // For rows that are no multiple of 16 bytes. 8 tokens per block (x), V columns per thread (y).
@@ -562,53 +560,47 @@ constexpr int kSplitThreads = 256;
 __host__ __device__ inline int e8_of(int E) { return (E + 7) / 8 * 8; }
 __host__ __device__ inline int k2_of(int E) { return (2 * e8_of(E) + 63) / 64 * 64; }
 
-// dzs[t, :] = hi / lo layout of dz[t, :] for t < T, zero rows for T <= t < T_pad (one warp per
-// row, grid-stride). Column sums of dz over the block's rows go to dbg_part[block, :] (warps
-// in order, rows in grid-stride order). Block 0 also writes the bucket offsets.
+// dzs[t, c] for t < T_pad, c < K2: hi of dz[t, c] (c < E), lo of dz[t, c - E8]
+// (E8 <= c < E8 + E), 0 elsewhere and for t >= T; one thread per column pair (bf16x2 store),
+// grid-stride. Block 0 also writes the bucket offsets. (Reading each dz value once and
+// storing its two halves separately measured slower: 36 vs 31 us at 32768 x 256.)
+__device__ __forceinline__ float split_val(const float* __restrict__ dz, int Tn, int E, int e8, int t, int c) {
+    if (t >= Tn) return 0.f;
+    if (c < E) return __bfloat162float(__float2bfloat16_rn(dz[(size_t)t * E + c]));
+    if (c >= e8 && c < e8 + E) {
+        const float z = dz[(size_t)t * E + c - e8];
+        return z - __bfloat162float(__float2bfloat16_rn(z));
+    }
+    return 0.f;
+}
+
 __global__ void __launch_bounds__(kSplitThreads)
 soft_split_kernel(const float* __restrict__ dz, int Tn, int Tpad, int E, __nv_bfloat16* __restrict__ dzs,
-                  float* __restrict__ dbg_part, int32_t* __restrict__ offs, int splits, int bucket) {
+                  int32_t* __restrict__ offs, int splits, int bucket) {
     pdl_wait();
-    __shared__ float s_sum[kSplitThreads / 32][MOE_MAX_EXPERTS];
-    const int e8 = e8_of(E), k2 = k2_of(E);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int e8 = e8_of(E), k2 = k2_of(E), half = k2 / 2;
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= splits; i += blockDim.x) offs[i] = min(i * bucket, Tpad);
         if (threadIdx.x == 0) { offs[splits + 1] = 0; offs[splits + 2] = Tpad; }
     }
-    float acc[kQ];
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tpad; t += nwarps) {
-        __nv_bfloat16* row = dzs + (size_t)t * k2;
-        for (int c = lane; c < k2; c += 32) {
-            float v = 0.f;
-            if (t < Tn) {
-                if (c < E) {
-                    v = __bfloat162float(__float2bfloat16_rn(dz[(size_t)t * E + c]));
-                } else if (c >= e8 && c < e8 + E) {
-                    const float z = dz[(size_t)t * E + c - e8];
-                    v = z - __bfloat162float(__float2bfloat16_rn(z));
-                }
-            }
-            row[c] = __float2bfloat16_rn(v);
-        }
-        if (t < Tn) {
-#pragma unroll
-            for (int q = 0; q < kQ; ++q)
-                if (lane + 32 * q < E) acc[q] += dz[(size_t)t * E + lane + 32 * q];
-        }
+    const long long n = (long long)Tpad * half;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / half), c = (int)(i % half) * 2;
+        const __nv_bfloat162 v = __floats2bfloat162_rn(split_val(dz, Tn, E, e8, t, c), split_val(dz, Tn, E, e8, t, c + 1));
+        *reinterpret_cast<__nv_bfloat162*>(dzs + (size_t)t * k2 + c) = v;
     }
-#pragma unroll
-    for (int q = 0; q < kQ; ++q)
-        if (lane + 32 * q < E) s_sum[warp][lane + 32 * q] = acc[q];
-    __syncthreads();
+}
+
+// dbg_part[b, e] = sum of dz[t, e] over the 64 rows of block b (in order), thread e.
+constexpr int kDzsumRows = 64;
+__global__ void __launch_bounds__(256)
+soft_dzsum_kernel(const float* __restrict__ dz, int Tn, int E, float* __restrict__ dbg_part) {
+    pdl_wait();
+    const int t0 = blockIdx.x * kDzsumRows, t1 = min(Tn, t0 + kDzsumRows);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kSplitThreads / 32; ++w) v += s_sum[w][e];
-        dbg_part[(size_t)blockIdx.x * E + e] = v;
+        float a = 0.f;
+        for (int t = t0; t < t1; ++t) a += dz[(size_t)t * E + e];
+        dbg_part[(size_t)blockIdx.x * E + e] = a;
     }
 }
 
@@ -712,7 +704,7 @@ static SoftTc soft_tc_geom(const moe_config_t& c) {
     g.splits = std::min(want, max_splits);
     g.bucket = (ceil_div(g.tpad, g.splits) + 63) / 64 * 64;
     g.splits = ceil_div(g.tpad, g.bucket);
-    g.nblk = std::max(1, std::min(ceil_div(g.tpad, kSplitThreads / 32), 2 * num_sms()));
+    g.nblk = std::max(1, ceil_div(c.T, kDzsumRows));   // dz column-sum partials
     return g;
 }
 
@@ -734,11 +726,18 @@ void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
     }
 }
 
-// dz (fp32 [T, E]) -> hi/lo bf16 layout, dbg partials and bucket offsets.
-static cudaError_t launch_soft_split(const moe_config_t& c, const float* dz, const SoftScratch& s, cudaStream_t st) {
+// dz (fp32 [T, E]) -> hi/lo bf16 layout and bucket offsets; with want_sums also the column-sum
+// partials of dz (for dbg).
+static cudaError_t launch_soft_split(const moe_config_t& c, const float* dz, bool want_sums, const SoftScratch& s,
+                                     cudaStream_t st) {
     const SoftTc g = soft_tc_geom(c);
-    cudaError_t e = launch_pdl(soft_split_kernel, dim3(g.nblk), dim3(kSplitThreads), 0, st, dz, c.T, g.tpad, c.E,
-                               (__nv_bfloat16*)s.dzs, s.dbg_part, s.offs, g.splits, g.bucket);
+    const long long n = (long long)g.tpad * (g.k2 / 2);
+    const int grid = (int)std::max(1LL, std::min((n + kSplitThreads - 1) / kSplitThreads, (long long)num_sms() * 8));
+    cudaError_t e = launch_pdl(soft_split_kernel, dim3(grid), dim3(kSplitThreads), 0, st, dz, c.T, g.tpad, c.E,
+                               (__nv_bfloat16*)s.dzs, s.offs, g.splits, g.bucket);
+    count_launch();
+    if (e != cudaSuccess || !want_sums || c.T == 0) return e;
+    e = launch_pdl(soft_dzsum_kernel, dim3(g.nblk), dim3(256), 0, st, dz, c.T, c.E, s.dbg_part);
     count_launch();
     return e;
 }
@@ -791,8 +790,12 @@ cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, floa
         cudaError_t e = launch_fill(s.part, (long long)c.E, 0.f, st);
         if (e != cudaSuccess) return e;
     }
-    launch_pdl(soft_final_kernel, 1, kFinalThreads, 0, st, s.part, nchunk, c.T, c.E, weight, P, loss);
+    launch_pdl(soft_final_kernel, ceil_div(c.E, 32), kFinalThreads, 0, st, s.part, nchunk, c.E, P);
     count_launch();
+    if (loss) {
+        launch_pdl(soft_loss_kernel, 1, 32, 0, st, (const float*)P, c.T, c.E, weight, loss);
+        count_launch();
+    }
     return cudaGetLastError();
 }
 
@@ -808,7 +811,7 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
                                    inv_temp, weight, s.dz);
         count_launch();
         if (e != cudaSuccess) return e;
-        if ((e = launch_soft_split(c, s.dz, s, st)) != cudaSuccess) return e;
+        if ((e = launch_soft_split(c, s.dz, dbg != nullptr, s, st)) != cudaSuccess) return e;
         if ((e = launch_dzwg_tc(c, Wg, dx, s, st)) != cudaSuccess) return e;
         return launch_dzx_tc(c, x, dWg, dbg, true, s, st);
     }
@@ -853,7 +856,7 @@ cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void*
                              bool accumulate, const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0 && accumulate) return cudaSuccess;
     if (c.T > 0 && soft_tc_ok(c)) {
-        cudaError_t e = launch_soft_split(c, dz, s, st);
+        cudaError_t e = launch_soft_split(c, dz, dbg != nullptr, s, st);
         if (e != cudaSuccess) return e;
         return launch_dzx_tc(c, x, dWg, dbg, accumulate, s, st);
     }
