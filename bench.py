@@ -46,8 +46,111 @@ def _peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, src="fallback")
 
 
+REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+
+
+def reasons_from_mask(mask):
+    """Names of the active clock-event reasons in an NVML reason bit mask (nvml.h values)."""
+    return [n for n, b in REASON_BITS if mask & b]
+
+
+def summarise_clocks(samples):
+    """samples: (sm_mhz, sm_max_mhz, reason names) tuples -> the bench line's `clocks` object."""
+    if not samples:
+        return None
+    reasons = sorted({r for _, _, rs in samples for r in rs})
+    return {"sm_mhz": statistics.median(a for a, _, _ in samples),
+            "sm_max_mhz": max(b for _, b, _ in samples), "reasons": reasons, "samples": len(samples)}
+
+
+class NvmlReader:
+    """SM clock, maximum SM clock and clock-event reasons of one GPU, read through the NVML
+    library that ships with the driver (the library nvidia-smi itself uses). Read-only."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, uuid=None, index=0):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError("no NVML handle for the device")
+        self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.h, self.NVML_CLOCK_SM, self.ct.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return float(v.value)
+
+    def sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def sm_max_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reason_mask(self):
+        v = self.ct.c_ulonglong()
+        if self.get_reasons(self.h, self.ct.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return int(v.value)
+
+
+class PollingClockSampler:
+    """Polls a reader (NvmlReader or a stand-in) every `period` seconds on a thread while the
+    timed region runs, so that even a region of a few milliseconds gets several samples."""
+
+    def __init__(self, reader, period=0.001):
+        self.reader = reader
+        self.period = period
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _sample(self):
+        r = self.reader
+        self.samples.append((r.sm_mhz(), r.sm_max_mhz(), reasons_from_mask(r.reason_mask())))
+
+    def _run(self):
+        try:
+            while not self.stop_flag.is_set():
+                self._sample()
+                self.stop_flag.wait(self.period)
+        except Exception:
+            pass
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join(timeout=5)
+        if not self.samples:   # a region shorter than one NVML query: sample right after it
+            try:
+                self._sample()
+            except Exception:
+                pass
+        out = summarise_clocks(self.samples)
+        if out is not None:
+            out["source"] = "nvml"
+        return out
+
+
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running (used when the
+    NVML library cannot be loaded)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -83,24 +186,32 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        samples = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                a, b = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            samples.append((a, b, [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]))
+        out = summarise_clocks(samples)
+        if out is not None:
+            out["source"] = "nvidia-smi"
+        return out
+
+
+def make_clock_sampler(dev, local):
+    """NVML polling when the library loads, else the nvidia-smi sampler."""
+    try:
+        import torch
+        uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+        uuid = f"GPU-{uuid}" if uuid is not None else None
+        return PollingClockSampler(NvmlReader(uuid=uuid, index=local))
+    except Exception:
+        return ClockSampler(local)
 
 
 GEMM_SOURCES = ["token_routing_gb300/csrc/gemm_tc_pair.cu", "token_routing_gb300/csrc/gemm_tc.cu",
@@ -350,7 +461,7 @@ def run_ours(args, cfg):
     moe.get_error(stream)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = make_clock_sampler(dev, local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)

@@ -162,6 +162,57 @@ __device__ __forceinline__ void gelu_and_grad_f(float a, float& g, float& gp) {
     gp = fmaf(a * 0.39894228040143268f, e, Phi);                  // Phi + a phi(a)
 }
 
+// ---- packed fp32 pairs: Blackwell's f32x2 add/mul/fma issue two IEEE fp32 operations (round
+// to nearest, no flush) per instruction. A pair lives in one 64-bit register pair.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t splat2(float c) { return pk2(c, c); }
+
+// gelu_and_grad_f on two values at once: the same formula and constants, with the
+// polynomial, the products and the final combination in f32x2 operations (the reciprocal and
+// the exponential stay per element on the special-function unit).
+__device__ __forceinline__ void gelu_and_grad_f2(float a0, float a1, float& g0, float& g1, float& gp0,
+                                                 float& gp1) {
+    const uint64_t a = pk2(a0, a1);
+    const float p = 0.3275911f * 0.70710678118654752f;
+    const uint64_t t = pk2(rcp_approx(fmaf(p, fabsf(a0), 1.0f)), rcp_approx(fmaf(p, fabsf(a1), 1.0f)));
+    uint64_t q = fma2(splat2(0.5f * 1.061405429f), t, splat2(0.5f * -1.453152027f));
+    q = fma2(q, t, splat2(0.5f * 1.421413741f));
+    q = fma2(q, t, splat2(0.5f * -0.284496736f));
+    q = fma2(q, t, splat2(0.5f * 0.254829592f));
+    float r0, r1;
+    upk2(mul2(mul2(a, a), splat2(-0.72134752044448170f)), r0, r1);   // -a^2 log2(e) / 2
+    const uint64_t e = pk2(ex2_approx(r0), ex2_approx(r1));           // exp(-a^2/2)
+    const uint64_t h = mul2(mul2(q, t), e);                            // 0.5 erfc(|a| / sqrt 2)
+    float h0, h1, o0, o1;
+    upk2(h, h0, h1);
+    upk2(fma2(h, splat2(-1.0f), splat2(1.0f)), o0, o1);               // 1 - h
+    const uint64_t Phi = pk2(a0 >= 0.f ? o0 : h0, a1 >= 0.f ? o1 : h1);
+    upk2(mul2(a, Phi), g0, g1);
+    upk2(fma2(mul2(a, splat2(0.39894228040143268f)), e, Phi), gp0, gp1);
+}
+
 __device__ __forceinline__ float gelu_f(float a) {
     return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
 }

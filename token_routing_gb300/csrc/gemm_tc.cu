@@ -220,7 +220,8 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                         // H = GELU(A) for the second GEMM, GELU'(A) saved for the backward
                         float gp[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) gelu_and_grad_f(v[i], v[i], gp[i]);
+                        for (int i = 0; i < 32; i += 2)
+                            gelu_and_grad_f2(v[i], v[i + 1], v[i], v[i + 1], gp[i], gp[i + 1]);
                         uint32_t b = st.acquire(lane);
                         st.store(lane, b, gp, &tmO0, n, y);
                         b = st.acquire(lane);

@@ -316,7 +316,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     float bv[32];
                     unpack_raw32(cur, bv);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] += bv[i];
+                    for (int i = 0; i < 32; i += 2) upk2(add2(pk2(v[i], v[i + 1]), pk2(bv[i], bv[i + 1])), v[i], v[i + 1]);
                     if (KIND == kGemmFfn1) {
                         // H = GELU(A) for the second GEMM, GELU'(A) saved for the backward
                         const uint32_t b = st2.acquire(lane);
@@ -338,7 +338,8 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     __syncwarp();
                     if (KIND == kGemmDH) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= a[i];  // a = GELU'(A) saved by the forward
+                        for (int i = 0; i < 32; i += 2)   // a = GELU'(A) saved by the forward
+                            upk2(mul2(pk2(v[i], v[i + 1]), pk2(a[i], a[i + 1])), v[i], v[i + 1]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] += a[i];  // accumulate into aux (= out0)

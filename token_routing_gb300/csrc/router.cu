@@ -164,13 +164,16 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
 }
 
 // noise[e, t] = N(0,1) normal of (token t, expert e), expert-major so that the router's
-// lanes (consecutive tokens) read consecutive addresses.
+// lanes (consecutive tokens) read consecutive addresses. Experts run over grid.y and tokens
+// over grid.x, so no thread divides a 64-bit index.
 __global__ void __launch_bounds__(256)
 noise_kernel(int Tn, int E, uint32_t seed, float* __restrict__ noise) {
     pdl_wait();
-    const long long n = (long long)Tn * E;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-        noise[i] = routing_noise((int)(i % Tn), (int)(i / Tn), seed);
+    for (int e = blockIdx.y; e < E; e += gridDim.y) {
+        float* row = noise + (size_t)e * Tn;
+        for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < Tn; t += gridDim.x * blockDim.x)
+            row[t] = routing_noise(t, e, seed);
+    }
 }
 
 // balance_loss = mean over experts of (counts[e] - T*k/E)^2 (fp32: one warp, lanes over
@@ -201,9 +204,10 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         const bool noisy = c.noise_std > 0.f;
         if (noisy) {
             if (!noise) return cudaErrorInvalidValue;
-            const long long n = (long long)c.T * c.E;
-            const int grid = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 16);
-            st = launch_pdl(noise_kernel, dim3(grid), dim3(256), 0, s, c.T, c.E, c.noise_seed, noise);
+            // one block row per expert (E <= 256), about 16 blocks of 256 threads per SM in all
+            const int gx = std::min(ceil_div(c.T, 256), std::max(1, num_sms() * 16 / c.E));
+            const dim3 grid((unsigned)gx, (unsigned)c.E);
+            st = launch_pdl(noise_kernel, grid, dim3(256), 0, s, c.T, c.E, c.noise_seed, noise);
             count_launch();
             if (st != cudaSuccess) return st;
         }

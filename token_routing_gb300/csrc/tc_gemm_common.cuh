@@ -232,7 +232,8 @@ struct Stager2 {
         for (int j = 0; j < 4; ++j) {
             float g[8], gp[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) gelu_and_grad_f(a[8 * j + i], g[i], gp[i]);
+            for (int i = 0; i < 8; i += 2)
+                gelu_and_grad_f2(a[8 * j + i], a[8 * j + i + 1], g[i], g[i + 1], gp[i], gp[i + 1]);
             sts128(sw64_addr(buf, lane, j), pack8(gp));
             sts128(sw64_addr(buf + STG_BYTES, lane, j), pack8(g));
         }
