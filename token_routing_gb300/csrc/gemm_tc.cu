@@ -244,9 +244,11 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 32; ++i) v[i] *= a[i];  // a = GELU'(A) saved by the forward
                     st.store(lane, b, v, &tmO0, n, y);
                     if (p.colsum) {
-                        // db1 partial of this tile's lane quarter (32 rows), fixed-order butterfly
-                        const float sum = warp_colsum32(v, lane);
-                        p.colsum[((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n + lane] = sum;
+                        // db1 partial of this tile's lane quarter (32 rows) from the staged dA chunk
+                        const float2 cs = staged_colsum32(b, lane);
+                        if (lane < 16)
+                            *reinterpret_cast<float2*>(p.colsum + ((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n +
+                                                       2 * lane) = cs;
                     }
                 } else {
                     const uint32_t b = st.acquire(lane);

@@ -31,11 +31,16 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 // 8 epilogue warps (two per TMEM lane quarter, 128 columns each) that fetch the next chunk's
 // accumulator columns and side input ahead of use. Ffn1 writes two outputs per chunk (GELU'
 // and H): each of its warps keeps two staging buffer pairs, and its ring has five 32 KB stages
-// instead of six. (Sixteen epilogue warps without the fetch-ahead measured slower.)
+// instead of six. (Twelve Ffn1 epilogue warps, three per quarter with one buffer pair each,
+// measured the same; sixteen without the fetch-ahead measured slower.)
 template <int KIND> constexpr int pair_epi_warps() { return 8; }
 template <int KIND> constexpr int pair_threads() { return 64 + 32 * pair_epi_warps<KIND>(); }
 template <int KIND> constexpr int pair_stages() { return KIND == kGemmFfn1 ? 5 : 6; }
-template <int KIND> constexpr int pair_epi_bytes() { return pair_epi_warps<KIND>() * (KIND == kGemmFfn1 ? 4 : 2) * STG_BYTES; }
+// staging buffer pairs per Ffn1 epilogue warp
+template <int KIND> constexpr int pair_ffn1_nb() { return pair_epi_warps<KIND>() > 8 ? 1 : 2; }
+template <int KIND> constexpr int pair_epi_bytes() {
+    return pair_epi_warps<KIND>() * (KIND == kGemmFfn1 ? 2 * pair_ffn1_nb<KIND>() : 2) * STG_BYTES;
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -115,7 +120,10 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     constexpr bool AUX = (KIND == kGemmDH || KIND == kGemmAccum);   // side input read per chunk
     constexpr int P_STAGES = pair_stages<KIND>();
     constexpr int PE_THREADS = 32 * pair_epi_warps<KIND>();
-    constexpr int COLS = BN / (pair_epi_warps<KIND>() / 4);   // accumulator columns per epilogue warp
+    // accumulator columns per epilogue warp: the tile's 32-column chunks spread over the warps of
+    // a lane quarter (4 + 4 with two warps, 3 + 3 + 2 with three)
+    constexpr int WPQ = pair_epi_warps<KIND>() / 4;
+    constexpr int CHUNKS = BN / 32;
     // the heavy epilogues (Ffn1's GELU, dH's product with GELU') load the next accumulator
     // chunk from TMEM while processing the current one
     constexpr bool PREFETCH = KIND == kGemmFfn1 || KIND == kGemmDH;
@@ -245,9 +253,12 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     } else {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
         const int quarter = warp & 3;
-        const int c_lo = ((warp - 2) >> 2) * COLS;
+        const int grp = (warp - 2) >> 2;
+        const int c_lo = 32 * (grp * (CHUNKS / WPQ) + min(grp, CHUNKS % WPQ));
+        const int COLS = 32 * (CHUNKS / WPQ + (grp < CHUNKS % WPQ ? 1 : 0));
         Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
-        Stager2<2> st2{smem_u32(stg_smem + (warp - 2) * 4 * STG_BYTES), 0};   // Ffn1 only
+        constexpr int NB = pair_ffn1_nb<KIND>();
+        Stager2<NB> st2{smem_u32(stg_smem + (warp - 2) * 2 * NB * STG_BYTES), 0};   // Ffn1 only
         const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(tempty), 0), map_to_rank(smem_u32(tempty + 1), 0)};
         uint32_t tl = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += nclusters) {
@@ -346,8 +357,11 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     }
                     st.store(lane, b, v, &tmO0, n, y);
                     if (KIND == kGemmDH && p.colsum) {
-                        const float sum = warp_colsum32(v, lane);
-                        p.colsum[((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n + lane] = sum;
+                        // db1 partial of this lane quarter (32 rows) from the staged dA chunk
+                        const float2 cs = staged_colsum32(b, lane);
+                        if (lane < 16)
+                            *reinterpret_cast<float2*>(p.colsum + ((size_t)(t.m0 / BM) * 4 + quarter) * p.N + n +
+                                                       2 * lane) = cs;
                     }
                 } else {
                     const uint32_t b = st.acquire(lane);

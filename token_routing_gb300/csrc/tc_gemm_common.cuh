@@ -114,22 +114,6 @@ __device__ __forceinline__ void unpack_raw32(const Raw32& r, float* out) {
     }
 }
 
-// Column sums of a warp's 32 rows x 32 columns (one row per lane, v[i] = column i):
-// a butterfly that halves the columns each lane carries; lane l ends with column l.
-__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool hi = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = hi ? v[i] : v[i + s];
-            const float keep = hi ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-    return v[0];
-}
-
 template <int KIND>
 constexpr bool has_bias() { return KIND == kGemmFfn1 || KIND == kGemmFfn2; }
 
@@ -247,6 +231,29 @@ struct Stager2 {
         ++count;
     }
 };
+
+// Column sums of the 32 x 32 bf16 chunk a Stager has just written to `buf` (lane = row,
+// swizzled 64-byte rows), i.e. of the values the chunk stores. Lanes 0-15 add the even rows and
+// lanes 16-31 the odd rows, each lane two adjacent columns read as one 32-bit word: a step reads
+// one 128-byte line, with no bank conflicts. The two halves then combine across lanes l, l + 16.
+// Lane l < 16 returns the sums of columns 2l and 2l + 1.
+__device__ __forceinline__ float2 staged_colsum32(uint32_t buf, int lane) {
+    const int c = lane & 15;
+    const uint32_t off = (uint32_t)(c & 3) * 4;
+    uint64_t acc = pk2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 2 * i + (lane >> 4);
+        uint32_t w;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(sw64_addr(buf, r, c >> 2) + off));
+        acc = add2(acc, pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+    }
+    float s0, s1;
+    upk2(acc, s0, s1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    return make_float2(s0, s1);
+}
 
 template <int KIND>
 __device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
