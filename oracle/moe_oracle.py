@@ -139,16 +139,24 @@ def philox4x64_10(counter, key):
 
 
 def routing_noise(T, E, seed):
-    """Standard normal noise for every (token t, expert e): Philox4x64-10 at counter
-    (t, e, 0, 0) with key (seed, 0); the top 24 bits of its first two outputs give
-    u1, u2 in (0, 1] and Box-Muller gives sqrt(-2 ln u1) cos(2 pi u2)."""
+    """Standard normal noise for every (token t, expert e), four experts per generator draw:
+    experts 4g .. 4g+3 of token t take Philox4x64-10 at counter (t, g, 0, 0) with key
+    (seed, 0). The top 24 bits of outputs 0, 1 and of outputs 2, 3 give two pairs (u1, u2) in
+    (0, 1]; Box-Muller makes each pair the two normals sqrt(-2 ln u1) cos(2 pi u2) and
+    sqrt(-2 ln u1) sin(2 pi u2), in that order."""
     n = np.zeros((T, E))
     for t in range(T):
-        for e in range(E):
-            o = philox4x64_10((t, e, 0, 0), (seed, 0))
-            u1 = ((o[0] >> 40) + 1) / float(1 << 24)
-            u2 = ((o[1] >> 40) + 1) / float(1 << 24)
-            n[t, e] = math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+        for g in range((E + 3) // 4):
+            o = philox4x64_10((t, g, 0, 0), (seed, 0))
+            z = []
+            for h in range(2):
+                u1 = ((o[2 * h] >> 40) + 1) / float(1 << 24)
+                u2 = ((o[2 * h + 1] >> 40) + 1) / float(1 << 24)
+                r = math.sqrt(-2.0 * math.log(u1))
+                z += [r * math.cos(2.0 * math.pi * u2), r * math.sin(2.0 * math.pi * u2)]
+            for j in range(4):
+                if 4 * g + j < E:
+                    n[t, 4 * g + j] = z[j]
     return n
 
 

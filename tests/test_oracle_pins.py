@@ -452,6 +452,19 @@ def test_routing_noise_is_standard_normal():
     assert not np.array_equal(O.routing_noise(3, 4, 1), O.routing_noise(3, 4, 2))
 
 
+def test_routing_noise_pairs_are_independent():
+    """Four experts share one generator draw: the cosine and sine normals of a Box-Muller pair,
+    and the two pairs of a draw, are uncorrelated (a reused output would not be),
+    and every expert column is N(0, 1) on its own. A ragged last group (E = 10) is filled."""
+    n = O.routing_noise(4000, 10, seed=11)
+    c = np.corrcoef(n.T)
+    off = c[~np.eye(10, dtype=bool)]
+    assert np.abs(off).max() < 0.06                      # 4000 samples: sd of r is ~0.016
+    assert np.abs(n.mean(axis=0)).max() < 0.06
+    assert np.abs(n.std(axis=0) - 1.0).max() < 0.05
+    assert len(np.unique(n)) == n.size
+
+
 def test_noisy_route_is_plain_route_of_noisy_logits():
     inp = _rand_inputs(50, 8, 12, 4, seed=91)
     noisy = O.route(inp["x"], inp["Wg"], None, 2, 1.0, noise_std=0.1, noise_seed=5)

@@ -222,12 +222,14 @@ __device__ __forceinline__ float gelu_grad_f(float a) {
     return Phi + a * phi;
 }
 
-// Training-time routing noise: a standard normal per (token, expert) from the Philox4x64-10
-// counter-based generator (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
-// 1, 2, 3", SC 2011) at counter (t, e, 0, 0), key (seed, 0); the top 24 bits of the first two
-// outputs give u1, u2 in (0, 1] and Box-Muller gives sqrt(-2 ln u1) cos(2 pi u2).
-__device__ __forceinline__ float routing_noise(int t, int e, uint32_t seed) {
-    uint64_t c0 = (uint64_t)(uint32_t)t, c1 = (uint64_t)(uint32_t)e, c2 = 0, c3 = 0;
+// Training-time routing noise: a standard normal per (token, expert), four experts per draw of
+// the Philox4x64-10 counter-based generator (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011). Experts 4g .. 4g + 3 of token t take counter
+// (t, g, 0, 0) with key (seed, 0); the top 24 bits of outputs 0, 1 and of outputs 2, 3 give two
+// (u1, u2) pairs in (0, 1], and Box-Muller turns each pair into the two normals
+// sqrt(-2 ln u1) cos(2 pi u2) and sqrt(-2 ln u1) sin(2 pi u2), in that order.
+__device__ __forceinline__ void routing_noise4(int t, int g, uint32_t seed, float (&z)[4]) {
+    uint64_t c0 = (uint64_t)(uint32_t)t, c1 = (uint64_t)(uint32_t)g, c2 = 0, c3 = 0;
     uint64_t k0 = seed, k1 = 0;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
@@ -238,9 +240,25 @@ __device__ __forceinline__ float routing_noise(int t, int e, uint32_t seed) {
         k0 += 0x9E3779B97F4A7C15ull;
         k1 += 0xBB67AE8584CAA73Bull;
     }
-    const float u1 = (float)((c0 >> 40) + 1) * 5.9604644775390625e-8f;  // 2^-24
-    const float u2 = (float)((c1 >> 40) + 1) * 5.9604644775390625e-8f;
-    return sqrtf(-2.0f * logf(u1)) * cosf(6.28318530717958648f * u2);
+    const uint64_t o[4] = {c0, c1, c2, c3};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float u1 = (float)((uint32_t)(o[2 * h] >> 40) + 1u) * 5.9604644775390625e-8f;   // 2^-24
+        const float u2 = (float)((uint32_t)(o[2 * h + 1] >> 40) + 1u) * 5.9604644775390625e-8f;
+        const float r = sqrtf(-2.0f * logf(u1));
+        float sn, cs;
+        sincosf(6.28318530717958648f * u2, &sn, &cs);
+        z[2 * h] = r * cs;
+        z[2 * h + 1] = r * sn;
+    }
+}
+
+// The normal of (token t, expert e) alone (its group's draw, one of the four kept).
+__device__ __forceinline__ float routing_noise(int t, int e, uint32_t seed) {
+    float z[4];
+    routing_noise4(t, e >> 2, seed, z);
+    const int j = e & 3;
+    return j == 0 ? z[0] : j == 1 ? z[1] : j == 2 ? z[2] : z[3];
 }
 
 // ---------------------------------------------------------------- host side

@@ -104,6 +104,9 @@ sort_kernel(SortArgs a) {
     __shared__ int s_kept[MOE_MAX_EXPERTS];
     const int tid = threadIdx.x;
     const int G = gridDim.x;
+    // the next kernel may start its prologue once every block has passed this point, i.e. once
+    // the whole cooperative grid is resident
+    pdl_wait();
 
     // ---- phase 1: chunk histograms
     for (int ch = blockIdx.x; ch < a.nchunk; ch += G) {
@@ -352,7 +355,7 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     a.assign_off = s.assign_off; a.assign_tok = s.assign_tok;
     a.kept = kept; a.offsets = offsets; a.row_token = row_token; a.slot_row = slot_row;
     a.n_dropped = n_dropped; a.bar = s.bar; a.err = device_error_word();
-    cudaError_t e = cudaMemsetAsync(s.bar, 0, sizeof(unsigned), st);
+    cudaError_t e = launch_fill(s.bar, 1, 0u, st);
     if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(a.nchunk, std::min(sort_coresident_blocks(), 2 * num_sms())));
     cudaLaunchConfig_t cfg{};
@@ -360,11 +363,13 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     cfg.blockDim = dim3(kSortTok);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, sort_kernel, a);
     count_launch();
     if (e != cudaSuccess) return e;

@@ -164,15 +164,20 @@ route_kernel(const T* __restrict__ x, const T* __restrict__ Wg, const float* __r
 }
 
 // noise[e, t] = N(0,1) normal of (token t, expert e), expert-major so that the router's
-// lanes (consecutive tokens) read consecutive addresses. Experts run over grid.y and tokens
-// over grid.x, so no thread divides a 64-bit index.
+// lanes (consecutive tokens) read consecutive addresses. One thread per (token, group of four
+// experts): groups run over grid.y and tokens over grid.x.
 __global__ void __launch_bounds__(256)
 noise_kernel(int Tn, int E, uint32_t seed, float* __restrict__ noise) {
     pdl_wait();
-    for (int e = blockIdx.y; e < E; e += gridDim.y) {
-        float* row = noise + (size_t)e * Tn;
-        for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < Tn; t += gridDim.x * blockDim.x)
-            row[t] = routing_noise(t, e, seed);
+    const int groups = (E + 3) >> 2;
+    for (int g = blockIdx.y; g < groups; g += gridDim.y) {
+        for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < Tn; t += gridDim.x * blockDim.x) {
+            float z[4];
+            routing_noise4(t, g, seed, z);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * g + j < E) noise[(size_t)(4 * g + j) * Tn + t] = z[j];
+        }
     }
 }
 
@@ -204,9 +209,11 @@ cudaError_t launch_route(const moe_config_t& c, const void* x, const void* Wg, c
         const bool noisy = c.noise_std > 0.f;
         if (noisy) {
             if (!noise) return cudaErrorInvalidValue;
-            // one block row per expert (E <= 256), about 16 blocks of 256 threads per SM in all
-            const int gx = std::min(ceil_div(c.T, 256), std::max(1, num_sms() * 16 / c.E));
-            const dim3 grid((unsigned)gx, (unsigned)c.E);
+            // one block row per group of four experts (E <= 256), about 16 blocks of 256 threads
+            // per SM in all
+            const int groups = (c.E + 3) / 4;
+            const int gx = std::min(ceil_div(c.T, 256), std::max(1, num_sms() * 16 / groups));
+            const dim3 grid((unsigned)gx, (unsigned)groups);
             st = launch_pdl(noise_kernel, grid, dim3(256), 0, s, c.T, c.E, c.noise_seed, noise);
             count_launch();
             if (st != cudaSuccess) return st;

@@ -43,6 +43,15 @@ struct RouteTcParams {
 
 __host__ __device__ constexpr int route_stage_bytes(int E_pad) { return RBM * RBK * 2 + E_pad * RBK * 2; }
 
+// The routing-noise draws of experts c .. c + 31 for one token ([E, T] layout; zero past E or
+// without a token), all loaded before the chunk's stores so that the 32 loads overlap instead
+// of each waiting behind the previous expert's stores.
+__device__ __forceinline__ void load_noise32(const float* __restrict__ noise, int T, int E, int c, int tok,
+                                             bool live, float (&nz)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) nz[i] = (live && c + i < E) ? __ldg(noise + (size_t)(c + i) * T + tok) : 0.f;
+}
+
 template <int K>
 __global__ void __launch_bounds__(RTHREADS, 1)
 route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
@@ -152,6 +161,8 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     float* wr = p.w + (size_t)(live ? tok : 0) * p.E;
                     float m = -INFINITY;
                     for (int c = 0; c < p.E_pad; c += 32) {   // warp-uniform TMEM loads
+                        float nz[32];
+                        load_noise32(p.noise, p.T, p.E, c, tok, live, nz);
                         uint32_t r[32];
                         tmem_ld32(taddr + c, r);
                         tmem_ld_wait();
@@ -159,8 +170,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                         for (int i = 0; i < 32; ++i) {
                             const int e = c + i;
                             if (e < p.E && live) {
-                                const float v = fmaf(p.noise_std, p.noise[(size_t)e * p.T + tok],
-                                                     __uint_as_float(r[i]) + s_bias[e]);
+                                const float v = fmaf(p.noise_std, nz[i], __uint_as_float(r[i]) + s_bias[e]);
                                 if (p.logits) p.logits[(size_t)tok * p.E + e] = v;
                                 wr[e] = v;
                                 m = fmaxf(m, v);
@@ -212,6 +222,8 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
             for (int j = 0; j < K; ++j) { tv[j] = -INFINITY; te[j] = -1; }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
             for (int c = 0; c < p.E_pad; c += 32) {
+                float nz[32];
+                if (p.noise) load_noise32(p.noise, p.T, p.E, c, tok, tok < p.T, nz);
                 uint32_t r[32];
                 tmem_ld32(taddr + c, r);
                 tmem_ld_wait();
@@ -220,7 +232,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     int e = c + i;
                     if (e < p.E) {
                         float v = __uint_as_float(r[i]) + s_bias[e];
-                        if (p.noise && tok < p.T) v = fmaf(p.noise_std, p.noise[(size_t)e * p.T + tok], v);
+                        if (p.noise && tok < p.T) v = fmaf(p.noise_std, nz[i], v);
                         if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
                         // insert into the list sorted by (logit desc, id asc); experts arrive in
                         // ascending id, so an equal logit never displaces an earlier one
