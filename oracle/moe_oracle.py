@@ -20,7 +20,7 @@ Sources (pages cited by title and section):
   pre-selection then soft weights over those 8), section 4.2 idea 2 (tokens written straight
   into per-expert bucket offsets), section 5.5 (routing in FP32 precision).
 
-Readings where the pages are silent or ambiguous (each is also listed in the design doc):
+Readings where the pages are silent or ambiguous:
 * weights: top-k on logits, then softmax(z_sel / temperature) over the k selected (PithTrain
   4.1; temperature 1 for plain top-k). Indices equal those of softmax-then-top-k.
 * ties in top-k go to the lower expert id; slot j holds the j-th largest logit.
