@@ -280,6 +280,23 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def max_over_ranks(values, world, device=None):
+    """Per-rank timings -> the maximum of each over all ranks (every rank gets the same list).
+    One process per GPU: the job is as slow as its slowest replica."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: every replica's tokens over the slowest replica's step time."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def cpu_baseline(cfg, tokens):
     """The fp64 oracle, as it stands, on one batch of `tokens` tokens of the same workload."""
     sample, npin = oracle_sample_inputs(cfg, tokens)
@@ -480,10 +497,7 @@ def run_ours(args, cfg):
         torch.distributed.barrier()
     launches = graph.launches_per_step * args.steps
     ms = sum(a.elapsed_time(z) for a, z in zip(ev0, ev1)) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([ms], world, dev)[0]
 
     # end to end through the public API: every step copies its x and dy from pinned host memory
     # and reads its loss back to pinned host memory. Sequential: copy, step, read back, one after
@@ -546,10 +560,7 @@ def run_ours(args, cfg):
 
     pipelined(args.warmup)
     e2e = pipelined(args.steps)
-    if world > 1:
-        t = torch.tensor([e2e, e2e_seq], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e, e2e_seq = float(t[0].item()), float(t[1].item())
+    e2e, e2e_seq = max_over_ranks([e2e, e2e_seq], world, dev)
 
     extras = time_extras(moe, c, cfg, d_in, b, flush, stream, args.steps) if not args.no_extras else None
 
@@ -565,7 +576,7 @@ def run_ours(args, cfg):
             gbs = work[key] / (stage_ms[stage] * 1e-3) / 1e9
             hbm[stage] = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "algorithmic_mb": work[key] / 1e6}
         line = {
-            "metric": METRIC, "value": cfg.T * world / (ms * 1e-3), "unit": "tokens/s",
+            "metric": METRIC, "value": job_tokens_per_s(cfg.T, world, ms), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic",
@@ -586,13 +597,13 @@ def run_ours(args, cfg):
             "stage_ms": stage_ms,
             "ms_per_step_eager": eager_ms,
             "timing": "CUDA-graph replay of the five C-ABI calls; stage_ms: each call as its own graph",
-            "e2e": {"value": cfg.T * world / (e2e * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e), "unit": "tokens/s",
                     "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
                     "d2h_bytes_per_step": 4,
                     "timing": "pipelined: step i+1's x and dy copied on a copy stream during step i "
                               "(two input buffers, one captured step each); every step's loss copied "
                               "back; events around the whole timed sequence; no L2 flush (working set > L2)",
-                    "sequential_tokens_per_s": cfg.T * world / (e2e_seq * 1e-3)},
+                    "sequential_tokens_per_s": job_tokens_per_s(cfg.T, world, e2e_seq)},
             "extras": extras,
             "gpu_launches": int(launches),
             "wall_s_timed": t_wall,
