@@ -167,6 +167,13 @@ cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s
     return c.row_align == 256 ? launch_row_gemm_tc_pair(c, a, s) : launch_row_gemm_tc(c, a, s);
 }
 cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
+    if (c.rows_capacity == 0) {
+        // no expert rows at all (an empty batch): every weight gradient is zero, and no
+        // operand is touched
+        const long long n = (long long)a.E * a.M * a.N;
+        if (a.f32 || c.dtype != MOE_BF16) return launch_fill(static_cast<float*>(a.C), n, 0.f, s);
+        return launch_fill(static_cast<uint16_t*>(a.C), n, (uint16_t)0, s);   // bf16 +0.0
+    }
     return use_tc(c) ? launch_wgrad_tc_pair(c, a, s) : launch_wgrad_simt(c, a, s);
 }
 
