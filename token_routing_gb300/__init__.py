@@ -10,6 +10,6 @@ from ._lib import (MoeConfig, MoeError, LIB_PATH, HEADER_PATH, load, header_symb
 from .layer import (make_config, config_from, workspace_bytes, alloc_buffers, route,  # noqa: F401
                     dispatch, expert_ffn, combine, backward, forward, forward_backward, coselect,
                     soft_balance, soft_balance_backward,
-                    get_error, kernel_launches, StepGraph)
+                    get_error, kernel_launches, selftest_wait_timeout, StepGraph)
 
 __version__ = "0.1"

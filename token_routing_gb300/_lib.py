@@ -62,6 +62,7 @@ _SIGS = {
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_kernel_launches": (ctypes.c_uint64, []),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, _P, _P, _P]),
 }
 
 _lib = None

@@ -42,34 +42,6 @@ struct SortArgs {
     int* err;
 };
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid barrier: returns false (and records a device error) if the wait ran out.
-__device__ bool grid_barrier(unsigned* bar, unsigned target, int* err) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        s_ok = 1;
-        __threadfence();
-        atomicAdd(bar, 1u);
-        const long long t0 = clock64();
-        while (ld_acquire_u32(bar) < target) {
-            if (clock64() - t0 > kSpinBudgetCycles) {
-                raise_error(err, kErrTimeout);
-                s_ok = 0;
-                break;
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
 // Exclusive scan of n <= blockDim.x values in shared memory (blockDim.x = 256); returns the total.
 __device__ int block_exclusive_scan(int* buf, int n) {
     __shared__ int s_tot;

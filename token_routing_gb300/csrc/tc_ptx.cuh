@@ -38,11 +38,12 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait on a barrier phase; false (and a device error) when the budget runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          long long budget = kSpinBudgetCycles) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try(bar, parity)) {
-        if (clock64() - t0 > kSpinBudgetCycles) {
+        if (clock64() - t0 > budget) {
             raise_error(err, kErrTimeout);
             return false;
         }

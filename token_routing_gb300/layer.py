@@ -137,6 +137,13 @@ def forward_backward(cfg, p, x, dy, b, stream=None):
     backward(cfg, dy, x, p["Wg"], p["W1"], p["W2"], b, stream)
 
 
+def selftest_wait_timeout(mode, budget_cycles, timed_out, scratch, stream=None):
+    """moe_selftest_wait_timeout: a bounded device wait that nothing satisfies (mode 0: an
+    mbarrier phase, mode 1: a grid barrier); read the resulting timeout with get_error()."""
+    L.check("moe_selftest_wait_timeout", L.load().moe_selftest_wait_timeout(
+        int(mode), int(budget_cycles), _p(timed_out), _p(scratch), _s(stream)))
+
+
 def get_error(stream=None):
     """Synchronise and report (and clear) the device error word."""
     L.check("moe_get_error", L.load().moe_get_error(_s(stream)))
