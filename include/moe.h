@@ -103,9 +103,11 @@ typedef struct {
     float noise_std;           /* >= 0: training-time routing noise, logits += noise_std * N(0,1)
                                   before top-k and softmax ("PyTorch distributed MoE training",
                                   section 4.3: randn_like(logits) * 0.1); 0 = off */
-    uint32_t noise_seed;       /* noise of (token t, expert e): Philox4x64-10 at counter
-                                  (t, e, 0, 0), key (noise_seed, 0); top 24 bits of the first
-                                  two outputs -> u1, u2 in (0,1]; sqrt(-2 ln u1) cos(2 pi u2).
+    uint32_t noise_seed;       /* noise of experts 4g .. 4g+3 of token t: one Philox4x64-10
+                                  draw at counter (t, g, 0, 0), key (noise_seed, 0); the top
+                                  24 bits of outputs (0, 1) and (2, 3) give two pairs u1, u2 in
+                                  (0,1], each turned into sqrt(-2 ln u1) cos(2 pi u2) and
+                                  sqrt(-2 ln u1) sin(2 pi u2), in that order.
                                   Vary the seed from step to step. */
     /* derived by moe_config_init */
     int32_t capacity;          /* ceil(capacity_factor*T*k/E) in double, or INT32_MAX */
