@@ -28,7 +28,7 @@ constexpr int RTHREADS = 192;
 
 struct RouteTcParams {
     int T, d, E, E_pad, stages;
-    int rows;          // tokens per CTA: 128, or 64 when 128-token tiles would leave SMs idle
+    int rows;          // tokens per CTA (RBM)
     float inv_temp;
     float noise_std;
     uint32_t noise_seed;
@@ -73,16 +73,6 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
     const int tok0 = blockIdx.x * p.rows;
     const int kblocks = (p.d + RBK - 1) / RBK;
     const uint32_t ncols = p.E_pad <= 32 ? 32 : p.E_pad <= 64 ? 64 : p.E_pad <= 128 ? 128 : 256;
-
-    // With 64-token tiles the MMA still runs M = 128: rows 64..127 of every stage's A tile are
-    // zeroed once (TMA fills only the first 64) and their accumulator rows are ignored.
-    if (p.rows < RBM) {
-        for (int s = 0; s < RSTAGES; ++s) {
-            uint4* a = reinterpret_cast<uint4*>(smem + s * stage_bytes + p.rows * RBK * 2);
-            for (int i = threadIdx.x; i < (RBM - p.rows) * RBK * 2 / 16; i += blockDim.x) a[i] = make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
 
     for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_cnt[e] = 0;
     if (threadIdx.x == 0) {
@@ -302,13 +292,14 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     p.idx = idx; p.w = w; p.counts = counts; p.logits = logits;
     p.noise = noise;
     p.err = device_error_word();
-    p.rows = (long long)c.T >= (long long)RBM * num_sms() ? RBM : 64;
+    // 128-token tiles with the full ring: 64-token tiles (twice the CTAs, two per SM, half the
+    // ring each) measured slower, 21 against 20 us per route call at 8192 tokens and 38 against
+    // 32 us at 16384 tokens and 128 experts
+    p.rows = RBM;
     CUtensorMap tx, tw;
     if (!make_map(&tx, x, (uint64_t)c.d, (uint64_t)c.T, (uint32_t)p.rows)) return cudaErrorInvalidValue;
     if (!make_map(&tw, Wg, (uint64_t)c.d, (uint64_t)c.E, (uint32_t)p.E_pad)) return cudaErrorInvalidValue;
-    // 64-token tiles fit two CTAs per SM (half the shared memory each)
-    const int budget = p.rows < RBM ? RSMEM_BUDGET / 2 : RSMEM_BUDGET;
-    p.stages = std::max(2, std::min(RMAX_STAGES, budget / route_stage_bytes(p.E_pad)));
+    p.stages = std::max(2, std::min(RMAX_STAGES, RSMEM_BUDGET / route_stage_bytes(p.E_pad)));
     const size_t smem = 1024 + (size_t)p.stages * route_stage_bytes(p.E_pad) +
                         (2 * RMAX_STAGES + 4) * sizeof(uint64_t) + 16 + 2 * MOE_MAX_EXPERTS * sizeof(int);
     if (dense_routing(c)) return launch_k<0>(p, tx, tw, smem, s);
