@@ -1,6 +1,7 @@
 // C ABI of the MoE layer library: argument validation, workspace layout and the order of
-// kernel launches for each entry point. The arithmetic lives in router.cu, dispatch.cu,
-// gemm_tc.cu / gemm_simt.cu and combine.cu.
+// kernel launches for each entry point. The arithmetic lives in router_tc.cu / router.cu,
+// dispatch.cu, gemm_tc_pair.cu / gemm_tc.cu / gemm_simt.cu, combine.cu, soft_balance.cu and
+// coselect.cu.
 #include <climits>
 #include <cmath>
 #include <initializer_list>
