@@ -17,8 +17,9 @@ Sources (pages cited by title and section):
   mean((load - mean(load))^2)), section 4.3 (aux_loss_weight = 0.01).
 * "Expert Parallelism: Scaling Mixture-of-Experts Models" (Expert-Parallelism page),
   section 2.2 (g = softmax(gate(x) / temperature), y = sum_i g_i expert_i(x); hybrid: top-8
-  pre-selection then soft weights over those 8), section 4.2 idea 2 (tokens written straight
-  into per-expert bucket offsets), section 5.5 (routing in FP32 precision).
+  pre-selection then soft weights over those 8), section 2.3 (load statistics averaged over a
+  sliding window of the last 100 batches), section 4.2 idea 2 (tokens written straight into
+  per-expert bucket offsets), section 5.5 (routing in FP32 precision).
 
 Readings where the pages are silent or ambiguous:
 * weights: top-k on logits, then softmax(z_sel / temperature) over the k selected (PithTrain
@@ -36,6 +37,10 @@ Readings where the pages are silent or ambiguous:
 * GELU is the exact erf form (nn.GELU default).
 * the loss the layer reports is sum(y * dy) + aux_loss_weight * balance_loss; dy is the
   gradient seed.
+* sliding window: the window holds the soft loads of the current batch and the W - 1 batches
+  before it (all batches so far until W have been seen); the loss is the soft balance loss of
+  their mean, and its gradient reaches only the current batch (earlier batches are stored
+  statistics).
 
 Every function below is pinned by tests/test_oracle_pins.py and tests/test_oracle_grad.py
 against closed forms, hand-worked examples (tests/golden/), brute force on tiny inputs and
@@ -160,19 +165,29 @@ def routing_noise(T, E, seed):
     return n
 
 
-def route(x, Wg, bg, k, temperature=1.0, noise_std=0.0, noise_seed=0):
+def route(x, Wg, bg, k, temperature=1.0, noise_std=0.0, noise_seed=0, idx=None):
     """Gate linear, top-k, softmax over the k, counts and balance loss. With noise_std > 0 the
     logits get noise_std * N(0,1) before the selection and the softmax (training-time routing
     noise, PyTorch-MoE page, section 4.3: logits + randn_like(logits) * 0.1); the noise is a
-    constant for the backward."""
+    constant for the backward.
+
+    `idx` [T,k] (optional) replaces the top-k selection with a given one; everything after the
+    selection (weights over the selected logits, counts, balance loss) follows from it as
+    usual. A token whose neighbouring logits nearly tie has more than one correct selection
+    under rounding; this lets the rest of the layer be evaluated on either."""
     z = gate_logits(x, Wg, bg)
     if noise_std > 0:
         z = z + noise_std * routing_noise(z.shape[0], z.shape[1], noise_seed)
     if k == z.shape[1]:
-        idx, z_sel, gap = select_all(z)
+        idx_d, z_sel, gap = select_all(z)
     else:
-        idx, z_sel = select_topk(z, k)
+        idx_d, z_sel = select_topk(z, k)
         gap = topk_gap(z, k)
+    if idx is None:
+        idx = idx_d
+    else:
+        idx = np.asarray(idx, dtype=np.int64).reshape(z.shape[0], k)
+        z_sel = np.take_along_axis(z, idx, axis=1)
     w = routing_weights(z_sel, temperature)
     counts = expert_counts(idx, z.shape[1])
     return dict(z=z, idx=idx, z_sel=z_sel, w=w, gap=gap, counts=counts,
@@ -277,12 +292,13 @@ def combine(Yp, w, slot_row, T):
 
 # ----------------------------------------------------------------------------- whole layer
 
-def forward(inp, k, temperature=1.0, C=None, align=1, noise_std=0.0, noise_seed=0):
-    """Forward of the layer. `inp` holds x, Wg, bg, W1, b1, W2, b2 (any array type)."""
+def forward(inp, k, temperature=1.0, C=None, align=1, noise_std=0.0, noise_seed=0, idx=None):
+    """Forward of the layer. `inp` holds x, Wg, bg, W1, b1, W2, b2 (any array type); `idx`
+    (optional) is a given top-k selection (see route)."""
     x = _f64(inp["x"])
     T = x.shape[0]
     E = np.asarray(inp["Wg"]).shape[0]
-    r = route(x, inp["Wg"], inp.get("bg"), k, temperature, noise_std, noise_seed)
+    r = route(x, inp["Wg"], inp.get("bg"), k, temperature, noise_std, noise_seed, idx=idx)
     dsp = dispatch(r["idx"], E, C, align)
     Xp = permute(x, dsp["row_token"])
     f = np.asarray(inp["W1"]).shape[1]
@@ -426,5 +442,40 @@ def soft_balance_grad(z, temperature, weight):
     p, P = soft_load(z, temperature)
     E = P.shape[0]
     g = weight * 2.0 * (P - P.mean()) / E
+    s = (p * g[None, :]).sum(axis=1, keepdims=True)
+    return p * (g[None, :] - s) / temperature
+
+
+# ----------------------------------------------------------------------------- sliding window
+
+def sliding_windows(loads, W):
+    """The windows of a sequence of batches (Expert-Parallelism page, section 2.3: the expert
+    load statistics are taken over the last 100 batches instead of one batch). `loads` lists
+    the soft loads P [E] of successive batches; window i holds batches max(0, i - W + 1) .. i,
+    oldest first: the current batch and the W - 1 before it (fewer at the start)."""
+    loads = [_f64(P) for P in loads]
+    return [np.stack(loads[max(0, i - W + 1):i + 1]) for i in range(len(loads))]
+
+
+def window_balance_loss(P_window, weight):
+    """Balance loss on the window mean: Pbar = mean over the window's batches of the soft load,
+    loss = weight * mean_e (Pbar_e - mean(Pbar))^2 (the soft_balance_loss form applied to
+    Pbar). Returns (Pbar [E], loss)."""
+    Pbar = _f64(P_window).mean(axis=0)
+    return Pbar, float(weight * np.mean((Pbar - Pbar.mean()) ** 2))
+
+
+def window_balance_grad(z, temperature, weight, P_window):
+    """d window_balance_loss / d z [T, E] of the current batch (the last row of P_window, whose
+    soft load is that of z). Earlier batches are stored statistics, constants here, so the
+    gradient reaches only the current batch: dloss/dP_now,e = g_e = weight * 2 (Pbar_e -
+    mean Pbar) / (E n) with n the window's batch count (the mean term drops out since
+    sum_e (Pbar_e - mean Pbar) = 0), then the softmax Jacobian per token,
+    dz_te = p_te (g_e - sum_j p_tj g_j) / temperature."""
+    p, _ = soft_load(z, temperature)
+    P_window = _f64(P_window)
+    n, E = P_window.shape
+    Pbar = P_window.mean(axis=0)
+    g = weight * 2.0 * (Pbar - Pbar.mean()) / (E * n)
     s = (p * g[None, :]).sum(axis=1, keepdims=True)
     return p * (g[None, :] - s) / temperature

@@ -138,3 +138,44 @@ def test_soft_balance_closed_forms():
     rng = np.random.default_rng(4)
     zz = rng.standard_normal((T, E))
     np.testing.assert_allclose(O.soft_balance_grad(zz, 0.5, 2.0).sum(axis=1), 0.0, atol=1e-12)
+
+
+def test_window_of_one_batch_is_the_soft_balance_loss():
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((9, 6))
+    _, P = O.soft_load(z, 0.7)
+    Pb, lo = O.window_balance_loss(P[None, :], 0.3)
+    np.testing.assert_array_equal(Pb, P)
+    assert lo == pytest.approx(O.soft_balance_loss(P, 0.3), rel=1e-14)
+    np.testing.assert_allclose(O.window_balance_grad(z, 0.7, 0.3, P[None, :]),
+                               O.soft_balance_grad(z, 0.7, 0.3), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("n_past", [0, 2, 4])
+def test_window_balance_gradient_matches_central_differences(n_past):
+    """The loss as a function of the current batch's logits, the past batches' loads fixed:
+    its central differences equal window_balance_grad (a missing 1/n, a wrong mean or a
+    dropped softmax term would fail)."""
+    rng = np.random.default_rng(20 + n_past)
+    T, E, temp, weight, W = 7, 5, 0.6, 0.9, 3
+    z = rng.standard_normal((T, E))
+    past = [rng.random(E) * T for _ in range(n_past)]
+
+    def loss_of(zz):
+        _, P = O.soft_load(zz, temp)
+        win = O.sliding_windows(past + [P], W)[-1]
+        return O.window_balance_loss(win, weight)[1]
+
+    _, P = O.soft_load(z, temp)
+    win = O.sliding_windows(past + [P], W)[-1]
+    assert win.shape[0] == min(n_past + 1, W)
+    g = O.window_balance_grad(z, temp, weight, win)
+    h = 1e-6
+    num = np.zeros_like(z)
+    for t in range(T):
+        for e in range(E):
+            zp, zm = z.copy(), z.copy()
+            zp[t, e] += h
+            zm[t, e] -= h
+            num[t, e] = (loss_of(zp) - loss_of(zm)) / (2 * h)
+    np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-9)

@@ -474,3 +474,85 @@ def test_noisy_route_is_plain_route_of_noisy_logits():
     np.testing.assert_allclose(noisy["w"], O.routing_weights(zsel), atol=1e-15)
     plain = O.route(inp["x"], inp["Wg"], None, 2, 1.0, noise_std=0.0, noise_seed=5)
     assert (plain["idx"] == O.select_topk(O.gate_logits(inp["x"], inp["Wg"]), 2)[0]).all()
+
+
+# ------------------------------------------------------------------ a given selection
+
+def test_given_selection_reproduces_the_oracle_selection():
+    """forward(idx = its own selection) is the same computation, value for value."""
+    inp = _rand_inputs(60, 12, 6, 10, seed=31)
+    C = O.capacity(1.0, 60, 2, 6)
+    a = O.forward(inp, 2, 0.7, C, align=4)
+    b = O.forward(inp, 2, 0.7, C, align=4, idx=a["idx"])
+    for key in ("idx", "w", "counts", "kept", "offsets", "slot_row", "row_token", "y"):
+        assert np.array_equal(a[key], b[key]), key
+    assert a["balance_loss"] == b["balance_loss"]
+
+
+def test_given_selection_on_an_exact_tie():
+    """Two experts with equal logits: either order is a correct top-2. The oracle's own
+    selection takes the lower id first; given the other order, the weights, counts and the
+    layout follow that order. Hand-worked: logits (1, 3, 3, 0), temperature 1, so both
+    selected weights are 1/2 whichever expert takes slot 0."""
+    x = np.array([[1.0, 0.0], [0.0, 1.0]])
+    Wg = np.array([[1.0, 0.0], [3.0, 3.0], [3.0, 3.0], [0.0, 0.0]])
+    z = O.gate_logits(x, Wg)
+    np.testing.assert_array_equal(z[0], [1.0, 3.0, 3.0, 0.0])
+    r_own = O.route(x, Wg, None, 2)
+    assert r_own["idx"][0].tolist() == [1, 2]
+    given = r_own["idx"].copy()
+    given[0] = [2, 1]
+    r = O.route(x, Wg, None, 2, idx=given)
+    assert r["idx"][0].tolist() == [2, 1]
+    np.testing.assert_allclose(r["w"][0], [0.5, 0.5], rtol=0, atol=1e-15)
+    assert r["counts"].tolist() == r_own["counts"].tolist()
+    d = O.dispatch(r["idx"], 4, None, 1)
+    # token 0's slot 0 now holds expert 2: its row sits in expert 2's bucket
+    assert d["slot_row"][0, 0] == d["offsets"][2]
+
+
+def test_valid_selection_helper():
+    """The parity tests' check that a near-tie token's GPU selection is a correct top-k."""
+    import parity as P
+    z = np.array([[0.5, 0.2, 0.2 + 5e-6, -1.0],
+                  [0.0, 1.0, 2.0, 3.0]])
+    # token 0: experts 1 and 2 nearly tie for slot 1; token 1 has no tie
+    assert P.valid_selection(z, [[0, 2], [3, 2]], 2).tolist() == [True, True]
+    assert P.valid_selection(z, [[0, 1], [3, 2]], 2).tolist() == [True, True]   # within the gap
+    assert P.valid_selection(z, [[0, 3], [2, 3]], 2).tolist() == [False, False]  # not the top-2
+    assert P.valid_selection(z, [[0, 0], [3, 3]], 2).tolist() == [False, False]  # repeated id
+    assert P.valid_selection(z, [[0, 4], [3, -1]], 2).tolist() == [False, False]  # out of range
+    assert P.valid_selection(z, [[2, 0], [2, 3]], 2).tolist() == [False, False]  # slot order
+
+
+# ------------------------------------------------------------------ sliding-window balance loss
+
+def test_golden_sliding_window_balance():
+    g = _load("sliding_window_balance_hand.json")
+    wins = O.sliding_windows(g["loads"], g["W"])
+    assert [w.tolist() for w in wins] == g["windows"]
+    for win, Pbar, loss, gexp in zip(wins, g["Pbar"], g["loss"], g["g"]):
+        Pb, lo = O.window_balance_loss(win, g["weight"])
+        np.testing.assert_allclose(Pb, Pbar, rtol=0, atol=1e-15)
+        assert lo == pytest.approx(loss, abs=1e-15)
+        # dloss / dP_now (the window's last row) by central differences: g_e = w 2 (Pbar_e - m) / (E n)
+        h = 1e-4
+        num = []
+        for e in range(len(Pbar)):
+            up, dn = win.copy(), win.copy()
+            up[-1, e] += h
+            dn[-1, e] -= h
+            num.append((O.window_balance_loss(up, g["weight"])[1] - O.window_balance_loss(dn, g["weight"])[1]) / (2 * h))
+        np.testing.assert_allclose(num, gexp, rtol=0, atol=1e-12)
+
+
+def test_window_before_it_fills_holds_every_batch():
+    """With the page's window of 100 batches, the first batches average all batches so far."""
+    rng = np.random.default_rng(3)
+    loads = [rng.random(6) * 10 for _ in range(5)]
+    for i, win in enumerate(O.sliding_windows(loads, 100)):
+        assert win.shape == (i + 1, 6)
+        np.testing.assert_array_equal(win, np.stack(loads[:i + 1]))
+    # and a full ring keeps only the last W, oldest first
+    wins = O.sliding_windows(loads, 2)
+    np.testing.assert_array_equal(wins[4], np.stack([loads[3], loads[4]]))
