@@ -1,11 +1,13 @@
 """Throughput of the MoE layer (forward + backward) on GB300, through the C ABI.
 
 One step = route -> dispatch -> expert_ffn -> combine -> backward over one batch of the
-workload (default: top-2 over 16 experts, T=8192, d=1024, d_ff=4096, capacity 1.0, bf16).
+workload (default: hybrid routing, top-8 pre-selection over 128 experts then softmax(z/0.2)
+over the 8, T=16384, d=1024, d_ff=4096, no capacity limit, bf16: 131,072 expert rows).
 The step is captured once into a CUDA graph (the same five C-ABI calls) and replayed;
-an eager pass gives the per-call times. Inputs are resident in HBM when the timed region
-starts; L2 is flushed (a 256 MB write)
-before every timed step, outside the step's events. Prints one JSON line.
+each call replayed as its own graph gives the per-call times, and a kernel trace (timing
+events around every launch) gives each kernel's own device time. Inputs are resident in
+HBM when the timed region starts; L2 is flushed (a 256 MB write) before every timed step,
+outside the step's events. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -256,6 +258,77 @@ def algorithmic_counts(cfg, kept_rows):
     )
 
 
+GEMM_KINDS = {0: "ffn1", 1: "ffn2", 2: "dH", 3: "dX", 4: "wgrad", 5: "accum", 6: "wgrad_f32"}
+
+
+def kernel_family(name):
+    """Short label of a traced kernel name: the tcgen05 GEMMs by their epilogue kind (first
+    template argument), everything else by its base name."""
+    import re
+    m = re.match(r"(tc_gemm_pair_kernel|tc_gemm_kernel)<(\d+)", name)
+    if m:
+        return GEMM_KINDS.get(int(m.group(2)), "gemm" + m.group(2))
+    return name.split("<")[0]
+
+
+def summarise_trace(records_per_step):
+    """[[(name, ms), ...] per step] -> {family: {"launches_per_step", "us_per_launch", "us_per_step"}}."""
+    steps = len(records_per_step)
+    acc = {}
+    for recs in records_per_step:
+        for name, ms in recs:
+            f = kernel_family(name)
+            a = acc.setdefault(f, {"n": 0, "ms": 0.0, "names": set()})
+            a["n"] += 1
+            a["ms"] += ms
+            a["names"].add(name)
+    out = {}
+    for f, a in acc.items():
+        out[f] = {"launches_per_step": a["n"] / steps, "us_per_launch": a["ms"] * 1e3 / a["n"],
+                  "us_per_step": a["ms"] * 1e3 / steps, "kernels": sorted(a["names"])}
+    return out
+
+
+def kernel_rooflines(cfg, kept, trace, peaks):
+    """Algorithmic work of the path's main kernels over their own device time (from the
+    kernel trace). Memory kernels against the measured HBM copy rate (bytes: reads + writes
+    the operation needs once); the tcgen05 GEMMs against the measured burst bf16 rate (each
+    traced kernel runs alone). Work per launch, N = kept assignments:
+      route_tc_kernel     T d es + E d es + T k 8            (x, Wg in; idx, w out)
+      sort + gather       T d es + N d es + 4 (N + T k)      (the permute)
+      combine_kernel      N d es + T d es + T k 8
+      combine_bwd_kernel  T d es + 2 N d es + T k 12         (dy, Yp, w, slot_row in; dYp, dw out)
+      router_bwd_kernel   N d es + T d es + T k 12           (dXp, routing in; dx out)
+      each expert GEMM    2 N d d_ff flop (Ffn1, Ffn2, dH, dX, each of the two weight gradients)"""
+    es = 2 if cfg.dtype == "bf16" else 4
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.d_ff
+    N = kept
+    mem = {
+        "route": (["route_tc_kernel", "route_kernel"], T * d * es + E * d * es + T * k * 8.0),
+        "dispatch": (["sort_kernel", "gather_kernel", "dense_layout_kernel"], T * d * es + N * d * es + 4.0 * (N + T * k)),
+        "combine": (["combine_kernel"], N * d * es + T * d * es + T * k * 8.0),
+        "combine_bwd": (["combine_bwd_kernel"], T * d * es + 2.0 * N * d * es + T * k * 12.0),
+        "router_bwd": (["router_bwd_kernel", "router_bwd_wide_kernel"], N * d * es + T * d * es + T * k * 12.0),
+    }
+    out = {}
+    for label, (fams, nbytes) in mem.items():
+        us = sum(trace[f]["us_per_step"] for f in fams if f in trace)
+        if us <= 0:
+            continue
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[label] = {"kernels": [f for f in fams if f in trace], "us": us, "algorithmic_mb": nbytes / 1e6,
+                      "gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "bound": "hbm"}
+    for fam in ("ffn1", "ffn2", "dH", "dX", "wgrad"):
+        if fam not in trace:
+            continue
+        t = trace[fam]
+        flops = 2.0 * N * d * f
+        tf = flops / (t["us_per_launch"] * 1e-6) / 1e12
+        out[fam] = {"us": t["us_per_launch"], "launches_per_step": t["launches_per_step"],
+                    "tflops": tf, "frac": tf / peaks["bf16_tflops"], "bound": "tensor"}
+    return out
+
+
 def oracle_step(cfg, npin):
     from oracle import moe_oracle as O
     C = O.capacity(cfg.capacity_factor, cfg.T, cfg.k, cfg.E)
@@ -382,6 +455,40 @@ def time_extras(moe, c, cfg, d_in, b, flush, stream, steps):
     return out
 
 
+def profile_call(args, moe, c, d_in, b, flush, stream, forward_only):
+    """For a profiler run: `--warmup` eager forward (+ backward) steps, then `--steps` calls of
+    the one C-ABI call named by --profile, each after an L2 flush; prints no JSON line."""
+    import torch
+
+    def fwd():
+        moe.route(c, d_in["x"], d_in["Wg"], d_in["bg"], b, stream)
+        moe.dispatch(c, b["idx"], d_in["x"], b, stream)
+        moe.expert_ffn(c, b["Xp"], b["offsets"], d_in["W1"], d_in["b1"], d_in["W2"], d_in["b2"], b, stream)
+        moe.combine(c, b["Yp"], b["slot_row"], b["w"], b["y"], stream)
+
+    calls = {
+        "route": lambda: moe.route(c, d_in["x"], d_in["Wg"], d_in["bg"], b, stream),
+        "dispatch": lambda: moe.dispatch(c, b["idx"], d_in["x"], b, stream),
+        "expert_ffn": lambda: moe.expert_ffn(c, b["Xp"], b["offsets"], d_in["W1"], d_in["b1"], d_in["W2"],
+                                             d_in["b2"], b, stream),
+        "combine": lambda: moe.combine(c, b["Yp"], b["slot_row"], b["w"], b["y"], stream),
+        "backward": lambda: moe.backward(c, d_in["dy"], d_in["x"], d_in["Wg"], d_in["W1"], d_in["W2"], b, stream),
+    }
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        if not forward_only:
+            calls["backward"]()
+    for _ in range(args.steps):
+        flush.zero_()
+        calls[args.profile]()
+    torch.cuda.synchronize()
+    moe.get_error(stream)
+    print(f"profiled {args.profile} x{args.steps} after {args.warmup} warm-up steps "
+          f"({c.T} tokens, {moe.kernel_launches()} kernel launches in all)", file=sys.stderr)
+    return 0
+
+
 def run_ours(args, cfg):
     import torch
     import synth
@@ -399,9 +506,12 @@ def run_ours(args, cfg):
     inp = synth.make_inputs(cfg, seed=cfg.seed + rank)
     d_in = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     c = moe.config_from(cfg)
-    b = moe.alloc_buffers(c, device=dev, backward=True)
+    forward_only = args.profile in ("route", "dispatch", "expert_ffn", "combine")
+    b = moe.alloc_buffers(c, device=dev, backward=not forward_only)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if args.profile:
+        return profile_call(args, moe, c, d_in, b, flush, stream, forward_only)
 
     names = ["route", "dispatch", "expert_ffn", "combine", "backward"]
 
@@ -455,6 +565,18 @@ def run_ours(args, cfg):
             if i >= 2:
                 stage_ms[n] += e0.elapsed_time(e1) / args.steps
     moe.get_error(stream)
+    # kernel trace: every kernel's own device time (timing events around each launch on its
+    # stream), eager steps with L2 flushed before each
+    trace_recs = []
+    for i in range(args.steps + 1):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        with moe.KernelTrace(512) as tr:
+            step()
+        if i >= 1:
+            trace_recs.append(tr.records)
+    moe.get_error(stream)
+    trace = summarise_trace(trace_recs)
     # eager pass (plain calls, host launch gaps included) for reference
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -569,7 +691,8 @@ def run_ours(args, cfg):
         work = algorithmic_counts(cfg, kept)
         ffn_s = stage_ms["expert_ffn"] * 1e-3
         gemm_tflops = work["ffn_fwd_flops"] / ffn_s / 1e12
-        peak_tc = peaks["bf16_tflops_sustained"]
+        # expert_ffn is timed as its own graph replay, between L2 flushes: the burst peak
+        peak_tc = peaks["bf16_tflops"]
         permute_gbs = work["permute_bytes"] / (stage_ms["dispatch"] * 1e-3) / 1e9
         hbm = {}
         for stage, key in (("route", "router_bytes"), ("dispatch", "permute_bytes"), ("combine", "combine_bytes")):
@@ -588,15 +711,23 @@ def run_ours(args, cfg):
             "roofline": {"kernel": "tcgen05 grouped GEMM, forward pair (GEMM1+GELU, GEMM2)",
                          "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": gemm_tflops / peak_tc,
-                         "peak_source": f"{peaks['src']} bf16 sustained",
+                         "peak_source": f"{peaks['src']} bf16 burst (the call is timed alone)",
+                         "units": f"4 N d d_ff flop per call, N = {kept} kept assignments",
+                         "call_us": stage_ms["expert_ffn"] * 1e3,
+                         "kernel_us": sum(trace[f]["us_per_step"] for f in ("ffn1", "ffn2") if f in trace),
                          "traffic": measured_traffic(cfg.name)},
+            "kernel_roofline": kernel_rooflines(cfg, kept, trace, peaks),
+            "kernel_trace": {f: {kk: (round(v, 2) if isinstance(v, float) else v) for kk, v in t.items()}
+                             for f, t in sorted(trace.items(), key=lambda kv: -kv[1]["us_per_step"])},
             "grouped_gemm_pct_bf16_peak": 100.0 * gemm_tflops / peak_tc,
             "permute_gbs": permute_gbs,
             "permute_frac_hbm": permute_gbs / peaks["hbm_gbs"],
             "hbm_stages": hbm,
             "stage_ms": stage_ms,
             "ms_per_step_eager": eager_ms,
-            "timing": "CUDA-graph replay of the five C-ABI calls; stage_ms: each call as its own graph",
+            "timing": "CUDA-graph replay of the five C-ABI calls; stage_ms: each call as its own graph; "
+                      "kernel_trace / kernel_roofline: each kernel's own device time (timing events "
+                      "around every launch, eager steps, L2 flushed before each step)",
             "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e), "unit": "tokens/s",
                     "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
                     "d2h_bytes_per_step": 4,
@@ -629,9 +760,15 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm; scaled by 2/k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional calls")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per batch instead of the workload's (a smaller case of the same layer)")
+    ap.add_argument("--profile", choices=["route", "dispatch", "expert_ffn", "combine", "backward"], default=None,
+                    help="for a profiler: warm up, then run only this call --steps times (no JSON line)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     cfg = synth.get(args.workload)
+    if args.tokens is not None:
+        cfg = cfg.with_(T=int(args.tokens), name=f"{cfg.name}@T{int(args.tokens)}")
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)

@@ -48,6 +48,10 @@
  *   cfg->rows_capacity rows.
  * - Calls are asynchronous on `stream` and never synchronise the host (except
  *   moe_get_error). Nothing that depends on data (counts, offsets) is read back.
+ * - The library keeps a few per-device handles for the life of the process (its side stream,
+ *   the device addresses of its error word and of the moe_dispatch_noalloc scratch array).
+ *   cudaDeviceReset invalidates them: a process must not call the library on a device after
+ *   resetting that device.
  * - Host-side validation failures return MOE_ERR_INVALID_ARG (bad value, null pointer) or
  *   MOE_ERR_UNSUPPORTED (valid but not implemented) and launch nothing. A failed launch
  *   returns MOE_ERR_CUDA. Faults detected on the device (a bounded wait that ran out, an
@@ -232,6 +236,41 @@ MOE_API moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const fl
                                                const void* Wg, void* dx, float* dWg, float* dbg,
                                                void* ws, moe_stream_t stream);
 
+/* The soft balance loss on a sliding window of batches: "Expert Parallelism: Scaling
+ * Mixture-of-Experts Models", section 2.3 (the per-expert load is averaged over the last 100
+ * batches before the balance loss is taken, because a single batch's load is too noisy).
+ * The caller owns the window's state; the library keeps none:
+ *   ring  [W, E] fp32 device: the soft loads of the last W batches (contents need no
+ *         initialisation: only slots written by earlier calls are read)
+ *   state [2] int32 device: state[0] = ring slot of the next batch, state[1] = batches in the
+ *         window (0..W). Set both to 0 before the first call; a state out of range sets
+ *         MOE_ERR_DEVICE_BOUNDS and the window restarts.
+ * Each call computes this batch's soft load P_e = sum_t softmax(logits_t / temperature)_e
+ * (as moe_soft_balance), stores it in slot state[0], and with n = min(state[1] + 1, W):
+ *   Pbar [E] = mean of the n most recent soft loads (this batch included),
+ *   loss [1] = weight * mean_e (Pbar_e - mean(Pbar))^2   (loss nullable),
+ * then advances the state: state[0] = (state[0] + 1) mod W, state[1] = n.
+ * W = 1 is moe_soft_balance. logits [T,E] fp32; P, Pbar [E] fp32 device; W in
+ * 1..MOE_MAX_WINDOW; ring and state 4-byte aligned. Scratch from ws (moe_workspace_bytes).
+ * Successive calls on one ring must be ordered on the GPU (one stream). */
+#define MOE_MAX_WINDOW 4096
+MOE_API moe_status_t moe_soft_balance_window(const moe_config_t* cfg, const float* logits, float weight,
+                                             int32_t W, float* ring, int32_t* state, float* P, float* Pbar,
+                                             float* loss, void* ws, moe_stream_t stream);
+
+/* Gradient of moe_soft_balance_window's loss, ADDED to the layer gradients. The earlier
+ * batches of the window are stored statistics, so the gradient reaches only this batch:
+ *   g_e = weight * 2 (Pbar_e - mean(Pbar)) / (E n),  n = state[1],
+ *   dz_te = p_te (g_e - sum_j p_tj g_j) / temperature,  dx += dz Wg, dWg += dz^T x,
+ *   dbg += sum_t dz (dbg nullable).
+ * Call it after the forward call of the same batch (which set state[1] = n) and before the
+ * next one, with that call's Pbar and state. logits, x [T,d] act, Wg [E,d] act; dx, dWg, dbg
+ * are read and updated in place. */
+MOE_API moe_status_t moe_soft_balance_window_backward(const moe_config_t* cfg, const float* logits,
+                                                      const float* Pbar, float weight, const int32_t* state,
+                                                      const void* x, const void* Wg, void* dx, float* dWg,
+                                                      float* dbg, void* ws, moe_stream_t stream);
+
 /* Expert co-selection matrix of a batch: "Expert Parallelism: Scaling Mixture-of-Experts
  * Models", section 3.2, step 1 (experts chosen by the same token; the input of the page's
  * affinity-aware placement). The page calls the matrix asymmetric; accordingly, for i != j,
@@ -262,6 +301,27 @@ MOE_API moe_status_t moe_get_error(moe_stream_t stream);
  * with moe_get_error. */
 MOE_API moe_status_t moe_selftest_wait_timeout(int32_t mode, int64_t budget_cycles, int32_t* timed_out,
                                                void* scratch, moe_stream_t stream);
+
+/* Kernel trace: the device time of every kernel the library launches, for profiling from
+ * the host without an external profiler. The pages have no counterpart.
+ * moe_trace_begin opens a trace on the calling host thread, with room for max_launches
+ * (1 .. 65536) launches; it creates 2 * max_launches CUDA timing events (no device memory)
+ * and discards the previous trace's results. Until moe_trace_end, every kernel the library
+ * launches from this thread, on a stream that is not being captured into a graph, is
+ * bracketed by two events recorded on its own stream: the kernel then starts only after the
+ * previous work of its stream has finished (no overlap with a dependent launch), so each
+ * duration is the kernel's own; while a trace is open, moe_backward also keeps its two
+ * branches from overlapping (its caller's stream waits for the side branch). Launches beyond
+ * max_launches are not traced (counted by moe_trace_dropped).
+ * moe_trace_end synchronises the recorded events and returns the number of traced launches
+ * (>= 0), or MOE_ERR_INVALID_ARG if no trace is open, or MOE_ERR_CUDA.
+ * moe_trace_record gives launch i's kernel name (without parameters, e.g.
+ * "route_tc_kernel<2>"; the string stays valid until the next moe_trace_begin on this thread)
+ * and its duration in milliseconds, in launch order. */
+MOE_API moe_status_t moe_trace_begin(int32_t max_launches);
+MOE_API int32_t moe_trace_end(void);
+MOE_API moe_status_t moe_trace_record(int32_t i, const char** name, float* ms);
+MOE_API int32_t moe_trace_dropped(void);
 
 /* Static description of a status code (never NULL). */
 MOE_API const char* moe_status_str(moe_status_t status);

@@ -59,7 +59,7 @@ WORKLOADS = {
     "tiny-fp32-fwd": LayerConfig(
         name="tiny-fp32-fwd", T=256, d=64, E=8, k=2, d_ff=256, capacity_factor=None,
         dtype="f32", backward=False),
-    # top-2 over 16 experts, capacity factor 1.0 (the headline throughput workload)
+    # top-2 over 16 experts, capacity factor 1.0
     "top2-e16-cap1.0": LayerConfig(
         name="top2-e16-cap1.0", T=8192, d=1024, E=16, k=2, d_ff=4096, capacity_factor=1.0),
     # top-2 over 64 experts with a Zipf(1.2) gate bias skewing the load, capacity 1.25
@@ -81,8 +81,9 @@ WORKLOADS = {
         capacity_factor=None, temperature=0.2),
 }
 
-# The throughput workload timed by the benchmark.
-HEADLINE = "top2-e16-cap1.0"
+# The throughput workload the benchmark times by default: the configuration with the most
+# work per step (hybrid top-8 over 128 experts, 131,072 expert rows, ~6.6 TFLOP fwd+bwd).
+HEADLINE = "hybrid-top8-e128-temp0.2"
 
 # Scaled-down parity cases: several 128-row tiles, ragged tails, drops, skew.
 SMALL_CASES = {
@@ -121,6 +122,11 @@ SMALL_CASES = {
         gate_bias="zipf", zipf_s=1.2, zipf_c=ZIPF_C_E64),
     "small-dense-e16-pairs": LayerConfig(
         name="small-dense-e16-pairs", T=1100, d=128, E=16, k=16, d_ff=128, capacity_factor=None,
+        temperature=0.5),
+    # dense routing past 32 experts: the gate-weight gradient dz^T x (and the soft balance
+    # loss's dz Wg) run on the tensor cores from the dense dz rows
+    "small-dense-e40": LayerConfig(
+        name="small-dense-e40", T=700, d=128, E=40, k=40, d_ff=128, capacity_factor=None,
         temperature=0.5),
     "small-dense-fp32": LayerConfig(
         name="small-dense-fp32", T=100, d=40, E=10, k=10, d_ff=24, capacity_factor=None,

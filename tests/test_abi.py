@@ -168,3 +168,53 @@ def test_binding_make_config(moe_lib):
     assert c.capacity == math.ceil(1.25 * 1000 * 2 / 8)
     with pytest.raises(moe_lib.MoeError):
         moe_lib.make_config(10, 16, 4, 5, 16)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), -1),                                    # fields never filled by moe_config_init
+    (dict(T=1 << 30, k=4, E=8, capacity_factor=0.0), -2),   # T*k beyond 2^31 - 1
+])
+def test_noalloc_dispatch_gives_the_dispatch_config_errors(moe_lib, kw, status):
+    """moe_dispatch_noalloc refuses a configuration with the same status as moe_dispatch,
+    before touching a GPU."""
+    lib = moe_lib.load()
+    c = _cfg(moe_lib, **kw)
+    p = ctypes.c_void_p(256)
+    fn = lib.moe_dispatch_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 10
+    got = fn(ctypes.byref(c), p, p, p, p, p, p, p, p, None)
+    ref = lib.moe_dispatch(ctypes.byref(c), p, p, p, p, p, p, p, p, p, None)
+    assert got == ref == status
+
+
+def test_trace_argument_checks(moe_lib):
+    """The kernel trace's host-side checks, before any CUDA call."""
+    import ctypes as ct
+    lib = moe_lib.load()
+    assert lib.moe_trace_begin(0) == moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_trace_begin(1 << 17) == moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_trace_end() == moe_lib.MOE_ERR_INVALID_ARG        # no trace open
+    name, ms = ct.c_char_p(), ct.c_float()
+    assert lib.moe_trace_record(-1, ct.byref(name), ct.byref(ms)) == moe_lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_trace_record(1 << 20, ct.byref(name), ct.byref(ms)) == moe_lib.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("W,null", [(0, None), (-3, None), (4097, None), (3, "ring"), (3, "state"),
+                                    (3, "Pbar")])
+def test_soft_window_argument_checks(moe_lib, W, null):
+    """moe_soft_balance_window refuses a bad window size or a missing buffer before any launch."""
+    lib = moe_lib.load()
+    c = _cfg(moe_lib)
+    assert lib.moe_config_init(ctypes.byref(c)) == 0
+    p = {k: ctypes.c_void_p(256) for k in ("logits", "ring", "state", "P", "Pbar", "loss", "ws")}
+    if null:
+        p[null] = None
+    st = lib.moe_soft_balance_window(ctypes.byref(c), p["logits"], ctypes.c_float(1e-3), W, p["ring"], p["state"],
+                                     p["P"], p["Pbar"], p["loss"], p["ws"], None)
+    assert st == moe_lib.MOE_ERR_INVALID_ARG
+    if null in ("state", "Pbar"):
+        # every call here must be refused before any launch (the pointers are not real)
+        st = lib.moe_soft_balance_window_backward(ctypes.byref(c), p["logits"], p["Pbar"], ctypes.c_float(1e-3),
+                                                  p["state"], p["P"], p["P"], p["P"], p["P"], None, p["ws"], None)
+        assert st == moe_lib.MOE_ERR_INVALID_ARG

@@ -57,11 +57,9 @@ def test_degenerate_layer_matches_oracle(name, moe_lib, cuda_device):
     b = moe.alloc_buffers(c, backward=True)
     moe.forward_backward(c, dev, dev["x"], dev["dy"], b)
     moe.get_error()
-    ok = P.nontie_tokens(fwd)
-    idx = b["idx"].cpu().numpy()
-    assert (idx[ok] == fwd["idx"][ok]).all()
-    if not (idx == fwd["idx"]).all():
-        pytest.skip(f"{(~ok).sum()} near-tie tokens routed differently")
+    # a near-tie token routed the other way: the oracle follows the GPU's (valid) selection
+    fwd, bwd, _ = P.oracle_on_gpu_routing(cfg, npin, fwd, b["idx"].cpu().numpy(), npin["dy"],
+                                          align=c.row_align)
     n = int(fwd["offsets"][-1])
     assert b["kept"].cpu().tolist() == fwd["kept"].tolist()
     assert b["offsets"].cpu().tolist() == fwd["offsets"].tolist()

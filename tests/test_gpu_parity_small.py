@@ -134,8 +134,7 @@ def test_backward(name, cases, moe_lib, cuda_device):
         P.assert_close(key, P.f64(b[key]), bwd[key], t)
     if cfg.gate_bias != "none":
         P.assert_close("dbg", P.f64(b["dbg"]), bwd["dbg"], t)
-    loss_ref = P.O.layer_loss(fwd, npin["dy"])
-    assert abs(b["loss"].item() - loss_ref) <= t * max(1.0, abs(loss_ref))
+    P.assert_loss_close(b["loss"].item(), fwd, npin["dy"], t)
     # experts with no kept rows get exactly zero weight gradients
     for e in np.nonzero(fwd["kept"] == 0)[0]:
         assert (b["dW1"][e] == 0).all() and (b["dW2"][e] == 0).all()
@@ -154,20 +153,27 @@ def test_end_to_end(name, cases, moe_lib, cuda_device):
     else:
         moe.forward(c, dev, dev["x"], b)
     moe.get_error()
-    idx = b["idx"].cpu().numpy()
-    ok = P.nontie_tokens(fwd)
-    assert (idx[ok] == fwd["idx"][ok]).all()
-    if not (idx == fwd["idx"]).all():
-        pytest.skip(f"{(~ok).sum()} near-tie tokens routed differently; stage tests cover the values")
+    # a near-tie token routed the other way is a correct answer too: the oracle then follows
+    # the GPU's selection, and every value downstream is still compared
+    fwd, bwd, _ = P.oracle_on_gpu_routing(cfg, npin, fwd, b["idx"].cpu().numpy(),
+                                          npin["dy"] if cfg.backward else None, align=c.row_align)
+    assert (b["idx"].cpu().numpy() == fwd["idx"]).all()
+    assert b["counts"].cpu().tolist() == fwd["counts"].tolist()
     n = int(fwd["offsets"][-1])
+    assert b["kept"].cpu().tolist() == fwd["kept"].tolist()
+    assert b["n_dropped"].item() == fwd["n_dropped"]
     assert b["offsets"].cpu().tolist() == fwd["offsets"].tolist()
     assert (b["slot_row"].cpu().numpy() == fwd["slot_row"]).all()
     assert (b["row_token"][:n].cpu().numpy() == fwd["row_token"]).all()
     t = P.tol(cfg)
+    P.assert_close("w", b["w"].cpu().double().numpy(), fwd["w"], P.tol(cfg) if cfg.dtype == "f32" else 1e-4)
     P.assert_close("y", P.f64(b["y"]), fwd["y"], t)
     if cfg.backward:
         for key in ("dx", "dWg", "dW1", "db1", "dW2", "db2", "dw"):
             P.assert_close(key, P.f64(b[key]), bwd[key], t)
+        if cfg.gate_bias != "none":
+            P.assert_close("dbg", P.f64(b["dbg"]), bwd["dbg"], t)
+        P.assert_loss_close(b["loss"].item(), fwd, npin["dy"], t)
 
 
 @pytest.mark.parametrize("name", ["small-top2-cap1.0", "small-hybrid-top8", "small-dense-e12-cap0.5"])

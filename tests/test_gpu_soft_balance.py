@@ -15,7 +15,7 @@ WEIGHT = 1e-3
 
 @pytest.mark.parametrize("name", ["small-top2-cap1.0", "small-zipf-cap1.25", "small-max-e256-k8",
                                   "small-fp32-bwd", "small-fp32-ragged", "small-dense-e12-cap0.5",
-                                  "top2-e16-cap1.0", "top2-e256-clusters-cap1.0"])
+                                  "small-dense-e40", "top2-e16-cap1.0", "top2-e256-clusters-cap1.0"])
 def test_soft_balance_matches_oracle(name, moe_lib, cuda_device):
     moe = moe_lib
     cfg = synth.get(name)
@@ -39,13 +39,17 @@ def test_soft_balance_matches_oracle(name, moe_lib, cuda_device):
     P.assert_close("logits", P.f64(logits), z, 1e-5)
     _, Po = P.O.soft_load(z, cfg.temperature)
     P.assert_close("P", P.f64(Pg), Po, 1e-5)
-    lo = P.O.soft_balance_loss(Po, WEIGHT)
-    assert loss.item() == pytest.approx(lo, rel=2e-3, abs=1e-6)
-    dZ = P.O.soft_balance_grad(z, cfg.temperature, WEIGHT)
+    # fp32 layers: the benchmark spec's fp32 bar (1e-4) on every value. bf16 layers: the loss and the
+    # gate gradients come from fp32 logits and fp32 dz, so they are held to 1e-3, stricter
+    # than the bf16 bar; dx is stored in bf16 and gets the bf16 bar.
     t = P.tol(cfg)
+    t_gate = t if cfg.dtype == "f32" else 1e-3
+    lo = P.O.soft_balance_loss(Po, WEIGHT)
+    assert abs(loss.item() - lo) <= t_gate * abs(lo), (loss.item(), lo)
+    dZ = P.O.soft_balance_grad(z, cfg.temperature, WEIGHT)
     P.assert_close("dx", P.f64(dx), dZ @ npin["Wg"], t)
-    P.assert_close("dWg", P.f64(dWg), dZ.T @ npin["x"], 1e-3)
-    P.assert_close("dbg", P.f64(dbg), dZ.sum(axis=0), 1e-3)
+    P.assert_close("dWg", P.f64(dWg), dZ.T @ npin["x"], t_gate)
+    P.assert_close("dbg", P.f64(dbg), dZ.sum(axis=0), t_gate)
 
 
 def test_soft_balance_backward_accumulates(moe_lib, cuda_device):

@@ -22,6 +22,7 @@ MOE_BF16 = 1
 MOE_ROW_ALIGN = 128
 MOE_MAX_EXPERTS = 256
 MOE_MAX_K = 8
+MOE_MAX_WINDOW = 4096
 
 
 class MoeConfig(ctypes.Structure):
@@ -63,6 +64,16 @@ _SIGS = {
     "moe_kernel_launches": (ctypes.c_uint64, []),
     "moe_version": (ctypes.c_char_p, []),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, _P, _P, _P]),
+    "moe_soft_balance_window": (ctypes.c_int, [_CFG, _P, ctypes.c_float, ctypes.c_int32, _P, _P, _P, _P, _P,
+                                               _P, _P]),
+    "moe_soft_balance_window_backward": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P,
+                                                        _P, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_trace_begin": (ctypes.c_int, [ctypes.c_int32]),
+    "moe_trace_end": (ctypes.c_int32, []),
+    "moe_trace_record": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_char_p),
+                                        ctypes.POINTER(ctypes.c_float)]),
+    "moe_trace_dropped": (ctypes.c_int32, []),
 }
 
 _lib = None

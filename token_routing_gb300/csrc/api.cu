@@ -145,19 +145,19 @@ cudaStream_t side_stream() {
 
 // Fork/join events of one call; destroyed when the call returns (pending waits still hold).
 struct EventSet {
-    cudaEvent_t a = nullptr, b = nullptr, c = nullptr, d = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr, c = nullptr, d = nullptr, e = nullptr, f = nullptr;
     bool ok = false;
-    EventSet() {
+    explicit EventSet(bool extra) {
         ok = cudaEventCreateWithFlags(&a, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&b, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&c, cudaEventDisableTiming) == cudaSuccess &&
-             cudaEventCreateWithFlags(&d, cudaEventDisableTiming) == cudaSuccess;
+             cudaEventCreateWithFlags(&d, cudaEventDisableTiming) == cudaSuccess &&
+             (!extra || (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess &&
+                         cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess));
     }
     ~EventSet() {
-        if (a) cudaEventDestroy(a);
-        if (b) cudaEventDestroy(b);
-        if (c) cudaEventDestroy(c);
-        if (d) cudaEventDestroy(d);
+        for (cudaEvent_t x : {a, b, c, d, e, f})
+            if (x) cudaEventDestroy(x);
     }
 };
 
@@ -179,6 +179,8 @@ cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+moe_status_t config_status(const moe_config_t* cfg) { return check_config(cfg); }
 
 int* device_error_word() {
     const int dev = current_device();
@@ -264,7 +266,40 @@ moe_status_t moe_soft_balance_backward(const moe_config_t* cfg, const float* log
     if (!aligned16({x, Wg, dx, ws})) return MOE_ERR_INVALID_ARG;
     BackwardScratch b;
     carve_backward(*cfg, ws, &b);
-    return cuda_status(launch_soft_balance_bwd(*cfg, logits, P, weight, x, Wg, dx, dWg, dbg, b.soft,
+    return cuda_status(launch_soft_balance_bwd(*cfg, logits, P, weight, nullptr, x, Wg, dx, dWg, dbg, b.soft,
+                                               (cudaStream_t)stream));
+}
+
+moe_status_t moe_soft_balance_window(const moe_config_t* cfg, const float* logits, float weight, int32_t W,
+                                     float* ring, int32_t* state, float* P, float* Pbar, float* loss, void* ws,
+                                     moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (W < 1 || W > MOE_MAX_WINDOW || !ring || !state || !P || !Pbar || !ws || (cfg->T > 0 && !logits) ||
+        !std::isfinite(weight))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16({ws}) || (reinterpret_cast<uintptr_t>(ring) & 3u) || (reinterpret_cast<uintptr_t>(state) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    BackwardScratch b;
+    carve_backward(*cfg, ws, &b);
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_TRY(launch_soft_balance(*cfg, logits, weight, P, nullptr, b.soft, s));
+    MOE_TRY(launch_soft_window(*cfg, P, weight, W, ring, state, Pbar, loss, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_soft_balance_window_backward(const moe_config_t* cfg, const float* logits, const float* Pbar,
+                                              float weight, const int32_t* state, const void* x, const void* Wg,
+                                              void* dx, float* dWg, float* dbg, void* ws, moe_stream_t stream) {
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!Pbar || !state || !Wg || !dWg || !ws || !std::isfinite(weight)) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!logits || !x || !dx)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16({x, Wg, dx, ws}) || (reinterpret_cast<uintptr_t>(state) & 3u)) return MOE_ERR_INVALID_ARG;
+    BackwardScratch b;
+    carve_backward(*cfg, ws, &b);
+    // state[1] is the window's batch count once the forward of this batch has run
+    return cuda_status(launch_soft_balance_bwd(*cfg, logits, Pbar, weight, state + 1, x, Wg, dx, dWg, dbg, b.soft,
                                                (cudaStream_t)stream));
 }
 
@@ -344,6 +379,13 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     carve_backward(c, ws, &b);
     float* dwp = dw ? dw : b.dw;
 
+    cudaStream_t side = side_stream();
+    if (!side) return MOE_ERR_CUDA;
+    // With a kernel trace open on this thread the main stream also waits for the side branch
+    // before dH and before dX, so that no two kernels overlap and each traced duration is the
+    // kernel's own, not a wait for SMs held by the other branch.
+    const bool serial = t_trace_on;
+
     // The backward is a small DAG.
     //   main: combine backward -> dH -> dX -> un-permute (dx)
     //   side: dz (softmax Jacobian) + loss -> dWg, dbg -> dW2, db2 -> [after dH] dW1, db1
@@ -355,9 +397,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     // (no tensor cores, more than 32 experts) the assignments are sorted by expert after dX.
     // The branches fork and join through events, which also works under stream capture; they
     // write disjoint outputs, so results do not depend on the overlap.
-    cudaStream_t side = side_stream();
-    if (!side) return MOE_ERR_CUDA;
-    EventSet ev;
+    EventSet ev(serial);
     if (!ev.ok) return MOE_ERR_CUDA;
     float* dbg_out = c.has_gate_bias ? dbg : nullptr;
     const bool early_dz = dense_routing(c) || (c.dtype == MOE_BF16 && c.d % 64 == 0 && c.E > 32);
@@ -377,6 +417,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     MOE_TRY(wgrad(c, w2, side));
     MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, side));
     MOE_TRY(launch_bias_reduce(c, b.colsum_d, c.d, offsets, db2, side));
+    if (serial) {
+        MOE_TRY(cudaEventRecord(ev.e, side));
+        MOE_TRY(cudaStreamWaitEvent(s, ev.e, 0));
+    }
     // experts backward on the main stream
     RowGemmArgs gh{};
     gh.kind = kGemmDH; gh.A = b.dYp; gh.B = W2; gh.aux = Gp; gh.out0 = b.dA;
@@ -390,6 +434,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
     MOE_TRY(wgrad(c, w1, side));
     MOE_TRY(launch_bias_reduce(c, b.colsum_f, c.d_ff, offsets, db1, side));
+    if (serial) {
+        MOE_TRY(cudaEventRecord(ev.f, side));
+        MOE_TRY(cudaStreamWaitEvent(s, ev.f, 0));
+    }
     RowGemmArgs gx{};
     gx.kind = kGemmDX; gx.A = b.dA; gx.B = W1; gx.out0 = b.dXp;
     gx.offsets = offsets; gx.E = c.E; gx.N = c.d; gx.K = c.d_ff; gx.rows_capacity = c.rows_capacity;

@@ -131,7 +131,7 @@ __device__ __forceinline__ void zero_padding_rows(const int32_t* __restrict__ of
 // then the padding rows of dYp are zeroed. lossblk[block] = the block's sum of w * dw over
 // kept slots (warps in order; a warp's tokens in order), so sum(lossblk) = sum_t <y[t], dy[t]>.
 template <typename T, int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, G >= 8 ? 2 : 1)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const float* __restrict__ w,
                    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ row_token,
                    const int32_t* __restrict__ slot_row, int Tn, int d, int k, int rows_cap,
@@ -156,13 +156,19 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ Yp, const flo
             }
             if ((d % V) == 0) {
                 for (int c = lane * V; c < d; c += 32 * V) {
+                    // the dy vector and every kept slot's Yp vector in flight before any arithmetic
+                    const uint4 graw = __ldg(reinterpret_cast<const uint4*>(dy + (size_t)t * d + c));
+                    uint4 yraw[G];
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        if (rows[j] >= 0) yraw[j] = __ldg(reinterpret_cast<const uint4*>(Yp + (size_t)rows[j] * d + c));
                     float g[V];
-                    load16(dy + (size_t)t * d + c, g);
+                    unpack16<T>(graw, g);
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
                         if (rows[j] < 0) continue;
                         float yv[V], o[V];
-                        load16(Yp + (size_t)rows[j] * d + c, yv);
+                        unpack16<T>(yraw[j], yv);
 #pragma unroll
                         for (int i = 0; i < V; ++i) { dot[j] = fmaf(g[i], yv[i], dot[j]); o[i] = ws[j] * g[i]; }
                         store16(dYp + (size_t)rows[j] * d + c, o);
@@ -256,7 +262,7 @@ router_dz_kernel(const float* __restrict__ w, const float* __restrict__ dw, cons
 //   s = sum_j w_j dw_j,  dz_j = w_j (dw_j - s) / temperature          (softmax Jacobian)
 //   dx[t] = sum_{kept j} dXp[slot_row[t,j]] + sum_j dz_j Wg[idx[t,j]]
 template <typename T, int KC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, KC >= 8 ? 2 : 1)
 router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_row,
                   const T* __restrict__ Wg, const T* __restrict__ dXp, int Tn, int d, int k,
@@ -299,6 +305,16 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
         }
         if ((d % V) == 0) {
             for (int c = lane * V; c < d; c += 32 * V) {
+                // every slot's dXp and Wg vectors in flight before any arithmetic, then the same
+                // order of additions as one slot at a time
+                uint4 xraw[KC], graw[KC];
+#pragma unroll
+                for (int j = 0; j < KC; ++j) {
+                    if (j < k) {
+                        if (rows[j] >= 0) xraw[j] = __ldg(reinterpret_cast<const uint4*>(dXp + (size_t)rows[j] * d + c));
+                        graw[j] = __ldg(reinterpret_cast<const uint4*>(Wg + (size_t)ex[j] * d + c));
+                    }
+                }
                 float acc[V];
 #pragma unroll
                 for (int i = 0; i < V; ++i) acc[i] = 0.f;
@@ -307,11 +323,11 @@ router_bwd_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                     if (j < k) {
                         float v[V];
                         if (rows[j] >= 0) {
-                            load16(dXp + (size_t)rows[j] * d + c, v);
+                            unpack16<T>(xraw[j], v);
 #pragma unroll
                             for (int i = 0; i < V; ++i) acc[i] += v[i];
                         }
-                        load16(Wg + (size_t)ex[j] * d + c, v);
+                        unpack16<T>(graw[j], v);
 #pragma unroll
                         for (int i = 0; i < V; ++i) acc[i] = fmaf(dzj[j], v[i], acc[i]);
                     }

@@ -65,6 +65,24 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- kernel trace (host)
+// While the calling host thread has a trace open (moe_trace_begin), each kernel launch on a
+// stream that is not being captured is bracketed by two timing events on its stream, so that
+// moe_trace_end can report every kernel's own device time. Off otherwise: one thread-local
+// test per launch.
+extern thread_local bool t_trace_on;
+int trace_before(const void* fn, cudaStream_t s);    // record slot, or -1
+void trace_after(int slot, cudaStream_t s);
+
+// cudaLaunchKernelEx with the trace hooks around it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(const cudaLaunchConfig_t& cfg, void (*kern)(KArgs...), Args... args) {
+    const int slot = t_trace_on ? trace_before(reinterpret_cast<const void*>(kern), cfg.stream) : -1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (slot >= 0) trace_after(slot, cfg.stream);
+    return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args... args) {
@@ -78,7 +96,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
+    return launch_ex(cfg, kern, args...);
 }
 
 // p[0..n) = v as a kernel, so that it orders with the dependent launches around it like any

@@ -342,7 +342,7 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, sort_kernel, a);
+    e = launch_ex(cfg, sort_kernel, a);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -50,8 +50,8 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
                                                      const void* x, int32_t* kept, int32_t* offsets,
                                                      int32_t* row_token, int32_t* slot_row,
                                                      int32_t* n_dropped, void* Xp, moe_stream_t stream) {
-    // a config that moe_config_init did not accept has no workspace size
-    if (moe_workspace_bytes(cfg) == 0) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = config_status(cfg);
+    if (st != MOE_OK) return st;
     if (!kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!idx || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (cfg->rows_capacity > 0 && (!row_token || !Xp)) return MOE_ERR_INVALID_ARG;

@@ -5,6 +5,10 @@
 
 namespace moe {
 
+// MOE_OK for a config that moe_config_init has filled, else the status every entry point
+// returns for it (MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED).
+moe_status_t config_status(const moe_config_t* cfg);
+
 // k = E: dense soft routing (every expert on every token, slot j = expert j). The bucket
 // layout is then closed-form and no sort runs.
 inline bool dense_routing(const moe_config_t& c) { return c.k == c.E; }
@@ -118,9 +122,15 @@ bool soft_tc_ok(const moe_config_t& c);
 // s.dwg_part, fixed-order reductions); accumulate = false overwrites dWg and dbg.
 cudaError_t launch_dense_dwg(const moe_config_t& c, const float* dz, const void* x, float* dWg, float* dbg,
                              bool accumulate, const SoftScratch& s, cudaStream_t st);
+// win_n: null for one batch; for a window mean load P (moe_soft_balance_window), the device
+// count of batches in the window (the gradient is divided by it and the mean taken from P).
 cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, const float* P, float weight,
-                                    const void* x, const void* Wg, void* dx, float* dWg, float* dbg,
-                                    const SoftScratch& s, cudaStream_t st);
+                                    const int32_t* win_n, const void* x, const void* Wg, void* dx, float* dWg,
+                                    float* dbg, const SoftScratch& s, cudaStream_t st);
+// Sliding window of soft loads: P (this batch) into ring slot state[0], Pbar = mean of the
+// window's loads, loss on Pbar, state advanced.
+cudaError_t launch_soft_window(const moe_config_t& c, const float* P, float weight, int W, float* ring,
+                               int32_t* state, float* Pbar, float* loss, cudaStream_t st);
 
 // coselect.cu: expert co-selection matrix H [E, E]
 cudaError_t launch_coselect(const moe_config_t& c, const int32_t* idx, int32_t* H, cudaStream_t s);

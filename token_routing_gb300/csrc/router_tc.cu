@@ -9,9 +9,13 @@
 // the logits stay fp32 from the accumulator to the softmax).
 //
 // One CTA per 128-token tile: warp 0 streams x and Wg tiles with TMA, warp 1 issues the
-// MMAs (N = E rounded up to 32), warps 2..5 read one token's E logits each from TMEM and
-// keep a sorted top-k list in registers (or, with k = E, take the softmax over all E). The
-// kernel is bound by reading x from HBM.
+// MMAs (N = E rounded up to 32), and G groups of four epilogue warps (one per TMEM lane
+// quarter) read the logits from TMEM. With k = E one group takes the softmax over all E per
+// token. For top-k, group g keeps a sorted top-k list per token over its share of the
+// 32-expert chunks (chunks g, g + G, ...), and group 0 merges the G lists through shared
+// memory: G = min(4, chunks) groups put four times the warps on the selection's dependent
+// compare-and-swap chains where there are many experts. The kernel is bound by reading x from
+// HBM.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -24,7 +28,8 @@ constexpr int RBM = 128;
 constexpr int RBK = 64;
 constexpr int RMAX_STAGES = 12;              // ring depth: as many stages as fit in ~200 KB
 constexpr int RSMEM_BUDGET = 200 * 1024;
-constexpr int RTHREADS = 192;
+// warps 0 (TMA) and 1 (MMA) plus G groups of four epilogue warps
+__host__ __device__ constexpr int route_threads(int G) { return 64 + 128 * G; }
 
 struct RouteTcParams {
     int T, d, E, E_pad, stages;
@@ -52,8 +57,29 @@ __device__ __forceinline__ void load_noise32(const float* __restrict__ noise, in
     for (int i = 0; i < 32; ++i) nz[i] = (live && c + i < E) ? __ldg(noise + (size_t)(c + i) * T + tok) : 0.f;
 }
 
+// Softmax over a token's k selected logits (tv[0] the largest), its indices and weights, and
+// its counts in the CTA's histogram.
 template <int K>
-__global__ void __launch_bounds__(RTHREADS, 1)
+__device__ __forceinline__ void route_finish(const RouteTcParams& p, int tok, const float (&tv)[K],
+                                             const int (&te)[K], int* s_cnt) {
+    float pr[K], s = 0.f;
+#pragma unroll
+    for (int j = 0; j < K; ++j) { pr[j] = expf((tv[j] - tv[0]) * p.inv_temp); s += pr[j]; }
+    const float inv = 1.f / s;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        p.idx[(size_t)tok * K + j] = te[j];
+        p.w[(size_t)tok * K + j] = pr[j] * inv;
+        if (te[j] >= 0) atomicAdd(&s_cnt[te[j]], 1);
+    }
+}
+
+__device__ __forceinline__ void epilogue_bar_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <int K, int G>
+__global__ void __launch_bounds__(route_threads(G), 1)
 route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmW) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -204,14 +230,16 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     }
                 }
             }
-        } else if (mbar_wait(tfull, 0, p.err)) {
-            tc_fence_after();
+        } else {
+            const int grp = (warp - 2) >> 2;
             float tv[K];
             int te[K];
 #pragma unroll
             for (int j = 0; j < K; ++j) { tv[j] = -INFINITY; te[j] = -1; }
+            const bool ok = mbar_wait(tfull, 0, p.err);
+            if (ok) tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
-            for (int c = 0; c < p.E_pad; c += 32) {
+            for (int c = 32 * grp; ok && c < p.E_pad; c += 32 * G) {
                 float nz[32];
                 if (p.noise) load_noise32(p.noise, p.T, p.E, c, tok, tok < p.T, nz);
                 uint32_t r[32];
@@ -238,16 +266,45 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     }
                 }
             }
-            if (tok < p.T) {
-                float pr[K], s = 0.f;
-#pragma unroll
-                for (int j = 0; j < K; ++j) { pr[j] = expf((tv[j] - tv[0]) * p.inv_temp); s += pr[j]; }
-                const float inv = 1.f / s;
+            if constexpr (G == 1) {
+                if (tok < p.T) route_finish<K>(p, tok, tv, te, s_cnt);
+            } else {
+                // The G partial lists of each token go to shared memory, over the operand ring:
+                // the accumulator-full barrier fired after the last MMA, so the ring is no
+                // longer read (a wait that ran out leaves empty lists, and the id check below
+                // keeps them out of the counts).
+                float* s_v = reinterpret_cast<float*>(smem);                                 // [G][RBM][K]
+                int* s_i = reinterpret_cast<int*>(smem + (size_t)G * RBM * K * sizeof(float));   // [G][RBM][K]
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
-                    p.idx[(size_t)tok * K + j] = te[j];
-                    p.w[(size_t)tok * K + j] = pr[j] * inv;
-                    atomicAdd(&s_cnt[te[j]], 1);
+                    s_v[((size_t)grp * RBM + row) * K + j] = tv[j];
+                    s_i[((size_t)grp * RBM + row) * K + j] = te[j];
+                }
+                epilogue_bar_sync(128 * G);
+                if (grp == 0) {
+                    // Merge of G lists sorted by (logit desc, id asc): take the larger head, the
+                    // lower expert id on equal logits, so the result is the top-k of all E.
+                    int head[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) head[g] = 0;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        float bv = -INFINITY;
+                        int bi = -1, bg = 0;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (head[g] < K) {
+                                const float v = s_v[((size_t)g * RBM + row) * K + head[g]];
+                                const int i = s_i[((size_t)g * RBM + row) * K + head[g]];
+                                if (i >= 0 && (bi < 0 || v > bv || (v == bv && i < bi))) { bv = v; bi = i; bg = g; }
+                            }
+                        }
+                        tv[j] = bv;
+                        te[j] = bi;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) head[g] += (g == bg && bi >= 0) ? 1 : 0;
+                    }
+                    if (tok < p.T) route_finish<K>(p, tok, tv, te, s_cnt);
                 }
             }
         }
@@ -264,15 +321,30 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
     }
 }
 
+template <int K, int G>
+cudaError_t launch_kg(const RouteTcParams& p, const CUtensorMap& tx, const CUtensorMap& tw, size_t smem,
+                      cudaStream_t s) {
+    auto kern = route_tc_kernel<K, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    launch_pdl(kern, dim3(ceil_div(p.T, p.rows)), dim3(route_threads(G)), smem, s, p, tx, tw);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// Epilogue groups: one per 32-expert chunk up to four (dense routing: one).
 template <int K>
 cudaError_t launch_k(const RouteTcParams& p, const CUtensorMap& tx, const CUtensorMap& tw, size_t smem,
                      cudaStream_t s) {
-    auto kern = route_tc_kernel<K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    launch_pdl(kern, dim3(ceil_div(p.T, p.rows)), dim3(RTHREADS), smem, s, p, tx, tw);
-    count_launch();
-    return cudaGetLastError();
+    if constexpr (K == 0) {
+        return launch_kg<0, 1>(p, tx, tw, smem, s);
+    } else {
+        const int chunks = p.E_pad / 32;
+        if (chunks <= 1) return launch_kg<K, 1>(p, tx, tw, smem, s);
+        if (chunks == 2) return launch_kg<K, 2>(p, tx, tw, smem, s);
+        if (chunks == 3) return launch_kg<K, 3>(p, tx, tw, smem, s);
+        return launch_kg<K, 4>(p, tx, tw, smem, s);
+    }
 }
 
 }  // namespace

@@ -145,6 +145,90 @@ soft_loss_kernel(const float* __restrict__ P, int T, int E, float weight, float*
     if (threadIdx.x == 0) *loss = weight * s / (float)E;
 }
 
+// Sum of one value per thread over a block of at most 1024 threads, in a fixed order (warp
+// butterflies, then the warp sums in warp order); every thread gets the result.
+__device__ __forceinline__ float block_sum(float v) {
+    __shared__ float s_w[32];
+    __shared__ float s_tot;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = warp_sum(v);
+    __syncthreads();   // s_w / s_tot free from a previous call
+    if (lane == 0) s_w[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += s_w[w];
+        s_tot = t;
+    }
+    __syncthreads();
+    return s_tot;
+}
+
+// Sliding window of soft loads ("Expert Parallelism", section 2.3: load statistics over the
+// last batches rather than one). One block, thread e = expert e. state[0] is the ring slot of
+// this batch, state[1] the batches already in the window. This batch's P goes into its slot;
+// Pbar_e = (sum of the window's n = min(state[1] + 1, W) loads, oldest first) / n;
+// loss = weight * mean_e (Pbar_e - mean(Pbar))^2; then the state advances. A state out of
+// range records MOE_ERR_DEVICE_BOUNDS and restarts the window.
+__global__ void __launch_bounds__(MOE_MAX_EXPERTS)
+soft_window_kernel(const float* __restrict__ P, int E, int W, float weight, float* __restrict__ ring,
+                   int* __restrict__ state, float* __restrict__ Pbar, float* __restrict__ loss, int* err) {
+    pdl_wait();
+    __shared__ int s_pos, s_n;
+    if (threadIdx.x == 0) {
+        int pos = state[0], filled = state[1];
+        if (pos < 0 || pos >= W || filled < 0 || filled > W) {
+            raise_error(err, kErrBounds);
+            pos = 0;
+            filled = 0;
+        }
+        s_pos = pos;
+        s_n = min(filled + 1, W);
+    }
+    __syncthreads();
+    const int pos = s_pos, n = s_n, e = threadIdx.x;
+    float pb = 0.f;
+    if (e < E) {
+        const float pe = P[e];
+        ring[(size_t)pos * E + e] = pe;
+        float acc = 0.f;
+        for (int i = n - 1; i >= 1; --i) {   // slots pos - n + 1 .. pos - 1 (mod W): earlier batches
+            const int slot = pos - i < 0 ? pos - i + W : pos - i;
+            acc += ring[(size_t)slot * E + e];
+        }
+        pb = (acc + pe) / (float)n;
+        Pbar[e] = pb;
+    }
+    const float mean = block_sum(pb) / (float)E;
+    const float dv = e < E ? pb - mean : 0.f;
+    const float q = block_sum(dv * dv);
+    if (threadIdx.x == 0) {
+        if (loss) *loss = weight * q / (float)E;
+        state[0] = pos + 1 == W ? 0 : pos + 1;
+        state[1] = n;
+    }
+}
+
+// g_e = weight * 2 (P_e - mean) / E into s_g (every thread of the block calls this). One batch
+// (win_n null): mean = T/E exactly, since each token's softmax sums to 1. A window mean load
+// (win_n = the window's batch count n): mean = mean_e P_e (fixed order) and g is divided by n,
+// the gradient reaching only the current batch's share of the mean.
+__device__ __forceinline__ void soft_grad_vector(const float* __restrict__ P, int Tn, int E, float weight,
+                                                 const int* __restrict__ win_n, float* s_g) {
+    float mean = (float)Tn / (float)E, scale = 1.f;
+    if (win_n) {
+        float v = 0.f;
+        for (int e = threadIdx.x; e < E; e += blockDim.x) v += P[e];
+        mean = block_sum(v) / (float)E;
+        scale = 1.f / (float)max(1, *win_n);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const float g = weight * 2.f * (P[e] - mean) / (float)E;
+        s_g[e] = win_n ? g * scale : g;
+    }
+    __syncthreads();
+}
+
 // For rows that are no multiple of 16 bytes. 8 tokens per block (x), V columns per thread (y).
 // dz_te = p_te (g_e - sum_j p_tj g_j) / temp for the block's tokens (written to dz by the first
 // column block), then dx[t, c..c+V) += sum_e dz_te Wg[e, c..c+V), experts in ascending order,
@@ -152,15 +236,13 @@ soft_loss_kernel(const float* __restrict__ P, int T, int E, float weight, float*
 template <typename T>
 __global__ void __launch_bounds__(kDxThreads)
 soft_dz_dx_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, int d,
-                  float inv_temp, float weight, const T* __restrict__ Wg, T* __restrict__ dx,
-                  float* __restrict__ dz) {
+                  float inv_temp, float weight, const int* __restrict__ win_n, const T* __restrict__ Wg,
+                  T* __restrict__ dx, float* __restrict__ dz) {
     pdl_wait();
     constexpr int V = Vec16<T>::N;
     __shared__ float s_g[MOE_MAX_EXPERTS];
     __shared__ float s_dz[kDxTok][MOE_MAX_EXPERTS];
-    const float mean = (float)Tn / (float)E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_g[e] = weight * 2.f * (P[e] - mean) / (float)E;
-    __syncthreads();
+    soft_grad_vector(P, Tn, E, weight, win_n, s_g);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kDxTok;
     const int nt = min(kDxTok, Tn - t0);
@@ -335,12 +417,10 @@ __device__ __forceinline__ void lds8(const T* p, float* out) {
 // dz_te = p_te (g_e - sum_j p_tj g_j) / temp, one warp per token.
 __global__ void __launch_bounds__(kSoftThreads)
 soft_dz_kernel(const float* __restrict__ logits, const float* __restrict__ P, int Tn, int E, float inv_temp,
-               float weight, float* __restrict__ dz) {
+               float weight, const int* __restrict__ win_n, float* __restrict__ dz) {
     pdl_wait();
     __shared__ float s_g[MOE_MAX_EXPERTS];
-    const float mean = (float)Tn / (float)E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_g[e] = weight * 2.f * (P[e] - mean) / (float)E;
-    __syncthreads();
+    soft_grad_vector(P, Tn, E, weight, win_n, s_g);
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
@@ -799,16 +879,24 @@ cudaError_t launch_soft_balance(const moe_config_t& c, const float* logits, floa
     return cudaGetLastError();
 }
 
+cudaError_t launch_soft_window(const moe_config_t& c, const float* P, float weight, int W, float* ring,
+                               int32_t* state, float* Pbar, float* loss, cudaStream_t st) {
+    launch_pdl(soft_window_kernel, 1, MOE_MAX_EXPERTS, 0, st, P, c.E, W, weight, ring, (int*)state, Pbar, loss,
+               device_error_word());
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, const float* P, float weight,
-                                    const void* x, const void* Wg, void* dx, float* dWg, float* dbg,
-                                    const SoftScratch& s, cudaStream_t st) {
+                                    const int32_t* win_n, const void* x, const void* Wg, void* dx, float* dWg,
+                                    float* dbg, const SoftScratch& s, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
     const float inv_temp = 1.0f / c.temperature;
     if (soft_tc_ok(c)) {
         // dz on CUDA cores, both contractions on the tensor cores
         const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
         cudaError_t e = launch_pdl(soft_dz_kernel, dim3(g0), dim3(kSoftThreads), 0, st, logits, P, c.T, c.E,
-                                   inv_temp, weight, s.dz);
+                                   inv_temp, weight, (const int*)win_n, s.dz);
         count_launch();
         if (e != cudaSuccess) return e;
         if ((e = launch_soft_split(c, s.dz, dbg != nullptr, s, st)) != cudaSuccess) return e;
@@ -817,7 +905,8 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
     }
     if (tiled_ok(c, Wg, dx)) {
         const int g0 = std::max(1, std::min(ceil_div(c.T, kSoftThreads / 32), num_sms() * 8));
-        launch_pdl(soft_dz_kernel, g0, kSoftThreads, 0, st, logits, P, c.T, c.E, inv_temp, weight, s.dz);
+        launch_pdl(soft_dz_kernel, g0, kSoftThreads, 0, st, logits, P, c.T, c.E, inv_temp, weight,
+                   (const int*)win_n, s.dz);
         count_launch();
         dim3 g(ceil_div(c.T, 16), ceil_div(c.d, kTileCols));
         if (c.dtype == MOE_BF16) {
@@ -840,11 +929,11 @@ cudaError_t launch_soft_balance_bwd(const moe_config_t& c, const float* logits, 
         const int V = c.dtype == MOE_BF16 ? 8 : 4;
         dim3 g0(ceil_div(c.T, kDxTok), ceil_div(c.d, kDxThreads * V));
         if (c.dtype == MOE_BF16)
-            launch_pdl(soft_dz_dx_kernel<__nv_bfloat16>, g0, kDxThreads, 0, st, 
-                logits, P, c.T, c.E, c.d, inv_temp, weight, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
+            launch_pdl(soft_dz_dx_kernel<__nv_bfloat16>, g0, kDxThreads, 0, st, logits, P, c.T, c.E, c.d, inv_temp,
+                       weight, (const int*)win_n, (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, s.dz);
         else
             launch_pdl(soft_dz_dx_kernel<float>, g0, kDxThreads, 0, st, logits, P, c.T, c.E, c.d, inv_temp, weight,
-                                                                (const float*)Wg, (float*)dx, s.dz);
+                       (const int*)win_n, (const float*)Wg, (float*)dx, s.dz);
         count_launch();
     }
     cudaError_t e = cudaGetLastError();

@@ -89,6 +89,22 @@ def soft_balance_backward(cfg, logits, P, weight, x, Wg, dx, dWg, dbg, ws, strea
         _p(dbg), _p(ws), _s(stream)))
 
 
+def soft_balance_window(cfg, logits, weight, W, ring, state, P, Pbar, loss, ws, stream=None):
+    """Soft load P [E] of this batch into the caller's ring [W, E] (slot state[0]), window
+    mean Pbar [E] and weight * mean_e (Pbar_e - mean Pbar)^2 into loss [1]; advances state [2]
+    (int32; zero it before the first batch)."""
+    L.check("moe_soft_balance_window", L.load().moe_soft_balance_window(
+        ctypes.byref(cfg), _p(logits), ctypes.c_float(weight), int(W), _p(ring), _p(state), _p(P), _p(Pbar),
+        _p(loss), _p(ws), _s(stream)))
+
+
+def soft_balance_window_backward(cfg, logits, Pbar, weight, state, x, Wg, dx, dWg, dbg, ws, stream=None):
+    """Adds the window loss's gradient (through this batch only) into dx, dWg and (if given) dbg."""
+    L.check("moe_soft_balance_window_backward", L.load().moe_soft_balance_window_backward(
+        ctypes.byref(cfg), _p(logits), _p(Pbar), ctypes.c_float(weight), _p(state), _p(x), _p(Wg), _p(dx),
+        _p(dWg), _p(dbg), _p(ws), _s(stream)))
+
+
 def dispatch(cfg, idx, x, b, stream=None):
     L.check("moe_dispatch", L.load().moe_dispatch(
         ctypes.byref(cfg), _p(idx), _p(x), _p(b["kept"]), _p(b["offsets"]), _p(b["row_token"]),
@@ -142,6 +158,35 @@ def selftest_wait_timeout(mode, budget_cycles, timed_out, scratch, stream=None):
     mbarrier phase, mode 1: a grid barrier); read the resulting timeout with get_error()."""
     L.check("moe_selftest_wait_timeout", L.load().moe_selftest_wait_timeout(
         int(mode), int(budget_cycles), _p(timed_out), _p(scratch), _s(stream)))
+
+
+class KernelTrace:
+    """Device time of every kernel the library launches from this thread while the context
+    is open (moe_trace_begin / moe_trace_end): `records` is a list of (kernel name, ms) in
+    launch order. Launches on a stream being captured into a graph are not traced."""
+
+    def __init__(self, max_launches=256):
+        self.max_launches = int(max_launches)
+        self.records = []
+
+    def __enter__(self):
+        L.check("moe_trace_begin", L.load().moe_trace_begin(self.max_launches))
+        return self
+
+    def __exit__(self, *exc):
+        lib = L.load()
+        n = lib.moe_trace_end()
+        if exc[0] is not None:
+            return False
+        if n < 0:
+            raise L.MoeError("moe_trace_end", n)
+        name = ctypes.c_char_p()
+        ms = ctypes.c_float()
+        for i in range(n):
+            L.check("moe_trace_record", lib.moe_trace_record(i, ctypes.byref(name), ctypes.byref(ms)))
+            self.records.append((name.value.decode(), float(ms.value)))
+        self.dropped = int(lib.moe_trace_dropped())
+        return False
 
 
 def get_error(stream=None):
