@@ -18,19 +18,21 @@ namespace {
 
 constexpr int kSortTok = 256;   // tokens per block in the histogram / rank kernels
 
-// The whole sort in one cooperative launch (all blocks co-resident, grid barriers between
-// phases; each barrier wait is bounded and records kErrTimeout if it runs out):
-//   1. per-chunk expert histograms (chunks of kSortTok tokens, checked for bad/repeated ids)
-//   2. per-expert exclusive scans over the chunks (chunk bases) and the totals (counts)
-//   3. every block derives kept / bucket offsets / assignment offsets from the counts, then
-//      ranks its chunks' assignments with per-expert token bitmasks (population counts) and
-//      writes slot_row, row_token (padding rows -1) and the expert-major assignment list.
+// The whole sort in one cooperative launch (all blocks co-resident, one grid barrier; its
+// wait is bounded and records kErrTimeout if it runs out). Block b owns the contiguous chunks
+// [b q, (b + 1) q) of kSortTok tokens:
+//   1. per-chunk expert histograms of its chunks (checked for bad/repeated ids)
+//   -- grid barrier --
+//   2. every block reads all chunk histograms: the expert totals (counts), and the sum over
+//      the chunks before its own (the rank base of its first chunk)
+//   3. kept / bucket offsets / assignment offsets from the counts, then the ranks of its
+//      chunks' assignments from per-expert token bitmasks (population counts), in chunk order
+//      with the base advanced by each chunk's histogram; it writes slot_row, row_token
+//      (padding rows -1) and the expert-major assignment list.
 struct SortArgs {
     const int32_t* idx;
     int T, k, E, C, align, nchunk;
     int32_t* blk_hist;
-    int32_t* blk_base;
-    int32_t* counts;
     int32_t* assign_off;
     int32_t* assign_tok;
     int32_t* kept;       // bucket outputs: null in assignment-only mode
@@ -68,20 +70,27 @@ __device__ int block_exclusive_scan(int* buf, int n) {
 __global__ void __launch_bounds__(kSortTok)
 sort_kernel(SortArgs a) {
     constexpr int W = kSortTok / 32;
+    constexpr int NW = kSortTok / 32;     // warps per block
     __shared__ uint32_t s_mask[MOE_MAX_EXPERTS * W];
     __shared__ int s_h[MOE_MAX_EXPERTS];
     __shared__ int s_scan[kSortTok];
     __shared__ int s_off[MOE_MAX_EXPERTS + 1];
     __shared__ int s_aoff[MOE_MAX_EXPERTS + 1];
     __shared__ int s_kept[MOE_MAX_EXPERTS];
+    __shared__ int s_cnt[MOE_MAX_EXPERTS];
+    __shared__ int s_base[MOE_MAX_EXPERTS];
+    __shared__ int s_part[2][NW][MOE_MAX_EXPERTS];
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x;
+    const int q = (a.nchunk + G - 1) / G;
+    const int c0 = min(a.nchunk, (int)blockIdx.x * q), c1 = min(a.nchunk, c0 + q);
     // the next kernel may start its prologue once every block has passed this point, i.e. once
     // the whole cooperative grid is resident
     pdl_wait();
 
-    // ---- phase 1: chunk histograms
-    for (int ch = blockIdx.x; ch < a.nchunk; ch += G) {
+    // ---- phase 1: histograms of this block's chunks
+    for (int ch = c0; ch < c1; ++ch) {
         for (int e = tid; e < a.E; e += blockDim.x) s_h[e] = 0;
         __syncthreads();
         const int t = ch * kSortTok + tid;
@@ -102,24 +111,32 @@ sort_kernel(SortArgs a) {
     }
     if (!grid_barrier(a.bar, (unsigned)G, a.err)) return;
 
-    // ---- phase 2: per-expert scans over the chunks
-    for (int e = blockIdx.x; e < a.E; e += G) {
-        int carry = 0;
-        for (int c0 = 0; c0 < a.nchunk; c0 += kSortTok) {
-            const int n = min(kSortTok, a.nchunk - c0);
-            s_scan[tid] = tid < n ? __ldcg(a.blk_hist + (size_t)(c0 + tid) * a.E + e) : 0;
-            const int tot = block_exclusive_scan(s_scan, n);
-            if (tid < n) a.blk_base[(size_t)(c0 + tid) * a.E + e] = carry + s_scan[tid];
-            carry += tot;
-            __syncthreads();
+    // ---- phase 2: expert totals and this block's prefix, from all chunk histograms (warp w
+    // sums chunks w, w + NW, ...; the warp partials are then added in warp order)
+    for (int e = lane; e < a.E; e += 32) {
+        int tot = 0, pre = 0;
+#pragma unroll 4
+        for (int c = warp; c < a.nchunk; c += NW) {
+            const int v = __ldcg(a.blk_hist + (size_t)c * a.E + e);
+            tot += v;
+            pre += c < c0 ? v : 0;
         }
-        if (tid == 0) a.counts[e] = carry;
+        s_part[0][warp][e] = tot;
+        s_part[1][warp][e] = pre;
     }
-    if (!grid_barrier(a.bar, 2u * (unsigned)G, a.err)) return;
+    __syncthreads();
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        int tot = 0, pre = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) { tot += s_part[0][w][e]; pre += s_part[1][w][e]; }
+        s_cnt[e] = tot;
+        s_base[e] = pre;
+    }
+    __syncthreads();
 
     // ---- phase 3: offsets (every block), then ranks and the bucket layout
     for (int e = tid; e < a.E; e += blockDim.x) {
-        const int cnt = __ldcg(a.counts + e);
+        const int cnt = s_cnt[e];
         const int kept = min(cnt, a.C);
         s_kept[e] = kept;
         s_scan[e] = (kept + a.align - 1) / a.align * a.align;
@@ -153,7 +170,7 @@ sort_kernel(SortArgs a) {
         for (int e = blockIdx.x; e < a.E; e += G)
             for (int r = s_off[e] + s_kept[e] + tid; r < s_off[e + 1]; r += blockDim.x) a.row_token[r] = -1;
     }
-    for (int ch = blockIdx.x; ch < a.nchunk; ch += G) {
+    for (int ch = c0; ch < c1; ++ch) {
         for (int i = tid; i < a.E * W; i += blockDim.x) s_mask[i] = 0u;
         __syncthreads();
         const int t = ch * kSortTok + tid;
@@ -184,7 +201,7 @@ sort_kernel(SortArgs a) {
                 const uint32_t* m = s_mask + e * W;
                 int local = __popc(m[word] & (bit - 1u));
                 for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
-                const int rank = __ldcg(a.blk_base + (size_t)ch * a.E + e) + local;
+                const int rank = s_base[e] + local;
                 a.assign_tok[s_aoff[e] + rank] = t * a.k + j;
                 if (a.slot_row) {
                     if (rank < a.C) {
@@ -196,6 +213,14 @@ sort_kernel(SortArgs a) {
                     }
                 }
             }
+        }
+        __syncthreads();
+        // the next chunk's base: this chunk's assignments counted in
+        for (int e = tid; e < a.E; e += blockDim.x) {
+            int c = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < W; ++w2) c += __popc(s_mask[e * W + w2]);
+            s_base[e] += c;
         }
         __syncthreads();
     }
@@ -295,10 +320,8 @@ int sort_blocks(int T) { return T > 0 ? ceil_div(T, kSortTok) : 1; }
 void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s) {
     const int nblk = sort_blocks(c.T);
     s->blk_hist = ws.take<int32_t>((size_t)nblk * c.E);
-    s->blk_base = ws.take<int32_t>((size_t)nblk * c.E);
     s->assign_off = ws.take<int32_t>((size_t)c.E + 1);
     s->assign_tok = ws.take<int32_t>((size_t)c.T * c.k + 1);
-    s->counts = ws.take<int32_t>((size_t)c.E);
     s->bar = ws.take<unsigned>(1);
 }
 
@@ -323,7 +346,7 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     SortArgs a{};
     a.idx = idx; a.T = c.T; a.k = c.k; a.E = c.E; a.C = c.capacity; a.align = c.row_align;
     a.nchunk = sort_blocks(c.T);
-    a.blk_hist = s.blk_hist; a.blk_base = s.blk_base; a.counts = s.counts;
+    a.blk_hist = s.blk_hist;
     a.assign_off = s.assign_off; a.assign_tok = s.assign_tok;
     a.kept = kept; a.offsets = offsets; a.row_token = row_token; a.slot_row = slot_row;
     a.n_dropped = n_dropped; a.bar = s.bar; a.err = device_error_word();

@@ -66,11 +66,9 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
 
 // dispatch.cu: stable counting sort of the assignments by expert
 struct SortScratch {
-    int32_t* blk_hist;     // [nblk, E]
-    int32_t* blk_base;     // [nblk, E]
+    int32_t* blk_hist;     // [nblk, E] per-chunk expert histograms
     int32_t* assign_off;   // [E+1] exclusive scan of counts
     int32_t* assign_tok;   // [T*k] assignment (t*k+j) in expert-major, token-minor order
-    int32_t* counts;       // [E]
     unsigned* bar;         // grid-barrier counter of the cooperative sort
 };
 int sort_blocks(int T);
