@@ -6,8 +6,9 @@ over the 8, T=16384, d=1024, d_ff=4096, no capacity limit, bf16: 131,072 expert 
 The step is captured once into a CUDA graph (the same five C-ABI calls) and replayed;
 each call replayed as its own graph gives the per-call times, and a kernel trace (timing
 events around every launch) gives each kernel's own device time. Inputs are resident in
-HBM when the timed region starts; L2 is flushed (a 256 MB write) before every timed step,
-outside the step's events. Prints one JSON line.
+HBM when the timed region starts; L2 is flushed before every timed step, outside the step's
+events: a 256 MB write, then a 256 MB read of another buffer that evicts the written lines
+(so their write-back does not land in the step's first kernel). Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -29,6 +30,24 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % BF16 peak; permute GB/s"
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Empties L2 between timed steps: writes a 256 MB buffer (twice the 129 MB L2), then reads
+    another 256 MB buffer. The read evicts the written lines, so their write-back to HBM also
+    happens before the next timed step instead of inside its first kernel; the step then starts
+    with an L2 that holds only clean lines of an unrelated buffer."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        torch.amax(self.r, dim=0, out=self.sink)
 
 
 def _dist_env():
@@ -231,16 +250,17 @@ def gemm_source_hash():
 
 
 def measured_traffic(workload):
-    """DRAM bytes per launch of the forward GEMM pair from the committed ncu record, if it was
-    taken on this workload with the current GEMM sources (else None)."""
+    """DRAM bytes of one moe_expert_ffn call (its GEMM launches together) from the committed ncu
+    record, if one was taken on this workload with the current GEMM sources (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as fh:
             rec = json.load(fh)
     except Exception:
         return None
-    if rec.get("workload") != workload or rec.get("gemm_source_hash") != gemm_source_hash():
+    if rec.get("gemm_source_hash") != gemm_source_hash():
         return None
-    return rec.get("ffn_pair_dram_bytes_per_launch")
+    w = rec.get("workloads", {}).get(workload)
+    return None if w is None else w.get("expert_ffn_dram_bytes_per_call")
 
 
 def algorithmic_counts(cfg, kept_rows):
@@ -299,7 +319,8 @@ def kernel_rooflines(cfg, kept, trace, peaks):
       combine_kernel      N d es + T d es + T k 8
       combine_bwd_kernel  T d es + 2 N d es + T k 12         (dy, Yp, w, slot_row in; dYp, dw out)
       router_bwd_kernel   N d es + T d es + T k 12           (dXp, routing in; dx out)
-      each expert GEMM    2 N d d_ff flop (Ffn1, Ffn2, dH, dX, each of the two weight gradients)"""
+      each expert GEMM    2 N d d_ff flop (Ffn1, Ffn2, dH, dX, each of the two weight gradients;
+                          a row GEMM's time is that of its launches together)"""
     es = 2 if cfg.dtype == "bf16" else 4
     T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.d_ff
     N = kept
@@ -318,13 +339,16 @@ def kernel_rooflines(cfg, kept, trace, peaks):
         gbs = nbytes / (us * 1e-6) / 1e9
         out[label] = {"kernels": [f for f in fams if f in trace], "us": us, "algorithmic_mb": nbytes / 1e6,
                       "gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "bound": "hbm"}
+    # a row GEMM (Ffn1, Ffn2, dH, dX) is one or two launches (CTA-pair bodies + one-CTA tails):
+    # its time is their sum; the weight gradients are two whole GEMMs (dW2, dW1) per step
     for fam in ("ffn1", "ffn2", "dH", "dX", "wgrad"):
         if fam not in trace:
             continue
         t = trace[fam]
+        us = t["us_per_step"] / 2.0 if fam == "wgrad" else t["us_per_step"]
         flops = 2.0 * N * d * f
-        tf = flops / (t["us_per_launch"] * 1e-6) / 1e12
-        out[fam] = {"us": t["us_per_launch"], "launches_per_step": t["launches_per_step"],
+        tf = flops / (us * 1e-6) / 1e12
+        out[fam] = {"us": us, "launches_per_step": t["launches_per_step"],
                     "tflops": tf, "frac": tf / peaks["bf16_tflops"], "bound": "tensor"}
     return out
 
@@ -508,7 +532,7 @@ def run_ours(args, cfg):
     c = moe.config_from(cfg)
     forward_only = args.profile in ("route", "dispatch", "expert_ffn", "combine")
     b = moe.alloc_buffers(c, device=dev, backward=not forward_only)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     if args.profile:
         return profile_call(args, moe, c, d_in, b, flush, stream, forward_only)
@@ -570,7 +594,9 @@ def run_ours(args, cfg):
     trace_recs = []
     for i in range(args.steps + 1):
         flush.zero_()
-        torch.cuda.synchronize(dev)
+        # ~1 ms of GPU spin after the flush, so that the host has queued the whole traced step
+        # before its first kernel runs: no launch latency inside any kernel's event window
+        torch.cuda._sleep(2_000_000)
         with moe.KernelTrace(512) as tr:
             step()
         if i >= 1:
@@ -706,7 +732,8 @@ def run_ours(args, cfg):
             "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
                        "d_ff": cfg.d_ff, "capacity_factor": cfg.capacity_factor,
                        "temperature": cfg.temperature, "kept_assignments": kept,
-                       "l2": "flushed (256 MB write) before every timed step, outside its events",
+                       "l2": "flushed before every timed step, outside its events: a 256 MB write, then a "
+                             "256 MB read of another buffer (evicts the written lines)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"kernel": "tcgen05 grouped GEMM, forward pair (GEMM1+GELU, GEMM2)",
                          "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc,

@@ -42,7 +42,7 @@
  *   type selected by cfg->dtype: fp32 (MOE_F32) or bf16 (MOE_BF16) for x, weights,
  *   activations and their gradients. Routing weights, logits and bias gradients are fp32.
  * - Permuted rows live in expert buckets: bucket e holds rows [offsets[e], offsets[e+1]),
- *   offsets[e] is a multiple of cfg->row_align (128 or 256, chosen by moe_config_init), the
+ *   offsets[e] is a multiple of cfg->row_align (128 rows, set by moe_config_init), the
  *   first kept[e] rows are expert e's tokens in ascending token order and the rest of the
  *   bucket is padding (row_token = -1, zero rows in Xp). Buffers of permuted rows have
  *   cfg->rows_capacity rows.
@@ -87,7 +87,7 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
-#define MOE_ROW_ALIGN 128   /* minimum bucket alignment (rows); cfg->row_align is 128 or 256 */
+#define MOE_ROW_ALIGN 128   /* bucket alignment (rows); cfg->row_align */
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_K 8           /* largest top-k selection; k = E (dense) is allowed for any E */
 
@@ -116,9 +116,10 @@ typedef struct {
     /* derived by moe_config_init */
     int32_t capacity;          /* ceil(capacity_factor*T*k/E) in double, or INT32_MAX */
     int32_t rows_capacity;     /* rows of every permuted buffer (Xp, A, H, Yp) */
-    int32_t row_align;         /* bucket alignment: 256 when the average bucket can reach 1024
-                                  rows (min(T*k, E*C)/E >= 1024; the GEMMs then run 256-row
-                                  tiles on CTA pairs), else 128 */
+    int32_t row_align;         /* bucket alignment: MOE_ROW_ALIGN (128 rows). When the average
+                                  bucket can reach 1024 rows (min(T*k, E*C)/E >= 1024) the
+                                  expert GEMMs run each bucket's 256-row tiles on CTA pairs and
+                                  its odd 128-row tile at the end on one CTA */
 } moe_config_t;
 
 /* Validates the caller's fields and fills the derived ones. Must be called before any

@@ -61,8 +61,8 @@ def test_rows_capacity_bounds_every_bucket_layout(moe_lib):
         assert moe_lib.load().moe_config_init(ctypes.byref(c)) == 0
         C = c.capacity
         n_max = min(T * k, E * C)
-        # 256-row buckets only when an average bucket can reach 1024 rows
-        assert c.row_align == (256 if n_max >= 1024 * E else 128)
+        # 128-row buckets (the GEMM row tile) at every size
+        assert c.row_align == 128
         # worst case: every bucket wastes row_align - 1 rows of padding
         worst = n_max + (c.row_align - 1) * min(E, n_max)
         assert c.rows_capacity >= worst and c.rows_capacity % c.row_align == 0
@@ -80,7 +80,7 @@ def test_dense_routing_config(moe_lib, T, E, cf):
     kept = min(T, c.capacity)
     B = -(-kept // c.row_align) * c.row_align
     assert E * B <= c.rows_capacity
-    assert c.row_align == (256 if kept >= 1024 else 128)
+    assert c.row_align == 128
     assert moe_lib.load().moe_workspace_bytes(ctypes.byref(c)) > 0
 
 

@@ -38,11 +38,13 @@ int64_t derived_nmax(const moe_config_t& c, int64_t cap) {
     return std::min((int64_t)c.T * c.k, (int64_t)c.E * cap);
 }
 
-// 256-row buckets let the row GEMMs run 256-row tiles on CTA pairs; they pay up to 255 padding
-// rows per expert, so they are used only when an average bucket can reach 1024 rows.
-int32_t derived_align(const moe_config_t& c, int64_t cap) {
-    return derived_nmax(c, cap) >= 1024LL * c.E ? 256 : MOE_ROW_ALIGN;
-}
+// Buckets are padded to 128 rows (MOE_ROW_ALIGN), the row tile of the GEMMs.
+int32_t derived_align(const moe_config_t&, int64_t) { return MOE_ROW_ALIGN; }
+
+// The row GEMMs run on CTA pairs (256-row tiles; an odd bucket's last tile has a second half
+// past the bucket's end that is computed but not stored) when an average bucket can reach 1024
+// rows; below that most buckets are a few 128-row tiles and the one-CTA kernel takes them.
+bool pair_rows(const moe_config_t& c) { return derived_nmax(c, derived_capacity(c)) >= 1024LL * c.E; }
 
 int64_t derived_rows(const moe_config_t& c, int64_t cap) {
     const int64_t n_max = derived_nmax(c, cap);
@@ -165,7 +167,7 @@ bool use_tc(const moe_config_t& c) { return c.dtype == MOE_BF16 && tc_gemm_suppo
 
 cudaError_t row_gemm(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
     if (!use_tc(c)) return launch_row_gemm_simt(c, a, s);
-    return c.row_align == 256 ? launch_row_gemm_tc_pair(c, a, s) : launch_row_gemm_tc(c, a, s);
+    return pair_rows(c) ? launch_row_gemm_tc_pair(c, a, s) : launch_row_gemm_tc(c, a, s);
 }
 cudaError_t wgrad(const moe_config_t& c, const WgradArgs& a, cudaStream_t s) {
     if (c.rows_capacity == 0) {

@@ -276,6 +276,7 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_SMEM + 16 * sizeof(uint64_t) +
                               16 + kMaxOffsets * sizeof(int);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // ------------------------------------------------------------------------- host side
 template <int KIND, bool A_MN, bool B_MN>

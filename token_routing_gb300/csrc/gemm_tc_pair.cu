@@ -89,10 +89,14 @@ __device__ __forceinline__ void commit_pair_local(uint64_t* bar) {
 
 struct PairTile {
     int e, m0, n0, row0, kblocks;
+    int end;      // row GEMMs: first row past the tile's bucket (a half at or past it is not stored)
 };
 
+// Row GEMMs: pair tile r of the launch is the (r - pairs_before(e))-th 256-row tile of bucket e,
+// the largest e with pairs_before(e) <= r (s_q: the odd-bucket prefix).
 template <bool WGRAD>
-__device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const int* s_off, int tile) {
+__device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const int* s_off, const uint16_t* s_q,
+                                                     int tile) {
     PairTile t;
     const int nt = tile % p.n_tiles;
     const int rest = tile / p.n_tiles;
@@ -102,11 +106,13 @@ __device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const in
         t.e = rest / p.m_tiles;
         t.row0 = s_off[t.e];
         t.kblocks = (s_off[t.e + 1] - s_off[t.e]) / BK;
+        t.end = 0;
     } else {
-        t.m0 = rest * P_BM;          // buckets are 256-row aligned on this path
-        t.e = bucket_of(s_off, p.E, t.m0);
+        t.e = bucket_of_pair(s_off, s_q, p.E, rest);
+        t.m0 = s_off[t.e] + (rest - pairs_before(s_off, s_q, t.e)) * P_BM;
         t.row0 = t.m0;
         t.kblocks = p.K / BK;
+        t.end = s_off[t.e + 1];
     }
     return t;
 }
@@ -138,6 +144,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* s_fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+    uint16_t* s_q = reinterpret_cast<uint16_t*>(s_off + kMaxOffsets);   // odd-bucket prefix (row GEMMs)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -163,13 +170,17 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     // previous kernel's tail; global memory is read from here on
     pdl_wait();
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
+    if (!WGRAD) {
+        __syncthreads();
+        if (warp == 0) bucket_odd_prefix(s_off, p.E, s_q, lane);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     cluster_sync();  // both CTAs' barriers exist before any remote arrive or complete_tx
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = WGRAD ? p.E * p.m_tiles * p.n_tiles : (s_off[p.E] / P_BM) * p.n_tiles;
+    const int num_tiles = WGRAD ? p.E * p.m_tiles * p.n_tiles : pairs_before(s_off, s_q, p.E) * p.n_tiles;
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs): own A rows, own half of B
@@ -177,7 +188,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             uint32_t it = 0;
             bool ok = true;
             for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
-                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, tile);
+                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, s_q, tile);
                 const int mr = t.m0 + (int)rank * P_HALF;   // this CTA's rows of the tile
                 const int nh = t.n0 + (int)rank * P_HALF;   // this CTA's half of B's columns
                 for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
@@ -218,7 +229,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             uint32_t it = 0, tl = 0;
             bool ok = true;
             for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
-                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, tile);
+                const PairTile t = decode_pair_tile<WGRAD>(p, s_off, s_q, tile);
                 if (t.kblocks == 0) continue;
                 const int buf = tl & 1;
                 const uint32_t aph = (tl >> 1) & 1;
@@ -262,7 +273,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         const uint32_t tempty_leader[2] = {map_to_rank(smem_u32(tempty), 0), map_to_rank(smem_u32(tempty + 1), 0)};
         uint32_t tl = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += nclusters) {
-            const PairTile pt = decode_pair_tile<WGRAD>(p, s_off, tile);
+            const PairTile pt = decode_pair_tile<WGRAD>(p, s_off, s_q, tile);
             Tile t;
             t.e = pt.e; t.n0 = pt.n0; t.row0 = pt.row0; t.kblocks = pt.kblocks;
             t.m0 = pt.m0 + (int)rank * P_HALF;  // this CTA's rows
@@ -282,16 +293,26 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             const int buf = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            // the second half of an odd bucket's last tile lies past the bucket: computed by the
+            // pair's MMAs, not stored (its accumulator is only released)
+            const bool dead = !WGRAD && t.m0 >= pt.end;
             const size_t aux_row0 = (size_t)(t.m0 + quarter * 32 + (lane >> 2));
             // side input (bias row, or dH's saved GELU'(A)) of the first chunk, fetched while the
             // accumulator is produced; each later chunk's is fetched one chunk ahead
             Raw32 next;
-            if (t.n0 + c_lo < p.N) {
+            if (!dead && t.n0 + c_lo < p.N) {
                 if (has_bias<KIND>()) load_raw32(next, p.bias + (size_t)t.e * p.N + t.n0 + c_lo);
                 if (AUX) load_aux32<KIND>(next, p, aux_row0, t.n0 + c_lo, lane);
             }
             if (!mbar_wait(tfull + buf, aph, p.err)) break;
             tc_fence_after();
+            if (dead) {
+                tc_fence_before();
+                if (leader) mbar_arrive(tempty + buf);
+                else mbar_arrive_cluster(tempty_leader[buf]);
+                if (*s_fail) break;
+                continue;
+            }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN;
             // with PREFETCH the TMEM load of chunk c + 32 is in flight while chunk c is processed
             uint32_t acc[32];
@@ -391,7 +412,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
 template <int KIND>
 constexpr size_t pair_smem_bytes() {
     return 1024 + (size_t)pair_stages<KIND>() * P_STAGE_BYTES + pair_epi_bytes<KIND>() + 16 * sizeof(uint64_t) +
-           16 + kMaxOffsets * sizeof(int);
+           16 + kMaxOffsets * (sizeof(int) + sizeof(uint16_t));
 }
 static_assert(pair_smem_bytes<kGemmFfn1>() <= 227 * 1024 && pair_smem_bytes<kGemmFfn2>() <= 227 * 1024,
               "shared memory per CTA");
@@ -412,14 +433,14 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap& a, const CUtensorM
 
 cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s) {
     if (a.rows_capacity == 0) return cudaSuccess;
-    if (a.rows_capacity % P_BM != 0) return cudaErrorInvalidValue;  // 256-row tiles need 256-row buckets
+    if (a.rows_capacity % BM != 0) return cudaErrorInvalidValue;  // buckets are 128-row aligned
     TcParams p{};
     p.kind = a.kind;
     p.offsets = a.offsets;
     const int rows_valid = a.rows_valid > 0 ? a.rows_valid : a.rows_capacity;
     p.E = a.E; p.N = a.N; p.K = a.K; p.M = rows_valid;
     p.n_tiles = ceil_div(a.N, BN);
-    p.m_tiles = a.rows_capacity / P_BM;
+    p.m_tiles = ceil_div(a.rows_capacity, P_BM);   // (grid sizing) pair tiles per column block, at most
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
     p.aux = static_cast<const __nv_bfloat16*>(a.aux);
     p.out0 = static_cast<__nv_bfloat16*>(a.out0);

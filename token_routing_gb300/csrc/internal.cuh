@@ -93,7 +93,8 @@ cudaError_t launch_row_gemm_tc(const moe_config_t& c, const RowGemmArgs& a, cuda
 cudaError_t launch_wgrad_tc(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
 // gemm_tc_pair.cu: weight gradients on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles)
 cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cudaStream_t s);
-// row GEMMs on CTA pairs: 256-row tiles, needs cfg.row_align == 256
+// row GEMMs on CTA pairs: 256-row tiles of each bucket (an odd bucket's last tile computes a
+// second half past the bucket's end, not stored)
 cudaError_t launch_row_gemm_tc_pair(const moe_config_t& c, const RowGemmArgs& a, cudaStream_t s);
 
 // soft_balance.cu: differentiable balance loss on the soft load

@@ -121,6 +121,10 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
 
     if (warp == 0) {
         if (lane == 0) {
+            // Each CTA starts its walk along d at its own k-block (CTA index mod the k-block
+            // count) and wraps around: otherwise every CTA reads the same 128-byte column block
+            // of its rows, and of Wg, at the same time.
+            const int kb0 = (int)(blockIdx.x % (unsigned)kblocks);
             bool ok = true;
             int kb = 0;
             for (; kb < kblocks; ++kb) {
@@ -128,9 +132,10 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                 const uint32_t ph = (kb / RSTAGES) & 1;
                 if (!mbar_wait(empty + s, ph ^ 1, p.err)) { ok = false; break; }
                 const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                const int kc = kb + kb0 < kblocks ? kb + kb0 : kb + kb0 - kblocks;
                 mbar_expect_tx(full + s, p.rows * RBK * 2 + p.E_pad * RBK * 2);
-                tma_load_2d(sa, &tmX, kb * RBK, tok0, full + s);
-                tma_load_2d(sa + RBM * RBK * 2, &tmW, kb * RBK, 0, full + s);
+                tma_load_2d(sa, &tmX, kc * RBK, tok0, full + s);
+                tma_load_2d(sa + RBM * RBK * 2, &tmW, kc * RBK, 0, full + s);
             }
             if (!ok) {
                 s_fail = 1;

@@ -67,6 +67,52 @@ __device__ __forceinline__ int bucket_of(const int* s_off, int E, int row) {
     return lo;
 }
 
+// Pair tiles of the row GEMMs on CTA pairs: bucket e (128-row aligned, n_e tiles of 128 rows)
+// has ceil(n_e / 2) pair tiles of 256 rows; when n_e is odd the last one's second half lies
+// past the bucket's end (its rows are computed but not stored). s_q[e] = number of buckets
+// before e with an odd n_e (<= 256, so 16 bits), s_q[E] = all of them; the pair tiles before
+// bucket e then number (offsets[e] / 128 + s_q[e]) / 2. Warp 0 only (E <= 256: 8 buckets per
+// lane, then a warp scan of the lane sums).
+__device__ __forceinline__ void bucket_odd_prefix(const int* s_off, int E, uint16_t* s_q, int lane) {
+    int odd[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        odd[i] = e < E ? (((s_off[e + 1] - s_off[e]) / BM) & 1) : 0;
+        sum += odd[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        if (e < E) s_q[e] = (uint16_t)run;
+        run += odd[i];
+    }
+    if (lane == 31) s_q[E] = (uint16_t)incl;
+}
+
+// Number of pair tiles in buckets 0 .. e-1.
+__device__ __forceinline__ int pairs_before(const int* s_off, const uint16_t* s_q, int e) {
+    return (s_off[e] / BM + (int)s_q[e]) >> 1;
+}
+
+// The bucket of pair tile r: the largest e with pairs_before(e) <= r.
+__device__ __forceinline__ int bucket_of_pair(const int* s_off, const uint16_t* s_q, int E, int r) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pairs_before(s_off, s_q, mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
 template <bool WGRAD>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* s_off, int tile) {
     Tile t;
