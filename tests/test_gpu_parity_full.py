@@ -157,8 +157,9 @@ def test_full_size(name, moe_lib, cuda_device):
     P.assert_close("dW2", np.array(g_dW2), np.array(o_dW2), t)
     P.assert_close("db2", np.array(g_db2), np.array(o_db2), t)
     # experts without rows have exactly zero gradients
-    for e in np.nonzero(dsp["kept"] == 0)[0][:4]:
-        assert (b["dW1"][e] == 0).all() and (b["dW2"][e] == 0).all()
+    empty = torch.as_tensor(np.nonzero(dsp["kept"] == 0)[0], device=b["dW1"].device)
+    if empty.numel():
+        assert (b["dW1"][empty] == 0).all() and (b["dW2"][empty] == 0).all()
 
     # ---------------- gate gradient on the least-loaded expert that has assignments
     cand = np.nonzero(r["counts"] > 0)[0]

@@ -158,14 +158,17 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     } else {
         // ---------------- epilogue warps 2..9: TMEM lane quarter = warp % 4, column half
         const int quarter = warp & 3;
-        const int row_in_tile = quarter * 32 + lane;
         const int c_lo = ((warp - 2) >> 2) * (BN / 2);
         Stager st{smem_u32(stg_smem + (warp - 2) * 2 * STG_BYTES), 0};
         uint32_t tl = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Tile t = decode_tile<WGRAD>(p, s_off, tile);
             if (t.kblocks == 0) {
-                if (WGRAD) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
+                // an expert with no rows: its weight-gradient tile is zero
+                const int y = t.m0 + quarter * 32;
+                const int cols = min(BN / 2, p.N - (t.n0 + c_lo));
+                if (WGRAD && y < p.M && cols > 0)
+                    st.store_zero(lane, st.acquire(lane), &tmO0, t.n0 + c_lo, (cols + 31) / 32, t.e * p.M + y);
                 continue;
             }
             const int buf = tl & 1;

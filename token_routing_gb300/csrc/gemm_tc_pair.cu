@@ -279,7 +279,12 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
             t.m0 = pt.m0 + (int)rank * P_HALF;  // this CTA's rows
             const int row_in_tile = quarter * 32 + lane;
             if (t.kblocks == 0) {
-                if (KIND == kGemmWgrad) epilogue_zero<KIND>(p, t, row_in_tile, c_lo);
+                if (KIND == kGemmWgrad) {
+                    const int y = t.m0 + quarter * 32;
+                    const int cols = min(COLS, p.N - (t.n0 + c_lo));
+                    if (y < p.M && cols > 0)
+                        st.store_zero(lane, st.acquire(lane), &tmO0, t.n0 + c_lo, (cols + 31) / 32, t.e * p.M + y);
+                }
                 if (KIND == kGemmWgradF32) {
                     const int m = t.m0 + row_in_tile;
                     for (int c = c_lo; c < c_lo + COLS && m < p.M; c += 32)

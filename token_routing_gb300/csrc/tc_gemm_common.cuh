@@ -237,6 +237,21 @@ struct Stager {
         }
         ++count;
     }
+    // Zeros to `boxes` 32x32 boxes side by side (columns x0, x0 + 32, ...; rows y .. y + 31)
+    // from one zeroed buffer, in one bulk group: the weight-gradient tile of an expert that
+    // received no rows.
+    __device__ __forceinline__ void store_zero(int lane, uint32_t buf, const CUtensorMap* tm, int x0, int boxes, int y) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sts128(buf + lane * 64 + j * 16, z);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            for (int i = 0; i < boxes; ++i) tma_store_2d(tm, buf, x0 + 32 * i, y);
+            bulk_commit();
+        }
+        ++count;
+    }
 };
 
 // Two outputs per 32-column chunk (Ffn1: GELU'(A) and H): NB buffer pairs of one epilogue
@@ -300,19 +315,6 @@ __device__ __forceinline__ float2 staged_colsum32(uint32_t buf, int lane) {
     s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
     return make_float2(s0, s1);
 }
-
-template <int KIND>
-__device__ __forceinline__ void epilogue_zero(const TcParams& p, const Tile& t, int row_in_tile, int c_lo) {
-    // an expert with no rows: its weight-gradient tile is zero
-    float z[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = 0.f;
-    const int m = t.m0 + row_in_tile;
-    if (m >= p.M) return;
-    for (int c = c_lo; c < c_lo + BN / 2; c += 32)
-        if (t.n0 + c < p.N) store_row32(p.out0 + ((size_t)t.e * p.M + m) * p.N + t.n0 + c, z);
-}
-
 
 }  // namespace
 }  // namespace moe
