@@ -326,7 +326,7 @@ def kernel_rooflines(cfg, kept, trace, peaks):
     N = kept
     mem = {
         "route": (["route_tc_kernel", "route_kernel"], T * d * es + E * d * es + T * k * 8.0),
-        "dispatch": (["sort_kernel", "gather_kernel", "dense_layout_kernel"], T * d * es + N * d * es + 4.0 * (N + T * k)),
+        "dispatch": (["sort_hist_kernel", "sort_rank_kernel", "gather_kernel", "dense_layout_kernel"], T * d * es + N * d * es + 4.0 * (N + T * k)),
         "combine": (["combine_kernel"], N * d * es + T * d * es + T * k * 8.0),
         "combine_bwd": (["combine_bwd_kernel"], T * d * es + 2.0 * N * d * es + T * k * 12.0),
         "router_bwd": (["router_bwd_kernel", "router_bwd_wide_kernel"], N * d * es + T * d * es + T * k * 12.0),

@@ -35,8 +35,8 @@ def test_trace_names_and_times_every_launch(moe_lib, cuda_device):
     launched = moe.kernel_launches() - n0
     assert len(tr.records) == launched and tr.dropped == 0
     names = [n for n, _ in tr.records]
-    for base in ("route_tc_kernel", "sort_kernel", "gather_kernel", "tc_gemm_kernel", "combine_kernel",
-                 "combine_bwd_kernel", "router_bwd_kernel"):
+    for base in ("route_tc_kernel", "sort_hist_kernel", "sort_rank_kernel", "gather_kernel", "tc_gemm_kernel",
+                 "combine_kernel", "combine_bwd_kernel", "router_bwd_kernel"):
         assert any(n.split("<")[0] == base for n in names), (base, names)
     assert all(ms > 0.0 for _, ms in tr.records)
     n = int(b["offsets"][-1].item())   # rows past the buckets in use are unspecified

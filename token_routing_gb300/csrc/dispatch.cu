@@ -8,27 +8,26 @@
 //
 // The sort is deterministic: the rank of assignment (t, j) -> e is the number of earlier
 // tokens that picked e, computed as (per-chunk histogram -> column scan over chunks) +
-// (population count of e's token bitmask inside the chunk). Buckets are padded to the configured alignment (128 or
-// 256 rows) so that every GEMM row tile belongs to exactly one expert.
+// (population count of e's token bitmask inside the chunk). Buckets are padded to the row
+// alignment (128 rows) so that every GEMM row tile belongs to exactly one expert.
 #include "internal.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kSortTok = 256;   // tokens per block in the histogram / rank kernels
+constexpr int kSortTok = 256;   // tokens per chunk (one block per chunk in both sort kernels)
 
-// The whole sort in one cooperative launch (all blocks co-resident, one grid barrier; its
-// wait is bounded and records kErrTimeout if it runs out). Block b owns the contiguous chunks
-// [b q, (b + 1) q) of kSortTok tokens:
-//   1. per-chunk expert histograms of its chunks (checked for bad/repeated ids)
-//   -- grid barrier --
-//   2. every block reads all chunk histograms: the expert totals (counts), and the sum over
-//      the chunks before its own (the rank base of its first chunk)
-//   3. kept / bucket offsets / assignment offsets from the counts, then the ranks of its
-//      chunks' assignments from per-expert token bitmasks (population counts), in chunk order
-//      with the base advanced by each chunk's histogram; it writes slot_row, row_token
-//      (padding rows -1) and the expert-major assignment list.
+// The sort in two launches, one block per chunk of kSortTok tokens:
+//   sort_hist_kernel  the chunk's expert histogram (ids checked for range and repeats)
+//   sort_rank_kernel  every block reads all chunk histograms: the expert totals (counts) and
+//                     the sum over the chunks before its own (its rank base); then kept /
+//                     bucket offsets / assignment offsets from the counts, and the ranks of its
+//                     chunk's assignments from per-expert token bitmasks (population counts). It
+//                     writes slot_row, row_token (padding rows -1) and the expert-major
+//                     assignment list.
+// The kernel boundary orders the two phases: there is no grid barrier and no co-residency
+// requirement.
 struct SortArgs {
     const int32_t* idx;
     int T, k, E, C, align, nchunk;
@@ -40,120 +39,138 @@ struct SortArgs {
     int32_t* row_token;
     int32_t* slot_row;
     int32_t* n_dropped;
-    unsigned* bar;       // zeroed before the launch
     int* err;
 };
 
-// Exclusive scan of n <= blockDim.x values in shared memory (blockDim.x = 256); returns the total.
-__device__ int block_exclusive_scan(int* buf, int n) {
-    __shared__ int s_tot;
-    const int tid = threadIdx.x;
-    int v = tid < n ? buf[tid] : 0;
-    __syncthreads();
-    for (int off = 1; off < (int)blockDim.x; off <<= 1) {
-        const int other = tid >= off ? buf[tid - off] : 0;
-        __syncthreads();
-        if (tid < n) buf[tid] = (tid >= off ? other : 0) + buf[tid];
-        __syncthreads();
+// Exclusive scans of two arrays of n <= blockDim.x values in shared memory (blockDim.x a
+// multiple of 32, at most 1024): warp scans by shuffles, then the warp totals. The totals are
+// returned in *tot_a, *tot_b.
+__device__ void block_exclusive_scan2(int* a, int* b, int n, int* tot_a, int* tot_b) {
+    __shared__ int s_wa[32], s_wb[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int va = tid < n ? a[tid] : 0, vb = tid < n ? b[tid] : 0;
+    int ia = va, ib = vb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, ia, off), xb = __shfl_up_sync(0xffffffffu, ib, off);
+        if (lane >= off) { ia += xa; ib += xb; }
     }
-    // buf now holds inclusive sums
-    if (tid == n - 1) s_tot = buf[tid];
+    if (lane == 31) { s_wa[warp] = ia; s_wb[warp] = ib; }
     __syncthreads();
-    const int incl = tid < n ? buf[tid] : 0;
+    int pa = 0, pb = 0, ta = 0, tb = 0;
+    const int nw = (int)blockDim.x >> 5;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) { pa += s_wa[w]; pb += s_wb[w]; }
+        ta += s_wa[w]; tb += s_wb[w];
+    }
+    if (tid < n) { a[tid] = pa + ia - va; b[tid] = pb + ib - vb; }
+    *tot_a = ta;
+    *tot_b = tb;
     __syncthreads();
-    if (tid < n) buf[tid] = incl - v;
-    const int tot = n > 0 ? s_tot : 0;
-    __syncthreads();
-    return tot;
+}
+
+// The experts of token t's k slots, in slot order; -1 for an id out of range or repeated
+// (reported through the error word when `report`).
+__device__ __forceinline__ void token_experts(const SortArgs& a, int t, int (&mine)[MOE_MAX_K], bool report) {
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
+    for (int j = 0; j < a.k; ++j) {
+        const int e = a.idx[(size_t)t * a.k + j];
+        bool ok = (e >= 0 && e < a.E);
+        for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
+        if (ok) mine[j] = e;
+        else if (report) raise_error(a.err, kErrBounds);
+    }
 }
 
 __global__ void __launch_bounds__(kSortTok)
-sort_kernel(SortArgs a) {
-    constexpr int W = kSortTok / 32;
-    constexpr int NW = kSortTok / 32;     // warps per block
-    __shared__ uint32_t s_mask[MOE_MAX_EXPERTS * W];
+sort_hist_kernel(SortArgs a) {
     __shared__ int s_h[MOE_MAX_EXPERTS];
-    __shared__ int s_scan[kSortTok];
+    const int tid = threadIdx.x, ch = blockIdx.x;
+    for (int e = tid; e < a.E; e += blockDim.x) s_h[e] = 0;
+    pdl_wait();
+    __syncthreads();
+    const int t = ch * kSortTok + tid;
+    if (t < a.T) {
+        int mine[MOE_MAX_K];
+        token_experts(a, t, mine, true);
+        for (int j = 0; j < a.k; ++j)
+            if (mine[j] >= 0) atomicAdd(&s_h[mine[j]], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < a.E; e += blockDim.x) a.blk_hist[(size_t)ch * a.E + e] = s_h[e];
+}
+
+__global__ void __launch_bounds__(kSortTok)
+sort_rank_kernel(SortArgs a) {
+    constexpr int W = kSortTok / 32;      // mask words per expert
+    __shared__ uint32_t s_mask[MOE_MAX_EXPERTS * W];
     __shared__ int s_off[MOE_MAX_EXPERTS + 1];
     __shared__ int s_aoff[MOE_MAX_EXPERTS + 1];
     __shared__ int s_kept[MOE_MAX_EXPERTS];
     __shared__ int s_cnt[MOE_MAX_EXPERTS];
     __shared__ int s_base[MOE_MAX_EXPERTS];
-    __shared__ int s_part[2][NW][MOE_MAX_EXPERTS];
+    __shared__ int s_part[2][kSortTok];
     const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int G = gridDim.x;
-    const int q = (a.nchunk + G - 1) / G;
-    const int c0 = min(a.nchunk, (int)blockIdx.x * q), c1 = min(a.nchunk, c0 + q);
-    // the next kernel may start its prologue once every block has passed this point, i.e. once
-    // the whole cooperative grid is resident
+    const int ch = blockIdx.x;
+    const int t = ch * kSortTok + tid;
+    const int word = tid >> 5;
+    const uint32_t bit = 1u << (tid & 31);
+    for (int i = tid; i < a.E * W; i += blockDim.x) s_mask[i] = 0u;
     pdl_wait();
+    // this chunk's token bitmasks per expert (idx was checked by the histogram kernel)
+    int mine[MOE_MAX_K];
+    __syncthreads();
+    if (t < a.T) {
+        token_experts(a, t, mine, false);
+        for (int j = 0; j < a.k; ++j)
+            if (mine[j] >= 0) atomicOr(&s_mask[mine[j] * W + word], bit);
+    } else {
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
+    }
 
-    // ---- phase 1: histograms of this block's chunks
-    for (int ch = c0; ch < c1; ++ch) {
-        for (int e = tid; e < a.E; e += blockDim.x) s_h[e] = 0;
-        __syncthreads();
-        const int t = ch * kSortTok + tid;
-        if (t < a.T) {
-            int mine[MOE_MAX_K];
-            for (int j = 0; j < a.k; ++j) {
-                const int e = a.idx[(size_t)t * a.k + j];
-                bool ok = (e >= 0 && e < a.E);
-                for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
-                mine[j] = ok ? e : -1;
-                if (ok) atomicAdd(&s_h[e], 1);
-                else raise_error(a.err, kErrBounds);
+    // expert totals and this chunk's prefix, from all chunk histograms: thread (g, e) sums
+    // column e over the chunks c = g mod groups (consecutive threads read consecutive experts
+    // of a chunk's row; many rows in flight per thread), then the group partials are added
+    const int groups = max(1, kSortTok / a.E);
+    {
+        int tot = 0, pre = 0;
+        if (tid < groups * a.E) {
+            const int e = tid % a.E, g = tid / a.E;
+#pragma unroll 16
+            for (int c = g; c < a.nchunk; c += groups) {
+                const int v = __ldcg(a.blk_hist + (size_t)c * a.E + e);
+                tot += v;
+                pre += c < ch ? v : 0;
             }
         }
-        __syncthreads();
-        for (int e = tid; e < a.E; e += blockDim.x) a.blk_hist[(size_t)ch * a.E + e] = s_h[e];
-        __syncthreads();
-    }
-    if (!grid_barrier(a.bar, (unsigned)G, a.err)) return;
-
-    // ---- phase 2: expert totals and this block's prefix, from all chunk histograms (warp w
-    // sums chunks w, w + NW, ...; the warp partials are then added in warp order)
-    for (int e = lane; e < a.E; e += 32) {
-        int tot = 0, pre = 0;
-#pragma unroll 4
-        for (int c = warp; c < a.nchunk; c += NW) {
-            const int v = __ldcg(a.blk_hist + (size_t)c * a.E + e);
-            tot += v;
-            pre += c < c0 ? v : 0;
-        }
-        s_part[0][warp][e] = tot;
-        s_part[1][warp][e] = pre;
+        s_part[0][tid] = tot;
+        s_part[1][tid] = pre;
     }
     __syncthreads();
     for (int e = tid; e < a.E; e += blockDim.x) {
         int tot = 0, pre = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) { tot += s_part[0][w][e]; pre += s_part[1][w][e]; }
+        for (int g = 0; g < groups; ++g) { tot += s_part[0][g * a.E + e]; pre += s_part[1][g * a.E + e]; }
         s_cnt[e] = tot;
         s_base[e] = pre;
     }
     __syncthreads();
 
-    // ---- phase 3: offsets (every block), then ranks and the bucket layout
+    // offsets (every block computes them), then this chunk's ranks and the bucket layout
     for (int e = tid; e < a.E; e += blockDim.x) {
         const int cnt = s_cnt[e];
         const int kept = min(cnt, a.C);
         s_kept[e] = kept;
-        s_scan[e] = (kept + a.align - 1) / a.align * a.align;
+        s_off[e] = (kept + a.align - 1) / a.align * a.align;
         s_aoff[e] = cnt;
     }
     __syncthreads();
-    const int rows_total = block_exclusive_scan(s_scan, a.E);
-    for (int e = tid; e < a.E; e += blockDim.x) s_off[e] = s_scan[e];
-    if (tid == 0) s_off[a.E] = rows_total;
+    int rows_total, assign_total;
+    block_exclusive_scan2(s_off, s_aoff, a.E, &rows_total, &assign_total);
+    if (tid == 0) { s_off[a.E] = rows_total; s_aoff[a.E] = assign_total; }
     __syncthreads();
-    for (int e = tid; e < a.E; e += blockDim.x) s_scan[e] = s_aoff[e];
-    __syncthreads();
-    const int assign_total = block_exclusive_scan(s_scan, a.E);
-    for (int e = tid; e < a.E; e += blockDim.x) s_aoff[e] = s_scan[e];
-    if (tid == 0) s_aoff[a.E] = assign_total;
-    __syncthreads();
-    if (blockIdx.x == 0) {
+    if (ch == 0) {
         for (int e = tid; e <= a.E; e += blockDim.x) {
             a.assign_off[e] = s_aoff[e];
             if (a.offsets) a.offsets[e] = s_off[e];
@@ -167,62 +184,31 @@ sort_kernel(SortArgs a) {
     }
     // padding rows of the buckets this block owns
     if (a.row_token) {
-        for (int e = blockIdx.x; e < a.E; e += G)
+        for (int e = ch; e < a.E; e += gridDim.x)
             for (int r = s_off[e] + s_kept[e] + tid; r < s_off[e + 1]; r += blockDim.x) a.row_token[r] = -1;
     }
-    for (int ch = c0; ch < c1; ++ch) {
-        for (int i = tid; i < a.E * W; i += blockDim.x) s_mask[i] = 0u;
-        __syncthreads();
-        const int t = ch * kSortTok + tid;
-        const int word = tid >> 5;
-        const uint32_t bit = 1u << (tid & 31);
-        int mine[MOE_MAX_K];
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
-        if (t < a.T) {
-            for (int j = 0; j < a.k; ++j) {
-                const int e = a.idx[(size_t)t * a.k + j];
-                bool ok = (e >= 0 && e < a.E);
-                for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
-                if (ok) {
-                    mine[j] = e;
-                    atomicOr(&s_mask[e * W + word], bit);
+    if (t < a.T) {
+        for (int j = 0; j < a.k; ++j) {
+            const int e = mine[j];
+            if (e < 0) {
+                if (a.slot_row) a.slot_row[(size_t)t * a.k + j] = -1;
+                continue;
+            }
+            const uint32_t* m = s_mask + e * W;
+            int local = __popc(m[word] & (bit - 1u));
+            for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
+            const int rank = s_base[e] + local;
+            a.assign_tok[s_aoff[e] + rank] = t * a.k + j;
+            if (a.slot_row) {
+                if (rank < a.C) {
+                    const int row = s_off[e] + rank;
+                    a.slot_row[(size_t)t * a.k + j] = row;
+                    a.row_token[row] = t;
+                } else {
+                    a.slot_row[(size_t)t * a.k + j] = -1;
                 }
             }
         }
-        __syncthreads();
-        if (t < a.T) {
-            for (int j = 0; j < a.k; ++j) {
-                const int e = mine[j];
-                if (e < 0) {
-                    if (a.slot_row) a.slot_row[(size_t)t * a.k + j] = -1;
-                    continue;
-                }
-                const uint32_t* m = s_mask + e * W;
-                int local = __popc(m[word] & (bit - 1u));
-                for (int w2 = 0; w2 < word; ++w2) local += __popc(m[w2]);
-                const int rank = s_base[e] + local;
-                a.assign_tok[s_aoff[e] + rank] = t * a.k + j;
-                if (a.slot_row) {
-                    if (rank < a.C) {
-                        const int row = s_off[e] + rank;
-                        a.slot_row[(size_t)t * a.k + j] = row;
-                        a.row_token[row] = t;
-                    } else {
-                        a.slot_row[(size_t)t * a.k + j] = -1;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        // the next chunk's base: this chunk's assignments counted in
-        for (int e = tid; e < a.E; e += blockDim.x) {
-            int c = 0;
-#pragma unroll
-            for (int w2 = 0; w2 < W; ++w2) c += __popc(s_mask[e * W + w2]);
-            s_base[e] += c;
-        }
-        __syncthreads();
     }
 }
 
@@ -322,22 +308,6 @@ void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s) {
     s->blk_hist = ws.take<int32_t>((size_t)nblk * c.E);
     s->assign_off = ws.take<int32_t>((size_t)c.E + 1);
     s->assign_tok = ws.take<int32_t>((size_t)c.T * c.k + 1);
-    s->bar = ws.take<unsigned>(1);
-}
-
-// Blocks of sort_kernel that fit on the device at once (the grid barriers need them all resident).
-static int sort_coresident_blocks() {
-    static int cached[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cached[dev]) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sort_kernel, kSortTok, 0) != cudaSuccess)
-            per_sm = 1;
-        cached[dev] = std::max(1, per_sm) * num_sms();
-    }
-    return cached[dev];
 }
 
 cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScratch& s,
@@ -349,23 +319,11 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
     a.blk_hist = s.blk_hist;
     a.assign_off = s.assign_off; a.assign_tok = s.assign_tok;
     a.kept = kept; a.offsets = offsets; a.row_token = row_token; a.slot_row = slot_row;
-    a.n_dropped = n_dropped; a.bar = s.bar; a.err = device_error_word();
-    cudaError_t e = launch_fill(s.bar, 1, 0u, st);
+    a.n_dropped = n_dropped; a.err = device_error_word();
+    cudaError_t e = launch_pdl(sort_hist_kernel, a.nchunk, kSortTok, 0, st, a);
+    count_launch();
     if (e != cudaSuccess) return e;
-    const int grid = std::max(1, std::min(a.nchunk, std::min(sort_coresident_blocks(), 2 * num_sms())));
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kSortTok);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = launch_ex(cfg, sort_kernel, a);
+    e = launch_pdl(sort_rank_kernel, a.nchunk, kSortTok, 0, st, a);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -69,7 +69,6 @@ struct SortScratch {
     int32_t* blk_hist;     // [nblk, E] per-chunk expert histograms
     int32_t* assign_off;   // [E+1] exclusive scan of counts
     int32_t* assign_tok;   // [T*k] assignment (t*k+j) in expert-major, token-minor order
-    unsigned* bar;         // grid-barrier counter of the cooperative sort
 };
 int sort_blocks(int T);
 void sort_scratch_take(Workspace& ws, const moe_config_t& c, SortScratch* s);
