@@ -524,6 +524,7 @@ def profile_call(args, moe, c, d_in, b, flush, stream, forward_only):
         "combine": lambda: moe.combine(c, b["Yp"], b["slot_row"], b["w"], b["y"], stream),
         "backward": lambda: moe.backward(c, d_in["dy"], d_in["x"], d_in["Wg"], d_in["W1"], d_in["W2"], b, stream),
     }
+    calls["step"] = lambda: (fwd(), calls["backward"]())
     for _ in range(args.warmup):
         flush.zero_()
         fwd()
@@ -800,8 +801,10 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional calls")
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per batch instead of the workload's (a smaller case of the same layer)")
-    ap.add_argument("--profile", choices=["route", "dispatch", "expert_ffn", "combine", "backward"], default=None,
-                    help="for a profiler: warm up, then run only this call --steps times (no JSON line)")
+    ap.add_argument("--profile", choices=["route", "dispatch", "expert_ffn", "combine", "backward", "step"],
+                    default=None,
+                    help="for a profiler: warm up, then run only this call (or the whole eager fwd+bwd "
+                         "step) --steps times, each after an L2 flush (no JSON line)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     cfg = synth.get(args.workload)
