@@ -291,15 +291,15 @@ MOE_API moe_status_t moe_coselect(const moe_config_t* cfg, const int32_t* idx, i
 MOE_API moe_status_t moe_get_error(moe_stream_t stream);
 
 /* Self-test of the device-side bounded waits (failure detection without a GPU fault). A
- * kernel waits on an object that nothing signals, through the wait helpers the layer's kernels
- * use: mode 0 an mbarrier phase (as in the tensor-core pipelines), mode 1 a grid barrier of two
- * blocks with an unreachable target (as in the cooperative sort). After budget_cycles
- * (1e3 .. 4e9 SM clock cycles) each wait gives up, records MOE_ERR_DEVICE_TIMEOUT in the
- * device error word and the kernel returns; the context stays usable.
- *   timed_out: device int32, set to the number of waits that ran out (1 in mode 0, 2 in mode 1)
- *   scratch  : device buffer of at least 4 bytes (the barrier counter), 4-byte aligned
- * Returns MOE_ERR_INVALID_ARG for a bad mode, budget or pointer; the timeout itself is read
- * with moe_get_error. */
+ * kernel waits on an object that nothing signals, through the wait helper the layer's kernels
+ * use: an mbarrier phase wait, as in the tensor-core pipelines (mode 0, the only mode). After
+ * budget_cycles (1e3 .. 4e9 SM clock cycles) the wait gives up, records
+ * MOE_ERR_DEVICE_TIMEOUT in the device error word and the kernel returns; the context stays
+ * usable.
+ *   timed_out: device int32, set to the number of waits that ran out (1)
+ *   scratch  : unused (may be null)
+ * Returns MOE_ERR_INVALID_ARG for a mode other than 0, a bad budget or a null timed_out; the
+ * timeout itself is read with moe_get_error. */
 MOE_API moe_status_t moe_selftest_wait_timeout(int32_t mode, int64_t budget_cycles, int32_t* timed_out,
                                                void* scratch, moe_stream_t stream);
 

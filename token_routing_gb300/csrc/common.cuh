@@ -23,37 +23,6 @@ __device__ __forceinline__ void raise_error(int* err, int code) {
 // kErrTimeout and returns false so the kernel can unwind instead of hanging.
 constexpr long long kSpinBudgetCycles = 4000000000LL;
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid barrier of a launch whose blocks are all resident (a cooperative launch): each block
-// adds 1 to *bar and waits until it reaches `target`. Returns false (and records
-// kErrTimeout) if the wait ran out of `budget` cycles.
-__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned target, int* err,
-                                             long long budget = kSpinBudgetCycles) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        s_ok = 1;
-        __threadfence();
-        atomicAdd(bar, 1u);
-        const long long t0 = clock64();
-        while (ld_acquire_u32(bar) < target) {
-            if (clock64() - t0 > budget) {
-                raise_error(err, kErrTimeout);
-                s_ok = 0;
-                break;
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
 // ---------------------------------------------------------------- dependent launches
 // Kernels are launched with programmatic stream serialization: a kernel may start (and run
 // its prologue) while the previous kernel of its stream finishes. Every kernel therefore

@@ -1,33 +1,25 @@
 // Self-test of the device-side bounded waits: a kernel waits on an object that nothing
-// signals, with a short cycle budget, through the same wait helpers the layer's kernels use
-// (an mbarrier wait, as in the tensor-core pipelines; a grid barrier, as in the cooperative
-// sort). The wait runs out, records MOE_ERR_DEVICE_TIMEOUT in the device error word and the
-// kernel returns normally, so the context stays usable. No fault, trap or endless loop is
-// involved.
+// signals, with a short cycle budget, through the wait helper the layer's kernels use (an
+// mbarrier phase wait, as in the tensor-core pipelines). The wait runs out, records
+// MOE_ERR_DEVICE_TIMEOUT in the device error word and the kernel returns normally, so the
+// context stays usable. No fault, trap or endless loop is involved.
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
-// mode 0: one thread waits for phase 0 of a fresh mbarrier that expects one arrival (none
-// comes). mode 1: two blocks meet at a grid barrier whose target (3) two blocks cannot reach.
-__global__ void __launch_bounds__(32) wait_timeout_kernel(int mode, long long budget, unsigned* bar, int* err,
-                                                          int* done) {
-    if (mode == 0) {
-        __shared__ uint64_t mb;
-        if (threadIdx.x == 0) {
-            tc::mbar_init(&mb, 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const bool ok = tc::mbar_wait(&mb, 0, err, budget);
-            atomicAdd(done, ok ? 0 : 1);
-        }
-    } else {
-        const bool ok = grid_barrier(bar, 3u, err, budget);
-        if (threadIdx.x == 0) atomicAdd(done, ok ? 0 : 1);
+// One thread waits for phase 0 of a fresh mbarrier that expects one arrival (none comes).
+__global__ void __launch_bounds__(32) wait_timeout_kernel(long long budget, int* err, int* done) {
+    __shared__ uint64_t mb;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&mb, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = tc::mbar_wait(&mb, 0, err, budget);
+        atomicAdd(done, ok ? 0 : 1);
     }
 }
 
@@ -40,16 +32,12 @@ extern "C" {
 
 moe_status_t moe_selftest_wait_timeout(int32_t mode, int64_t budget_cycles, int32_t* timed_out, void* scratch,
                                        moe_stream_t stream) {
-    if ((mode != 0 && mode != 1) || budget_cycles < 1000 || budget_cycles > kSpinBudgetCycles || !timed_out ||
-        !scratch)
+    (void)scratch;
+    if (mode != 0 || budget_cycles < 1000 || budget_cycles > kSpinBudgetCycles || !timed_out)
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    unsigned* bar = static_cast<unsigned*>(scratch);
-    cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(timed_out, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    wait_timeout_kernel<<<mode == 0 ? 1 : 2, 32, 0, s>>>(mode, (long long)budget_cycles, bar,
-                                                       device_error_word(), timed_out);
+    if (cudaMemsetAsync(timed_out, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, s>>>((long long)budget_cycles, device_error_word(), timed_out);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -154,8 +154,8 @@ def forward_backward(cfg, p, x, dy, b, stream=None):
 
 
 def selftest_wait_timeout(mode, budget_cycles, timed_out, scratch, stream=None):
-    """moe_selftest_wait_timeout: a bounded device wait that nothing satisfies (mode 0: an
-    mbarrier phase, mode 1: a grid barrier); read the resulting timeout with get_error()."""
+    """moe_selftest_wait_timeout: a bounded device wait that nothing satisfies (mode 0, the
+    only mode: an mbarrier phase); read the resulting timeout with get_error()."""
     L.check("moe_selftest_wait_timeout", L.load().moe_selftest_wait_timeout(
         int(mode), int(budget_cycles), _p(timed_out), _p(scratch), _s(stream)))
 
