@@ -118,6 +118,14 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
+            // operand descriptors at stage 0, k = 0; a stage and a K step of UMMA_K advance the
+            // start-address field (16-byte units) by constants (K-major: 32 bytes inside the
+            // swizzle atom; MN-major: 16 rows)
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t a_desc0 = A_MN ? make_desc(s0, BK * 128, 1024) : make_desc(s0, 16, 1024);
+            const uint64_t b_desc0 = B_MN ? make_desc(s0 + A_BYTES, BK * 128, 1024) : make_desc(s0 + A_BYTES, 16, 1024);
+            constexpr uint32_t A_KSTEP = (A_MN ? UMMA_K * 128 : UMMA_K * 2) >> 4;
+            constexpr uint32_t B_KSTEP = (B_MN ? UMMA_K * 128 : UMMA_K * 2) >> 4;
             uint32_t it = 0, tl = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -134,17 +142,11 @@ tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(full + s, ph, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint64_t soff = (uint64_t)(s * (STAGE_BYTES >> 4));
+                    const uint64_t ad = a_desc0 + soff, bd = b_desc0 + soff;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // K-major: step 32 bytes inside the swizzle atom; MN-major: step 16 rows
-                        const uint64_t ad = A_MN ? make_desc(sa + kk * UMMA_K * 128, BK * 128, 1024)
-                                                 : make_desc(sa + kk * UMMA_K * 2, 16, 1024);
-                        const uint64_t bd = B_MN ? make_desc(sb + kk * UMMA_K * 128, BK * 128, 1024)
-                                                 : make_desc(sb + kk * UMMA_K * 2, 16, 1024);
-                        tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        tc_mma(d_tmem, ad + kk * A_KSTEP, bd + kk * B_KSTEP, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(empty + s);  // frees the stage once these MMAs have read it
                 }
                 if (!ok) break;

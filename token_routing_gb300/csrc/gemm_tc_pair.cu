@@ -185,15 +185,13 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs): own A rows, own half of B
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t s = 0, ph = 0;   // ring position: the stage, and the phase of its barriers
             bool ok = true;
             for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
                 const PairTile t = decode_pair_tile<WGRAD>(p, s_off, s_q, tile);
                 const int mr = t.m0 + (int)rank * P_HALF;   // this CTA's rows of the tile
                 const int nh = t.n0 + (int)rank * P_HALF;   // this CTA's half of B's columns
-                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-                    const int s = it % P_STAGES;
-                    const uint32_t ph = (it / P_STAGES) & 1;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1, p.err)) { ok = false; break; }
                     const uint32_t sa = smem_u32(smem + s * P_STAGE_BYTES);
                     const uint32_t sb = sa + P_A_BYTES;
@@ -218,6 +216,7 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                         for (int j = 0; j < P_HALF / 64; ++j)
                             tma_load_2d_pair(sb + j * (BK * 128), &tmB, nh + 64 * j, t.e * p.K + k0, fb);
                     }
+                    if (++s == P_STAGES) { s = 0; ph ^= 1; }
                 }
             }
             if (!ok) *s_fail = 1;
@@ -226,7 +225,17 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
         // ---------------- MMA issuer: one thread of the leader CTA drives the pair
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16(P_BM, BN, A_MN, B_MN);
-            uint32_t it = 0, tl = 0;
+            // The operands' descriptors at stage 0, k = 0. The start-address field counts 16-byte
+            // units, so a stage and a K step of UMMA_K advance it by constants. This keeps the
+            // issuing thread's work per k-block small: its instruction latency is on the
+            // tensor pipe's critical path.
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t a_desc0 = A_MN ? make_desc(s0, BK * 128, 1024) : make_desc(s0, 16, 1024);
+            const uint64_t b_desc0 = B_MN ? make_desc(s0 + P_A_BYTES, BK * 128, 1024) : make_desc(s0 + P_A_BYTES, 16, 1024);
+            constexpr uint32_t A_KSTEP = (A_MN ? UMMA_K * 128 : UMMA_K * 2) >> 4;
+            constexpr uint32_t B_KSTEP = (B_MN ? UMMA_K * 128 : UMMA_K * 2) >> 4;
+            constexpr uint32_t STAGE_STEP = P_STAGE_BYTES >> 4;
+            uint32_t s = 0, ph = 0, soff = 0, tl = 0;   // ring stage, its phase, its descriptor offset
             bool ok = true;
             for (int tile = cluster_id; tile < num_tiles && ok; tile += nclusters) {
                 const PairTile t = decode_pair_tile<WGRAD>(p, s_off, s_q, tile);
@@ -237,22 +246,15 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
                 if (!mbar_wait(tempty + buf, aph ^ 1, p.err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-                    const int s = it % P_STAGES;
-                    const uint32_t ph = (it / P_STAGES) & 1;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(full + s, ph, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * P_STAGE_BYTES);
-                    const uint32_t sb = sa + P_A_BYTES;
+                    const uint64_t ad = a_desc0 + soff, bd = b_desc0 + soff;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = A_MN ? make_desc(sa + kk * UMMA_K * 128, BK * 128, 1024)
-                                                 : make_desc(sa + kk * UMMA_K * 2, 16, 1024);
-                        const uint64_t bd = B_MN ? make_desc(sb + kk * UMMA_K * 128, BK * 128, 1024)
-                                                 : make_desc(sb + kk * UMMA_K * 2, 16, 1024);
-                        mma_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        mma_pair(d_tmem, ad + kk * A_KSTEP, bd + kk * B_KSTEP, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     commit_pair_both(empty + s);   // frees the stage in both CTAs
+                    if (++s == P_STAGES) { s = 0; ph ^= 1; soff = 0; } else { soff += STAGE_STEP; }
                 }
                 if (!ok) break;
                 commit_pair_both(tfull + buf);     // both CTAs' accumulator rows are ready
