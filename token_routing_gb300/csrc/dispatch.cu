@@ -72,11 +72,16 @@ __device__ void block_exclusive_scan2(int* a, int* b, int n, int* tot_a, int* to
 // The experts of token t's k slots, in slot order; -1 for an id out of range or repeated
 // (reported through the error word when `report`).
 __device__ __forceinline__ void token_experts(const SortArgs& a, int t, int (&mine)[MOE_MAX_K], bool report) {
+    int id[MOE_MAX_K];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) mine[j] = -1;
-    for (int j = 0; j < a.k; ++j) {
-        const int e = a.idx[(size_t)t * a.k + j];
+    for (int j = 0; j < MOE_MAX_K; ++j) id[j] = j < a.k ? a.idx[(size_t)t * a.k + j] : -1;   // all loads in flight
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) {
+        mine[j] = -1;
+        if (j >= a.k) continue;
+        const int e = id[j];
         bool ok = (e >= 0 && e < a.E);
+#pragma unroll
         for (int i = 0; i < j; ++i) ok = ok && (mine[i] != e);
         if (ok) mine[j] = e;
         else if (report) raise_error(a.err, kErrBounds);
@@ -138,11 +143,19 @@ sort_rank_kernel(SortArgs a) {
         int tot = 0, pre = 0;
         if (tid < groups * a.E) {
             const int e = tid % a.E, g = tid / a.E;
-#pragma unroll 16
-            for (int c = g; c < a.nchunk; c += groups) {
-                const int v = __ldcg(a.blk_hist + (size_t)c * a.E + e);
-                tot += v;
-                pre += c < ch ? v : 0;
+            constexpr int R = 16;   // rows in flight per thread
+            for (int c0 = g; c0 < a.nchunk; c0 += R * groups) {
+                int v[R];
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const int c = c0 + i * groups;
+                    v[i] = c < a.nchunk ? __ldcg(a.blk_hist + (size_t)c * a.E + e) : 0;
+                }
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    tot += v[i];
+                    pre += c0 + i * groups < ch ? v[i] : 0;
+                }
             }
         }
         s_part[0][tid] = tot;
