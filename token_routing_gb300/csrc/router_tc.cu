@@ -57,6 +57,60 @@ __device__ __forceinline__ void load_noise32(const float* __restrict__ noise, in
     for (int i = 0; i < 32; ++i) nz[i] = (live && c + i < E) ? __ldg(noise + (size_t)(c + i) * T + tok) : 0.f;
 }
 
+// N consecutive logits of a token (columns c .. c + N - 1 of its TMEM row: bias, optional
+// noise and logits output) inserted into its list sorted by (logit desc, id asc). Experts
+// arrive in ascending id, so an equal logit never displaces an earlier one.
+template <int K, int N, bool NOISE>
+__device__ __forceinline__ void select_cols(const RouteTcParams& p, const uint32_t (&r)[N], const float (&nz)[N],
+                                            int c, int tok, const float* s_bias, float (&tv)[K], int (&te)[K]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        int e = c + i;
+        if (e < p.E) {
+            float v = __uint_as_float(r[i]) + s_bias[e];
+            if (NOISE && tok < p.T) v = fmaf(p.noise_std, nz[i], v);
+            if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (te[j] < 0 || v > tv[j]) {
+                    const float ov = tv[j];
+                    const int oe = te[j];
+                    tv[j] = v; te[j] = e;
+                    v = ov; e = oe;
+                }
+            }
+        }
+    }
+}
+
+// One 32-expert chunk of a token's logits into its top-k list. Without noise, one 32-column
+// TMEM load; with noise, two halves of 16 columns and 16 draws each, so that the draws do
+// not add to the live registers of the 32-column path (a 576-thread block allows 96 per
+// thread; more spilled the lists to local memory in the selection).
+template <int K>
+__device__ __forceinline__ void select_chunk(const RouteTcParams& p, uint32_t taddr, int c, int tok,
+                                             const float* s_bias, float (&tv)[K], int (&te)[K]) {
+    if (p.noise) {
+#pragma unroll 1
+        for (int h = 0; h < 32; h += 16) {
+            float nz[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                nz[i] = (tok < p.T && c + h + i < p.E) ? __ldg(p.noise + (size_t)(c + h + i) * p.T + tok) : 0.f;
+            uint32_t r[16];
+            tmem_ld16(taddr + c + h, r);
+            tmem_ld_wait();
+            select_cols<K, 16, true>(p, r, nz, c + h, tok, s_bias, tv, te);
+        }
+    } else {
+        uint32_t r[32];
+        const float nz[32] = {};
+        tmem_ld32(taddr + c, r);
+        tmem_ld_wait();
+        select_cols<K, 32, false>(p, r, nz, c, tok, s_bias, tv, te);
+    }
+}
+
 // Softmax over a token's k selected logits (tv[0] the largest), its indices and weights, and
 // its counts in the CTA's histogram.
 template <int K>
@@ -245,31 +299,7 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
             if (ok) tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
             for (int c = 32 * grp; ok && c < p.E_pad; c += 32 * G) {
-                float nz[32];
-                if (p.noise) load_noise32(p.noise, p.T, p.E, c, tok, tok < p.T, nz);
-                uint32_t r[32];
-                tmem_ld32(taddr + c, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    int e = c + i;
-                    if (e < p.E) {
-                        float v = __uint_as_float(r[i]) + s_bias[e];
-                        if (p.noise && tok < p.T) v = fmaf(p.noise_std, nz[i], v);
-                        if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
-                        // insert into the list sorted by (logit desc, id asc); experts arrive in
-                        // ascending id, so an equal logit never displaces an earlier one
-#pragma unroll
-                        for (int j = 0; j < K; ++j) {
-                            if (te[j] < 0 || v > tv[j]) {
-                                const float ov = tv[j];
-                                const int oe = te[j];
-                                tv[j] = v; te[j] = e;
-                                v = ov; e = oe;
-                            }
-                        }
-                    }
-                }
+                select_chunk<K>(p, taddr, c, tok, s_bias, tv, te);
             }
             if constexpr (G == 1) {
                 if (tok < p.T) route_finish<K>(p, tok, tv, te, s_cnt);
