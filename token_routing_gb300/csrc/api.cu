@@ -110,6 +110,7 @@ struct BackwardScratch {
     float* colsum_f;    // column-sum partials of dA (db1)
     SoftScratch soft;   // soft balance loss
     float* noise;       // routing noise [E, T] (expert-major), when cfg.noise_std > 0
+    int32_t* used;      // [E] rows of each bucket holding an assignment (weight-gradient K)
 };
 
 size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
@@ -127,6 +128,7 @@ size_t carve_backward(const moe_config_t& c, void* base, BackwardScratch* b) {
     b->colsum_d = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d + 1);
     b->colsum_f = ws.take<float>((R / MOE_ROW_ALIGN) * kColsumParts * (size_t)c.d_ff + 1);
     b->noise = ws.take<float>(c.noise_std > 0.f ? (size_t)c.T * c.E + 1 : 1);
+    b->used = ws.take<int32_t>((size_t)c.E + 1);
     soft_scratch_take(ws, c, &b->soft);
     return align_up(ws.used, 256);
 }
@@ -415,7 +417,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
         MOE_TRY(cudaEventRecord(ev.d, side));
         MOE_TRY(launch_dense_dwg(c, dz_dense, x, dWg, dbg_out, false, b.soft, side));
     }
+    // the weight gradients' K loops stop at each bucket's last row with an assignment
+    if (use_tc(c)) MOE_TRY(launch_bucket_used(c, offsets, row_token, b.used, side));
     WgradArgs w2{b.dYp, H, dW2, offsets, c.E, c.d, c.d_ff};
+    if (use_tc(c)) w2.rows_used = b.used;
     MOE_TRY(wgrad(c, w2, side));
     MOE_TRY(launch_colsum(c, b.dYp, c.d, offsets, b.colsum_d, side));
     MOE_TRY(launch_bias_reduce(c, b.colsum_d, c.d, offsets, db2, side));
@@ -434,6 +439,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* dy, const void* x
     MOE_TRY(cudaEventRecord(ev.b, s));
     MOE_TRY(cudaStreamWaitEvent(side, ev.b, 0));
     WgradArgs w1{b.dA, Xp, dW1, offsets, c.E, c.d_ff, c.d};
+    if (use_tc(c)) w1.rows_used = b.used;
     MOE_TRY(wgrad(c, w1, side));
     MOE_TRY(launch_bias_reduce(c, b.colsum_f, c.d_ff, offsets, db1, side));
     if (serial) {

@@ -312,7 +312,36 @@ gather_kernel(const T* __restrict__ x, const int32_t* __restrict__ offsets, int 
     }
 }
 
+// Rows of each bucket that hold an assignment. They come first in the bucket, and the
+// padding after them (row_token -1) is shorter than the row alignment, so the first padding
+// row is found by a binary search over the bucket's last align - 1 rows.
+__global__ void __launch_bounds__(256)
+bucket_used_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_token, int E, int align,
+                   int32_t* __restrict__ used) {
+    pdl_wait();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const int lo = offsets[e], hi = offsets[e + 1];
+    int a = max(lo, hi - (align - 1)), b = hi;   // the first padding row is in [a, b] (b: none)
+    while (a < b) {
+        const int m = (a + b) >> 1;
+        if (row_token[m] < 0) b = m;
+        else a = m + 1;
+    }
+    used[e] = a - lo;
+}
+
 }  // namespace
+
+cudaError_t launch_bucket_used(const moe_config_t& c, const int32_t* offsets, const int32_t* row_token,
+                               int32_t* used, cudaStream_t st) {
+    if (c.E <= 0) return cudaSuccess;
+    cudaError_t e = launch_pdl(bucket_used_kernel, ceil_div(c.E, 256), 256, 0, st, offsets, row_token, c.E,
+                               c.row_align, used);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 int sort_blocks(int T) { return T > 0 ? ceil_div(T, kSortTok) : 1; }
 

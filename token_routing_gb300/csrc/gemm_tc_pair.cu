@@ -105,7 +105,9 @@ __device__ __forceinline__ PairTile decode_pair_tile(const TcParams& p, const in
         t.m0 = (rest % p.m_tiles) * P_BM;
         t.e = rest / p.m_tiles;
         t.row0 = s_off[t.e];
-        t.kblocks = (s_off[t.e + 1] - s_off[t.e]) / BK;
+        // the K loop stops at the last k-block that holds a row of the bucket with an
+        // assignment: the rows after it are zero padding and add nothing
+        t.kblocks = p.rows_used ? (int)s_q[t.e] : (s_off[t.e + 1] - s_off[t.e]) / BK;
         t.end = 0;
     } else {
         t.e = bucket_of_pair(s_off, s_q, p.E, rest);
@@ -173,6 +175,10 @@ tc_gemm_pair_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
     if (!WGRAD) {
         __syncthreads();
         if (warp == 0) bucket_odd_prefix(s_off, p.E, s_q, lane);
+    } else if (p.rows_used) {
+        // (the weight gradients do not use the odd-bucket prefix: its array holds each
+        // bucket's k-block count instead; the host passes rows_used only below 2^16 k-blocks)
+        for (int i = threadIdx.x; i < p.E; i += blockDim.x) s_q[i] = (uint16_t)((p.rows_used[i] + BK - 1) / BK);
     }
     tc_fence_before();
     __syncthreads();
@@ -494,6 +500,7 @@ cudaError_t launch_wgrad_tc_pair(const moe_config_t& c, const WgradArgs& a, cuda
     p.m_tiles = ceil_div(a.M, P_BM);
     p.out0 = a.f32 ? nullptr : static_cast<__nv_bfloat16*>(a.C);
     p.outf = a.f32 ? static_cast<float*>(a.C) : nullptr;
+    p.rows_used = (!a.f32 && a.rows_used && (long long)c.rows_capacity / BK < 65536) ? a.rows_used : nullptr;
     p.err = device_error_word();
     CUtensorMap ta, tb, to0;
     const uint64_t rows_p = (uint64_t)std::max(a.rows_p > 0 ? a.rows_p : c.rows_capacity, 1);

@@ -49,6 +49,7 @@ struct WgradArgs {
     int E, M, N;
     int rows_p = 0, rows_q = 0;   // rows of P and Q (0: cfg.rows_capacity)
     bool f32 = false;             // C is fp32 [E, M, N] (kGemmWgradF32)
+    const int32_t* rows_used = nullptr;   // [E] rows of each bucket with an assignment (or null)
 };
 
 // router.cu
@@ -78,6 +79,9 @@ cudaError_t launch_sort(const moe_config_t& c, const int32_t* idx, const SortScr
                         int32_t* n_dropped, cudaStream_t st);
 cudaError_t launch_dense_layout(const moe_config_t& c, const int32_t* idx, int32_t* kept, int32_t* offsets,
                                 int32_t* row_token, int32_t* slot_row, int32_t* n_dropped, cudaStream_t st);
+// used[e] = rows of bucket e that hold an assignment (row_token >= 0), from the bucket layout.
+cudaError_t launch_bucket_used(const moe_config_t& c, const int32_t* offsets, const int32_t* row_token,
+                               int32_t* used, cudaStream_t st);
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* offsets,
                           const int32_t* row_token, const int32_t* slot_row, void* Xp, cudaStream_t st);
 

@@ -39,6 +39,7 @@ struct TcParams {
     __nv_bfloat16* out1;
     float* outf;                 // kGemmWgradF32: fp32 [E, M, N]
     float* colsum;               // dH: per-(tile, lane quarter) column sums of dA, or null
+    const int32_t* rows_used;    // wgrad (bf16): rows of bucket e that hold assignments, or null
     int* err;
 };
 
