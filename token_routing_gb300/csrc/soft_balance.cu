@@ -641,33 +641,50 @@ __host__ __device__ inline int e8_of(int E) { return (E + 7) / 8 * 8; }
 __host__ __device__ inline int k2_of(int E) { return (2 * e8_of(E) + 63) / 64 * 64; }
 
 // dzs[t, c] for t < T_pad, c < K2: hi of dz[t, c] (c < E), lo of dz[t, c - E8]
-// (E8 <= c < E8 + E), 0 elsewhere and for t >= T; one thread per column pair (bf16x2 store),
-// grid-stride. Block 0 also writes the bucket offsets. (Reading each dz value once and
-// storing its two halves separately measured slower: 36 vs 31 us at 32768 x 256.)
-__device__ __forceinline__ float split_val(const float* __restrict__ dz, int Tn, int E, int e8, int t, int c) {
-    if (t >= Tn) return 0.f;
-    if (c < E) return __bfloat162float(__float2bfloat16_rn(dz[(size_t)t * E + c]));
-    if (c >= e8 && c < e8 + E) {
-        const float z = dz[(size_t)t * E + c - e8];
-        return z - __bfloat162float(__float2bfloat16_rn(z));
+// (E8 <= c < E8 + E), 0 elsewhere and for t >= T. One thread per 8-column group of a row (the
+// groups never straddle a region boundary, since E8 is a multiple of 8; one 16-byte store),
+// grid-stride, with 32-bit index arithmetic when the element count allows. Block 0 also
+// writes the bucket offsets. (A 64-bit division per column pair had made the kernel 31 us at
+// 32768 x 256.)
+__device__ __forceinline__ void split_group(const float* __restrict__ dz, int Tn, int E, int e8, int k2, int t,
+                                            int c, __nv_bfloat16* __restrict__ dzs) {
+    float v[8];
+    const bool lo = c >= e8;
+    const int src = lo ? c - e8 : c;   // first dz column of the group
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const bool live = t < Tn && src + j < E && (lo ? c < e8 + E : true);
+        const float z = live ? dz[(size_t)t * E + src + j] : 0.f;
+        const float hi = __bfloat162float(__float2bfloat16_rn(z));
+        v[j] = lo ? z - hi : hi;
     }
-    return 0.f;
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    *reinterpret_cast<uint4*>(dzs + (size_t)t * k2 + c) = u;
 }
 
 __global__ void __launch_bounds__(kSplitThreads)
 soft_split_kernel(const float* __restrict__ dz, int Tn, int Tpad, int E, __nv_bfloat16* __restrict__ dzs,
                   int32_t* __restrict__ offs, int splits, int bucket) {
     pdl_wait();
-    const int e8 = e8_of(E), k2 = k2_of(E), half = k2 / 2;
+    const int e8 = e8_of(E), k2 = k2_of(E), groups = k2 / 8;
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= splits; i += blockDim.x) offs[i] = min(i * bucket, Tpad);
         if (threadIdx.x == 0) { offs[splits + 1] = 0; offs[splits + 2] = Tpad; }
     }
-    const long long n = (long long)Tpad * half;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(i / half), c = (int)(i % half) * 2;
-        const __nv_bfloat162 v = __floats2bfloat162_rn(split_val(dz, Tn, E, e8, t, c), split_val(dz, Tn, E, e8, t, c + 1));
-        *reinterpret_cast<__nv_bfloat162*>(dzs + (size_t)t * k2 + c) = v;
+    const long long n = (long long)Tpad * groups;
+    if (n <= 0x7fffffffLL - (long long)gridDim.x * blockDim.x) {
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < (int)n; i += gridDim.x * blockDim.x) {
+            const int t = i / groups;
+            split_group(dz, Tn, E, e8, k2, t, (i - t * groups) * 8, dzs);
+        }
+    } else {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+            const int t = (int)(i / groups);
+            split_group(dz, Tn, E, e8, k2, t, (int)(i - (long long)t * groups) * 8, dzs);
+        }
     }
 }
 
@@ -811,7 +828,7 @@ void soft_scratch_take(Workspace& ws, const moe_config_t& c, SoftScratch* s) {
 static cudaError_t launch_soft_split(const moe_config_t& c, const float* dz, bool want_sums, const SoftScratch& s,
                                      cudaStream_t st) {
     const SoftTc g = soft_tc_geom(c);
-    const long long n = (long long)g.tpad * (g.k2 / 2);
+    const long long n = (long long)g.tpad * (g.k2 / 8);
     const int grid = (int)std::max(1LL, std::min((n + kSplitThreads - 1) / kSplitThreads, (long long)num_sms() * 8));
     cudaError_t e = launch_pdl(soft_split_kernel, dim3(grid), dim3(kSplitThreads), 0, st, dz, c.T, g.tpad, c.E,
                                (__nv_bfloat16*)s.dzs, s.offs, g.splits, g.bucket);
