@@ -239,16 +239,33 @@ dense_layout_kernel(const int32_t* __restrict__ idx, int T, int E, int C, int al
     const long long n_slot = (long long)T * E;
     const long long n_rows = B * E;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_slot + n_rows; i += stride) {
-        if (i < n_slot) {
-            const int t = (int)(i / E), j = (int)(i % E);
-            const bool ok = idx[i] == j;
-            if (!ok) raise_error(err, kErrBounds);
-            slot_row[i] = (ok && t < kp) ? (int32_t)(j * B + t) : -1;
-        } else {
-            const long long r = i - n_slot;
-            const int rr = (int)(r % B);
-            row_token[r] = rr < kp ? rr : -1;
+    if (n_slot + n_rows + stride <= 0x7fffffffLL) {
+        // 32-bit index arithmetic (a 64-bit division per item is a long software sequence)
+        const int ns = (int)n_slot, nt = (int)(n_slot + n_rows), b = (int)B;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nt; i += (int)stride) {
+            if (i < ns) {
+                const int t = i / E, j = i - t * E;
+                const bool ok = idx[i] == j;
+                if (!ok) raise_error(err, kErrBounds);
+                slot_row[i] = (ok && t < kp) ? j * b + t : -1;
+            } else {
+                const int r = i - ns;
+                const int rr = r % b;
+                row_token[r] = rr < kp ? rr : -1;
+            }
+        }
+    } else {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_slot + n_rows; i += stride) {
+            if (i < n_slot) {
+                const int t = (int)(i / E), j = (int)(i % E);
+                const bool ok = idx[i] == j;
+                if (!ok) raise_error(err, kErrBounds);
+                slot_row[i] = (ok && t < kp) ? (int32_t)(j * B + t) : -1;
+            } else {
+                const long long r = i - n_slot;
+                const int rr = (int)(r % B);
+                row_token[r] = rr < kp ? rr : -1;
+            }
         }
     }
     if (blockIdx.x == 0) {

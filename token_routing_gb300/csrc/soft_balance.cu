@@ -707,10 +707,20 @@ soft_wge_kernel(const __nv_bfloat16* __restrict__ Wg, int E, int d, __nv_bfloat1
     pdl_wait();
     const int e8 = e8_of(E), k2 = k2_of(E);
     const long long n = (long long)k2 * d;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(i / d), c = (int)(i % d);
-        const int src = r < E ? r : (r >= e8 && r < e8 + E ? r - e8 : -1);
-        wge[i] = src >= 0 ? Wg[(size_t)src * d + c] : __float2bfloat16_rn(0.f);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    if (n + stride <= 0x7fffffffLL) {
+        // 32-bit index arithmetic (a 64-bit division per item is a long software sequence)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < (int)n; i += (int)stride) {
+            const int r = i / d, c = i - r * d;
+            const int src = r < E ? r : (r >= e8 && r < e8 + E ? r - e8 : -1);
+            wge[i] = src >= 0 ? Wg[(size_t)src * d + c] : __float2bfloat16_rn(0.f);
+        }
+    } else {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+            const int r = (int)(i / d), c = (int)(i % d);
+            const int src = r < E ? r : (r >= e8 && r < e8 + E ? r - e8 : -1);
+            wge[i] = src >= 0 ? Wg[(size_t)src * d + c] : __float2bfloat16_rn(0.f);
+        }
     }
 }
 
