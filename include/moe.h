@@ -118,8 +118,9 @@ typedef struct {
     int32_t rows_capacity;     /* rows of every permuted buffer (Xp, A, H, Yp) */
     int32_t row_align;         /* bucket alignment: MOE_ROW_ALIGN (128 rows). When the average
                                   bucket can reach 1024 rows (min(T*k, E*C)/E >= 1024) the
-                                  expert GEMMs run each bucket's 256-row tiles on CTA pairs and
-                                  its odd 128-row tile at the end on one CTA */
+                                  expert GEMMs run 256-row tiles on CTA pairs (the last tile of
+                                  a bucket with an odd number of 128-row tiles computes a second
+                                  half it does not store); otherwise 128-row tiles on one CTA */
 } moe_config_t;
 
 /* Validates the caller's fields and fills the derived ones. Must be called before any
