@@ -106,6 +106,10 @@ SMALL_CASES = {
     # average bucket >= 1024 rows: 256-row buckets and GEMM tiles on CTA pairs
     "small-pair-tiles": LayerConfig(
         name="small-pair-tiles", T=2500, d=256, E=4, k=2, d_ff=384, capacity_factor=1.0),
+    # pair tiles with buckets of an odd and an even number of 128-row tiles (the odd ones end in
+    # a 128-row tile), and output widths past one 256-column tile with ragged last tiles
+    "small-pair-odd": LayerConfig(
+        name="small-pair-odd", T=2300, d=320, E=4, k=2, d_ff=448, capacity_factor=None),
     "small-max-e256-k8": LayerConfig(
         name="small-max-e256-k8", T=513, d=128, E=256, k=8, d_ff=128, capacity_factor=None,
         temperature=0.5),

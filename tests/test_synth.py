@@ -47,3 +47,16 @@ def test_clusters_and_zipf_recipes():
 def test_fp32_workload_dtype():
     a = synth.make_inputs(synth.get("tiny-fp32-fwd"))
     assert a["x"].dtype == torch.float32 and a["dy"] is None
+
+
+def test_pair_odd_case_mixes_odd_and_even_buckets():
+    """The pair-tile parity case keeps buckets of both parities of 128-row tiles (an odd one ends
+    in a 128-row pair tile) and an average bucket of at least 1024 rows (the pair path)."""
+    from oracle import moe_oracle as O
+    cfg = synth.get("small-pair-odd")
+    a = synth.make_inputs(cfg)
+    r = O.route(a["x"].double().numpy(), a["Wg"].double().numpy(), None, cfg.k)
+    tiles = [-(-int(n) // 128) for n in r["counts"]]
+    assert {t % 2 for t in tiles} == {0, 1}
+    assert cfg.T * cfg.k >= 1024 * cfg.E
+    assert cfg.d > 256 and cfg.d_ff > 256 and cfg.d % 256 and cfg.d_ff % 256
