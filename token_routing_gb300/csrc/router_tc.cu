@@ -11,11 +11,13 @@
 // One CTA per 128-token tile: warp 0 streams x and Wg tiles with TMA, warp 1 issues the
 // MMAs (N = E rounded up to 32), and G groups of four epilogue warps (one per TMEM lane
 // quarter) read the logits from TMEM. With k = E one group takes the softmax over all E per
-// token. For top-k, group g keeps a sorted top-k list per token over its share of the
-// 32-expert chunks (chunks g, g + G, ...), and group 0 merges the G lists through shared
-// memory: G = min(4, chunks) groups put four times the warps on the selection's dependent
-// compare-and-swap chains where there are many experts. The kernel is bound by reading x from
-// HBM.
+// token. For top-k, group g takes its share of the 32-expert chunks (chunks g, g + G, ...;
+// G = min(4, chunks)), and the groups' results meet through shared memory:
+//   * k = 8: value-only sorting networks give each token's 8 largest logits; the experts at or
+//     above the 8th go to their slots by rank, and a token with tied logits there takes the
+//     exact (logit, id) order over all its experts;
+//   * other k: each group keeps a sorted top-k list per token, and group 0 merges the G lists.
+// In each CTA the selection starts once the whole x tile has been read.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -108,6 +110,114 @@ __device__ __forceinline__ void select_chunk(const RouteTcParams& p, uint32_t ta
         tmem_ld32(taddr + c, r);
         tmem_ld_wait();
         select_cols<K, 32, false>(p, r, nz, c, tok, s_bias, tv, te);
+    }
+}
+
+// ---- top-8 in two passes (k = 8)
+//
+// Pass 1 finds the token's 8th-largest logit theta with value-only sorting networks (a
+// comparator is one max and one min). Every expert of the top 8 then has a logit >= theta, and
+// any expert below theta has 8 larger ones, so pass 2 collects the experts with logit >= theta
+// (8 of them unless logits tie at theta) and sorts only those by (logit desc, id asc).
+//
+// A (logit, expert) pair as one 64-bit key whose unsigned order is the selection order: the
+// logit's bits mapped to an order-preserving integer in the high word, the complement of the
+// expert id in the low word (equal logits: the lower id has the larger key). Key 0 lies below
+// every real logit and marks an empty slot (expert -1). -0 is folded into +0 first so that
+// the two compare equal, as the logits do.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+    uint32_t u = __float_as_uint(v + 0.0f);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((uint64_t)u << 32) | (uint32_t)~e;
+}
+__device__ __forceinline__ float key_logit(uint64_t k) {
+    const uint32_t u = (uint32_t)(k >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+__device__ __forceinline__ int key_expert(uint64_t k) { return (int)~(uint32_t)k; }
+
+// comparators: a >= b afterwards
+__device__ __forceinline__ uint64_t vmax(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ float vmax(float a, float b) { return fmaxf(a, b); }
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+    const uint64_t hi = a > b ? a : b;
+    b = a > b ? b : a;
+    a = hi;
+}
+__device__ __forceinline__ void cas_desc(float& a, float& b) {
+    const float hi = fmaxf(a, b);
+    b = fminf(a, b);
+    a = hi;
+}
+
+// Batcher's odd-even merge sort of 8 values, descending (19 comparators in 6 layers).
+template <typename V>
+__device__ __forceinline__ void sort8_desc(V (&k)[8]) {
+    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
+    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
+    cas_desc(k[1], k[2]); cas_desc(k[5], k[6]);
+    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
+    cas_desc(k[2], k[4]); cas_desc(k[3], k[5]);
+    cas_desc(k[1], k[2]); cas_desc(k[3], k[4]); cas_desc(k[5], k[6]);
+}
+
+// The 8 largest of two descending lists, descending, into r: the pairwise maxima of r and the
+// reversed s form a bitonic sequence that holds them, and three half-cleaner layers sort it.
+template <typename V>
+__device__ __forceinline__ void merge8_desc(V (&r)[8], const V (&s)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = vmax(r[i], s[7 - i]);
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if ((i & d) == 0) cas_desc(r[i], r[i + d]);
+}
+
+// The routing logit of expert e for a token from its accumulator column: bias, then noise.
+// Both passes compute it with this one expression, so they see the same bits.
+template <bool NOISE>
+__device__ __forceinline__ float route_logit(const RouteTcParams& p, uint32_t acc, float nz, int e, int tok,
+                                             const float* s_bias) {
+    float v = __uint_as_float(acc) + s_bias[e];
+    if (NOISE && tok < p.T) v = fmaf(p.noise_std, nz, v);
+    return v;
+}
+
+// Accumulator columns c .. c + 15 of the thread's token, and their noise draws.
+__device__ __forceinline__ void load_cols16(const RouteTcParams& p, uint32_t taddr, int c, int tok,
+                                            uint32_t (&r)[16], float (&nz)[16]) {
+    if (p.noise) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            nz[i] = (tok < p.T && c + i < p.E) ? __ldg(p.noise + (size_t)(c + i) * p.T + tok) : 0.f;
+    }
+    tmem_ld16(taddr + c, r);
+    tmem_ld_wait();
+}
+
+// Pass 1 over experts c .. c + 15: their logits into the token's 8 largest values so far
+// (experts past E count as -inf), into its row of the staged logits s_v ([E][RBM]) and into
+// the logits output.
+template <bool NOISE>
+__device__ __forceinline__ void top8_values16(const RouteTcParams& p, const uint32_t (&r)[16], const float (&nz)[16],
+                                              int c, int tok, int row, const float* s_bias, float* s_v,
+                                              float (&top)[8]) {
+#pragma unroll
+    for (int g = 0; g < 16; g += 8) {
+        float k[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = c + g + i;
+            k[i] = -INFINITY;
+            if (e < p.E) {
+                k[i] = route_logit<NOISE>(p, r[g + i], nz[g + i], e, tok, s_bias);
+                s_v[e * RBM + row] = k[i];
+                if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = k[i];
+            }
+        }
+        sort8_desc(k);
+        merge8_desc(top, k);
     }
 }
 
@@ -289,6 +399,126 @@ route_tc_kernel(const RouteTcParams p, const __grid_constant__ CUtensorMap tmX,
                     }
                 }
             }
+        } else if constexpr (K == 8) {
+            // Shared memory over the operand ring, which the accumulator-full barrier has
+            // retired (the host checks that it holds these): the staged logits, the G groups'
+            // value lists, each token's 8 largest values, the experts in their slots and the
+            // count of logits at or above theta.
+            float* s_v = reinterpret_cast<float*>(smem);                   // [E][RBM]
+            float* s_f = s_v + (size_t)p.E * RBM;                          // [G][8][RBM]
+            float* s_top = s_f + (size_t)G * 8 * RBM;                      // [8][RBM]
+            int* s_e = reinterpret_cast<int*>(s_top + 8 * RBM);            // [8][RBM]
+            int* s_n = s_e + 8 * RBM;                                      // [RBM]
+            const int grp = (warp - 2) >> 2;
+            const bool live = tok < p.T;
+            const bool ok = mbar_wait(tfull, 0, p.err);
+            if (ok) tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+            // pass 1: the 8 largest logits of the group's chunks (chunks grp, grp + G, ...)
+            float top[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) top[j] = -INFINITY;
+            for (int c = 32 * grp; ok && c < p.E_pad; c += 32 * G) {
+#pragma unroll 1
+                for (int h = c; h < c + 32 && h < p.E; h += 16) {   // warp-uniform bounds
+                    uint32_t r[16];
+                    float nz[16];
+                    load_cols16(p, taddr, h, tok, r, nz);
+                    if (p.noise) top8_values16<true>(p, r, nz, h, tok, row, s_bias, s_v, top);
+                    else top8_values16<false>(p, r, nz, h, tok, row, s_bias, s_v, top);
+                }
+            }
+            // the G lists meet in a tree: odd groups hand theirs to the even group below, then
+            // group 2 to group 0, which then holds the token's 8 largest logits
+            if constexpr (G > 1) {
+                if (grp & 1) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s_f[((size_t)grp * 8 + j) * RBM + row] = top[j];
+                }
+                epilogue_bar_sync(128 * G);
+                if (!(grp & 1) && grp + 1 < G) {
+                    float o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = s_f[((size_t)(grp + 1) * 8 + j) * RBM + row];
+                    merge8_desc(top, o);
+                }
+                if constexpr (G > 2) {
+                    if (grp == 2) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) s_f[((size_t)2 * 8 + j) * RBM + row] = top[j];
+                    }
+                    epilogue_bar_sync(128 * G);
+                    if (grp == 0) {
+                        float o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) o[j] = s_f[((size_t)2 * 8 + j) * RBM + row];
+                        merge8_desc(top, o);
+                    }
+                }
+            }
+            if (grp == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s_top[j * RBM + row] = top[j];
+                s_n[row] = 0;
+            }
+            epilogue_bar_sync(128 * G);
+            // pass 2: each expert of the group with logit >= theta = the 8th value goes to slot
+            // (number of the 8 values above its logit). With distinct values and exactly 8 such
+            // experts that is the order (logit desc); anything else is a tie, found below.
+            if (live) {
+                float vt[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vt[j] = s_top[j * RBM + row];
+                for (int c = 32 * grp; ok && c < p.E_pad; c += 32 * G) {
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c + i < p.E && s_v[(c + i) * RBM + row] >= vt[7]) mask |= 1u << i;
+                    while (mask) {
+                        const int e = c + __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const float v = s_v[e * RBM + row];
+                        int slot = 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) slot += vt[j] > v ? 1 : 0;
+                        if (slot < 8) s_e[slot * RBM + row] = e;
+                        atomicAdd(s_n + row, 1);
+                    }
+                }
+            }
+            epilogue_bar_sync(128 * G);
+            if (grp == 0 && live) {
+                float tv[8];
+                int te[8];
+                bool tie = s_n[row] != 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    tv[j] = top[j];
+                    te[j] = s_e[j * RBM + row];
+                    if (j > 0 && top[j] == top[j - 1]) tie = true;
+                }
+                if (tie) {
+                    // equal logits in or at the edge of the top 8: the exact order over every
+                    // expert's (logit, id) key, from the staged logits
+                    uint64_t key[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) key[j] = 0;
+                    for (int c = 0; c < p.E; c += 8) {
+                        uint64_t k[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            k[i] = c + i < p.E ? sel_key(s_v[(c + i) * RBM + row], c + i) : 0;
+                        sort8_desc(k);
+                        merge8_desc(key, k);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        tv[j] = key[j] ? key_logit(key[j]) : -INFINITY;
+                        te[j] = key_expert(key[j]);
+                    }
+                }
+                route_finish<8>(p, tok, tv, te, s_cnt);
+            }
         } else {
             const int grp = (warp - 2) >> 2;
             float tv[K];
@@ -410,6 +640,9 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wg
     const size_t smem = 1024 + (size_t)p.stages * route_stage_bytes(p.E_pad) +
                         (2 * RMAX_STAGES + 4) * sizeof(uint64_t) + 16 + 2 * MOE_MAX_EXPERTS * sizeof(int);
     if (dense_routing(c)) return launch_k<0>(p, tx, tw, smem, s);
+    // the top-8 path's staging (logits, group lists, values, slots, counts) lies over the ring
+    const size_t top8_bytes = (size_t)RBM * 4 * ((size_t)c.E + 4 * 8 + 8 + 8 + 1);
+    if (c.k == 8 && top8_bytes > (size_t)p.stages * route_stage_bytes(p.E_pad)) return cudaErrorInvalidValue;
     switch (c.k) {
         case 1: return launch_k<1>(p, tx, tw, smem, s);
         case 2: return launch_k<2>(p, tx, tw, smem, s);
