@@ -171,8 +171,9 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, c
  * Limits: T <= MOE_NOALLOC_MAX_TOKENS and T*k <= MOE_NOALLOC_MAX_ASSIGNMENTS; larger
  * configurations return MOE_ERR_UNSUPPORTED (use moe_dispatch with a workspace). With
  * k = E (dense routing) no sort and no scratch are used and the limits do not apply.
- * The first call on a device looks up the array's device address (once per device); make
- * that first call before any stream capture. All calls share the one array: calls that
+ * Each call looks up the array's device address (a host lookup; the first one on a device
+ * may load the library's device code, so make a first call before any stream capture, as
+ * for every entry point). All calls share the one array: calls that
  * may overlap on the GPU (other streams, other host threads) race and must be serialised
  * by the caller. Nothing in the array needs to start at zero; each call writes what it
  * reads. */

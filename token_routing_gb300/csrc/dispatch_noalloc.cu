@@ -7,8 +7,6 @@
 // point takes no workspace argument. Its sort scratch is a fixed array in the library's
 // own device memory, reserved on every GPU that loads the library until the process
 // exits. The arithmetic is that of moe_dispatch (same kernels, same results).
-#include <mutex>
-
 #include "internal.cuh"
 
 namespace moe {
@@ -19,25 +17,11 @@ namespace {
 // device symbol: host code must use the address cudaGetSymbolAddress returns.
 static __device__ __align__(256) unsigned char g_dispatch_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDev = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDev] = {};
-
-// Device address of the scratch array on the current device, resolved once per device.
+// Device address of the scratch array on the current device, looked up on every call (a host
+// lookup, no device work): after a device reset the module is loaded again and the array may
+// sit elsewhere, so a cached address could point the sort at memory it does not own.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
-    return cudaSuccess;
+    return cudaGetSymbolAddress(out, g_dispatch_scratch);
 }
 
 }  // namespace
