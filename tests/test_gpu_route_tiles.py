@@ -11,13 +11,16 @@ import parity as P
 pytestmark = pytest.mark.gpu
 
 CASES = {
-    # one epilogue group (E <= 32)
+    # one epilogue group (E <= 32), three tiles per CTA
     "tiles-e16-k2": (synth.LayerConfig(name="tiles-e16-k2", T=40000, d=64, E=16, k=2, d_ff=64,
                                        capacity_factor=None), 0.0),
-    # four groups, a gate bias and routing noise
-    "tiles-e200-k3-noise": (synth.LayerConfig(name="tiles-e200-k3-noise", T=45000, d=128, E=200, k=3, d_ff=64,
+    # four groups, a gate bias and routing noise; two tiles per CTA, the last CTA one
+    "tiles-e200-k3-noise": (synth.LayerConfig(name="tiles-e200-k3-noise", T=36000, d=128, E=200, k=3, d_ff=64,
                                               capacity_factor=None, gate_bias="zipf", zipf_s=1.2,
                                               zipf_c=synth.configs.ZIPF_C_E64), 0.1),
+    # four tiles per CTA (both accumulators reused twice)
+    "tiles-e128-k4": (synth.LayerConfig(name="tiles-e128-k4", T=60000, d=64, E=128, k=4, d_ff=64,
+                                        capacity_factor=None), 0.0),
     # the top-8 path in several waves of one-tile CTAs
     "tiles-e64-k8": (synth.LayerConfig(name="tiles-e64-k8", T=40000, d=64, E=64, k=8, d_ff=64,
                                        capacity_factor=None, temperature=0.2), 0.0),
