@@ -1,9 +1,11 @@
 """Routing with more 128-token tiles than SMs: the top-k router (k < 8) then runs one CTA per
 SM over equal shares of smaller tiles, selecting over one tile while the next one loads, and
 the k = 8 router runs several waves of CTAs. Small d and many tokens keep the oracle fast.
-Indices are compared bit-exact on every token outside the near-tie set, weights to 1e-4."""
+Indices are compared bit-exact on every token outside the near-tie set, weights to 1e-4, and
+the optional logits output element by element."""
 import numpy as np
 import pytest
+import torch
 
 import synth
 import parity as P
@@ -38,8 +40,11 @@ def test_route_many_tiles(name, moe_lib, cuda_device):
     c = moe.config_from(cfg, noise_std=noise_std, noise_seed=1)
     dev = P.to_dev(inp)
     b = moe.alloc_buffers(c, backward=False)
-    moe.route(c, dev["x"], dev["Wg"], dev["bg"], b)
+    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device="cuda")
+    moe.route(c, dev["x"], dev["Wg"], dev["bg"], b, logits=logits)
     moe.get_error()
+    # the logits output (bias and noise included): fp32 sums of bf16 products against fp64
+    P.assert_close("logits", P.f64(logits), fwd["z"], 1e-5)
     idx = b["idx"].cpu().numpy()
     ok = P.nontie_tokens(fwd)
     assert ok.mean() > 0.99
