@@ -61,8 +61,10 @@ __device__ __forceinline__ void load_noise32(const float* __restrict__ noise, in
 }
 
 // N consecutive logits of a token (columns c .. c + N - 1 of its TMEM row: bias, optional
-// noise and logits output) inserted into its list sorted by (logit desc, id asc). Experts
-// arrive in ascending id, so an equal logit never displaces an earlier one.
+// noise and logits output) inserted into its list sorted by (logit desc, id asc). A new expert
+// (ids arrive in ascending order) never displaces an equal logit; once it has displaced an
+// entry, the rest of the list shifts down one slot (each pushed entry comes before the next in
+// that order, equal logits included).
 template <int K, int N, bool NOISE>
 __device__ __forceinline__ void select_cols(const RouteTcParams& p, const uint32_t (&r)[N], const float (&nz)[N],
                                             int c, int tok, const float* s_bias, float (&tv)[K], int (&te)[K]) {
@@ -73,13 +75,15 @@ __device__ __forceinline__ void select_cols(const RouteTcParams& p, const uint32
             float v = __uint_as_float(r[i]) + s_bias[e];
             if (NOISE && tok < p.T) v = fmaf(p.noise_std, nz[i], v);
             if (p.logits && tok < p.T) p.logits[(size_t)tok * p.E + e] = v;
+            bool moved = false;
 #pragma unroll
             for (int j = 0; j < K; ++j) {
-                if (te[j] < 0 || v > tv[j]) {
+                if (moved || te[j] < 0 || v > tv[j]) {
                     const float ov = tv[j];
                     const int oe = te[j];
                     tv[j] = v; te[j] = e;
                     v = ov; e = oe;
+                    moved = true;
                 }
             }
         }
